@@ -1,0 +1,294 @@
+"""FP64 CPU oracle for split-KV GQA attention over an INT8 (or FP16) KV cache.
+
+TEST INFRASTRUCTURE ONLY.  This module is the slow, plain reference that the
+CUDA path is checked against.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline / reference arm may import it; the product package
+``int8_kv_cache_gb300`` never does, and this module imports nothing from it.
+
+What is computed (all in float64, from the inputs exactly as a kernel receives
+them: fp16 queries, int8 codes, fp32 scales):
+
+1. Dequantisation.  ``x = scale * code`` with a per-tensor scale (one number)
+   or a per-channel scale indexed by (kv_head, channel).  An fp16 cache is
+   taken as is.  [onnxruntime PR 29912 "PagedAttention: quantized KV cache ...",
+   Schema (k_quant_type / v_quant_type = PER_TENSOR | PER_CHANNEL, k_scale /
+   v_scale) and CUDA kernels ("all read paths dequantize with k_scale/v_scale").]
+2. Gather.  Sparse candidates: the entries of a row's index list that lie in
+   [0, N), in list order, duplicates kept; other entries are invalid and
+   skipped [onnxruntime PR 33707, Summary of Changes §1 test sweep "x invalid
+   indices"].  Paged: token t of sequence b sits in physical row
+   ``block_table[b, t // bs] * bs + t % bs`` for t < min(seq_len, cap), with
+   cap = max_blocks * bs [PR 29912, CUDA kernels: block-table-aware decode;
+   capacity block_table.shape[1] * block_size].
+3. GQA.  Query head h reads KV head h // G, G = Hq / Hkv (contiguous groups).
+4. Softmax in the natural-log domain with max subtraction:
+   s_t = sigma * sum_d Q[h,d] K[t,d];  m = max_t s_t;  Z = sum_t exp(s_t - m);
+   O = sum_t exp(s_t - m) V_t / Z;  lse = m + ln Z
+   [PR 33707 §1: scores and running maximum stay in natural-log units; the
+   expected output is an FP64 reference with max-subtracted weights].
+5. Head sink (optional, one logit per query head, same units as the scaled
+   scores, no value row):  O <- O / (1 + exp(s_h - lse))  [PR 29912, CUDA
+   kernels, ApplyHeadSink: exact post-hoc LSE rescale].  The returned lse is
+   that of the attended candidates, without the sink.
+6. Split form.  Positions are partitioned into chunks; each chunk publishes an
+   un-normalised partial (m_k, l_k, a_k) with a_k = sum exp(s_t - m_k) V_t; an
+   empty chunk publishes (-inf, 0, 0).  The combine is
+   M = max m_k;  L = sum l_k e^(m_k - M);  O = sum a_k e^(m_k - M) / L;
+   lse = M + ln L, then the sink [PR 33707 §2: every CTA of the split-K decode
+   writes an un-normalized partial (running maximum, running sum, accumulator)
+   and a merge kernel combines them].
+
+An empty candidate set gives O = 0 and lse = -inf (reading: the pages do not
+say; a split with no tiles publishes an empty partial [PR 33707 §2 tests], and
+the whole-row case is taken the same way).
+"""
+from __future__ import annotations
+
+import math
+from typing import List, Optional, Sequence, Tuple
+
+import numpy as np
+
+SCALE_PER_TENSOR = 1
+SCALE_PER_CHANNEL = 2
+
+
+# --------------------------------------------------------------------------
+# 1. dequantisation
+# --------------------------------------------------------------------------
+
+def dequantize(codes: np.ndarray, scale: np.ndarray, scale_kind: int, kv_head: int) -> np.ndarray:
+    """Rows ``codes[..., D]`` of one KV head -> float64 values.
+
+    per-tensor: scale[0] * code;  per-channel: scale[kv_head, d] * code.
+    A float16 cache is returned as is (no scale).
+    """
+    x = np.asarray(codes).astype(np.float64)
+    if codes.dtype == np.float16:
+        return x
+    if scale_kind == SCALE_PER_TENSOR:
+        return x * float(np.asarray(scale, dtype=np.float64).reshape(-1)[0])
+    if scale_kind == SCALE_PER_CHANNEL:
+        return x * np.asarray(scale, dtype=np.float64)[kv_head]
+    raise ValueError(f"unknown scale kind {scale_kind}")
+
+
+# --------------------------------------------------------------------------
+# 4./5. one query head against a candidate set
+# --------------------------------------------------------------------------
+
+def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, sigma: float) -> Tuple[np.ndarray, float]:
+    """Softmax attention of one query vector ``q[D]`` over rows ``K[T, D]``,
+    ``V[T, D]`` (float64).  Returns (O[D], lse)."""
+    q = np.asarray(q, dtype=np.float64)
+    T = K.shape[0]
+    if T == 0:
+        return np.zeros(V.shape[1], dtype=np.float64), -math.inf
+    s = sigma * (K @ q)
+    m = float(np.max(s))
+    w = np.exp(s - m)
+    Z = float(np.sum(w))
+    o = (w @ V) / Z
+    return o, m + math.log(Z)
+
+
+def apply_head_sink(o: np.ndarray, lse: float, s_h: Optional[float]) -> np.ndarray:
+    """O <- O / (1 + exp(s_h - lse)); no sink leaves O unchanged.  With an empty
+    candidate set (lse = -inf) O is already zero and stays zero."""
+    if s_h is None or lse == -math.inf:
+        return o
+    return o / (1.0 + math.exp(float(s_h) - lse))
+
+
+def _sink_of(sink, h):
+    return None if sink is None else float(np.asarray(sink, dtype=np.float64)[h])
+
+
+# --------------------------------------------------------------------------
+# 2. gathers
+# --------------------------------------------------------------------------
+
+def sparse_candidates(idx_row: np.ndarray, N: int) -> np.ndarray:
+    """Valid entries of one candidate list, in list order, duplicates kept."""
+    r = np.asarray(idx_row, dtype=np.int64)
+    return r[(r >= 0) & (r < N)]
+
+
+def paged_slots(block_table: np.ndarray, seq_lens: np.ndarray, bs: int) -> np.ndarray:
+    """Physical row of every token position: ``out[b, t] = bt[b, t//bs]*bs + t%bs``
+    for t < min(seq_len_b, cap), else -1.  Shape [B, cap], int64."""
+    bt = np.asarray(block_table, dtype=np.int64)
+    B, mb = bt.shape
+    cap = mb * bs
+    out = np.full((B, cap), -1, dtype=np.int64)
+    for b in range(B):
+        L = live_length(int(seq_lens[b]), cap)
+        for t in range(L):
+            out[b, t] = bt[b, t // bs] * bs + t % bs
+    return out
+
+
+def live_length(seq_len: int, cap: int) -> int:
+    """A sequence's attended length: its seq_len clamped to [0, cap]."""
+    return max(0, min(int(seq_len), int(cap)))
+
+
+# --------------------------------------------------------------------------
+# whole-row references
+# --------------------------------------------------------------------------
+
+def sparse_attention(q, k_codes, v_codes, k_scale, v_scale, scale_kind, idx, sigma, sink=None):
+    """Sparse-candidate attention (decode rows or prefill rows alike).
+
+    q [S, Hq, D] fp16; caches [N, Hkv, D]; idx [S, max_sel].
+    Returns O [S, Hq, D] float64 and lse [S, Hq] float64.
+    """
+    S, Hq, D = q.shape
+    N, Hkv, _ = k_codes.shape
+    G = Hq // Hkv
+    O = np.zeros((S, Hq, D), dtype=np.float64)
+    L = np.full((S, Hq), -math.inf, dtype=np.float64)
+    for r in range(S):
+        rows = sparse_candidates(idx[r], N)
+        for g in range(Hkv):
+            K = dequantize(k_codes[rows, g, :], k_scale, scale_kind, g)
+            V = dequantize(v_codes[rows, g, :], v_scale, scale_kind, g)
+            for h in range(g * G, (g + 1) * G):
+                o, lse = attend(q[r, h].astype(np.float64), K, V, sigma)
+                O[r, h] = apply_head_sink(o, lse, _sink_of(sink, h))
+                L[r, h] = lse
+    return O, L
+
+
+def paged_attention(q, k_cache, v_cache, k_scale, v_scale, scale_kind, block_table, seq_lens,
+                    sigma, sink=None):
+    """Paged-cache decode: one query row per sequence.
+
+    q [B, Hq, D]; caches [num_blocks, bs, Hkv, D]; block_table [B, max_blocks].
+    Returns O [B, Hq, D], lse [B, Hq] (float64).
+    """
+    B, Hq, D = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    G = Hq // Hkv
+    kf = k_cache.reshape(nb * bs, Hkv, D)
+    vf = v_cache.reshape(nb * bs, Hkv, D)
+    slots = paged_slots(block_table, seq_lens, bs)
+    O = np.zeros((B, Hq, D), dtype=np.float64)
+    L = np.full((B, Hq), -math.inf, dtype=np.float64)
+    for b in range(B):
+        rows = slots[b][slots[b] >= 0]
+        for g in range(Hkv):
+            K = dequantize(kf[rows, g, :], k_scale, scale_kind, g)
+            V = dequantize(vf[rows, g, :], v_scale, scale_kind, g)
+            for h in range(g * G, (g + 1) * G):
+                o, lse = attend(q[b, h].astype(np.float64), K, V, sigma)
+                O[b, h] = apply_head_sink(o, lse, _sink_of(sink, h))
+                L[b, h] = lse
+    return O, L
+
+
+# --------------------------------------------------------------------------
+# 6. split form: partials and the log-sum-exp combine
+# --------------------------------------------------------------------------
+
+def partial(q: np.ndarray, K: np.ndarray, V: np.ndarray, sigma: float):
+    """Un-normalised partial of one chunk: (m, l, a) with a = sum e^(s-m) V.
+    An empty chunk gives (-inf, 0, 0)."""
+    D = V.shape[1]
+    if K.shape[0] == 0:
+        return -math.inf, 0.0, np.zeros(D, dtype=np.float64)
+    s = sigma * (K @ np.asarray(q, dtype=np.float64))
+    m = float(np.max(s))
+    w = np.exp(s - m)
+    return m, float(np.sum(w)), w @ V
+
+
+def combine(ms: Sequence[float], ls: Sequence[float], accs: Sequence[np.ndarray],
+            s_h: Optional[float] = None) -> Tuple[np.ndarray, float]:
+    """Log-sum-exp merge of split partials, then the head sink."""
+    ms = np.asarray(ms, dtype=np.float64)
+    D = len(accs[0]) if len(accs) else 0
+    live = np.isfinite(ms)
+    if not np.any(live):
+        return np.zeros(D, dtype=np.float64), -math.inf
+    M = float(np.max(ms[live]))
+    f = np.where(live, np.exp(np.where(live, ms - M, 0.0)), 0.0)
+    Lsum = float(np.sum(f * np.asarray(ls, dtype=np.float64)))
+    o = np.zeros(D, dtype=np.float64)
+    for k in range(len(accs)):
+        if live[k]:
+            o += f[k] * np.asarray(accs[k], dtype=np.float64)
+    o /= Lsum
+    lse = M + math.log(Lsum)
+    return apply_head_sink(o, lse, s_h), lse
+
+
+def chunk_bounds(length: int, chunk: int, num_splits: int) -> List[Tuple[int, int]]:
+    """Split k covers positions [k*chunk, (k+1)*chunk) intersected with [0, length)."""
+    out = []
+    for k in range(num_splits):
+        lo = min(k * chunk, length)
+        hi = min((k + 1) * chunk, length)
+        out.append((lo, hi))
+    return out
+
+
+def sparse_split_partials(q, k_codes, v_codes, k_scale, v_scale, scale_kind, idx, sigma,
+                          num_splits: int, chunk: int):
+    """Partials of the split form over list positions: split k of row r covers
+    list positions [k*chunk, (k+1)*chunk) of idx[r] (invalid entries skipped).
+
+    Returns m, l [S, Hq, splits] and acc [S, Hq, splits, D] (float64)."""
+    S, Hq, D = q.shape
+    N, Hkv, _ = k_codes.shape
+    G = Hq // Hkv
+    m = np.full((S, Hq, num_splits), -math.inf)
+    l = np.zeros((S, Hq, num_splits))
+    a = np.zeros((S, Hq, num_splits, D))
+    max_sel = idx.shape[1]
+    for r in range(S):
+        for k, (lo, hi) in enumerate(chunk_bounds(max_sel, chunk, num_splits)):
+            rows = sparse_candidates(idx[r, lo:hi], N)
+            for g in range(Hkv):
+                K = dequantize(k_codes[rows, g, :], k_scale, scale_kind, g)
+                V = dequantize(v_codes[rows, g, :], v_scale, scale_kind, g)
+                for h in range(g * G, (g + 1) * G):
+                    m[r, h, k], l[r, h, k], a[r, h, k] = partial(q[r, h], K, V, sigma)
+    return m, l, a
+
+
+def paged_split_partials(q, k_cache, v_cache, k_scale, v_scale, scale_kind, block_table,
+                         seq_lens, sigma, num_splits: int, chunk: int):
+    """Partials of the split form over token positions of each sequence."""
+    B, Hq, D = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    G = Hq // Hkv
+    kf = k_cache.reshape(nb * bs, Hkv, D)
+    vf = v_cache.reshape(nb * bs, Hkv, D)
+    slots = paged_slots(block_table, seq_lens, bs)
+    cap = slots.shape[1]
+    m = np.full((B, Hq, num_splits), -math.inf)
+    l = np.zeros((B, Hq, num_splits))
+    a = np.zeros((B, Hq, num_splits, D))
+    for b in range(B):
+        Lb = live_length(int(seq_lens[b]), cap)
+        for k, (lo, hi) in enumerate(chunk_bounds(Lb, chunk, num_splits)):
+            rows = slots[b, lo:hi]
+            for g in range(Hkv):
+                K = dequantize(kf[rows, g, :], k_scale, scale_kind, g)
+                V = dequantize(vf[rows, g, :], v_scale, scale_kind, g)
+                for h in range(g * G, (g + 1) * G):
+                    m[b, h, k], l[b, h, k], a[b, h, k] = partial(q[b, h], K, V, sigma)
+    return m, l, a
+
+
+def combine_all(m, l, a, sink=None):
+    """Combine partials [R, Hq, splits(, D)] row by row -> O [R, Hq, D], lse [R, Hq]."""
+    R, Hq, ns = m.shape
+    D = a.shape[-1]
+    O = np.zeros((R, Hq, D))
+    L = np.full((R, Hq), -math.inf)
+    for r in range(R):
+        for h in range(Hq):
+            O[r, h], L[r, h] = combine(m[r, h], l[r, h], list(a[r, h]), _sink_of(sink, h))
+    return O, L
