@@ -1,0 +1,542 @@
+#!/usr/bin/env python3
+"""Benchmark of the INT8 split-KV decode path on GB300.
+
+Headline workload: sparse-candidate INT8 decode, S = 8 query rows, 24 query /
+2 KV heads, head_dim 256, a 16384-token INT8 cache with per-channel scales,
+2048 sorted unique candidates per row, softmax scale 1/16 (the shapes the
+onnxruntime PR 33707 page measures).  One step is one decode pass over L
+layers, each with its own cache, query rows and candidate lists (L = 32 by
+default: 537 MB of caches, more than three times the L2), captured as one
+CUDA graph of L dsa_decode calls (decode kernel + combine kernel each).
+
+value = algorithmic bytes of all calls / device time (GB/s, whole job).  The
+algorithmic bytes of one call are the gathered K and V rows, the query, the
+index lists, the scales and the output; split-workspace traffic is not
+counted.  The JSON line also carries us_per_call, the decode kernel's roofline
+(its bytes / its own CUDA-event time from a graph of partials-only launches),
+an end-to-end figure through the public API with host buffers, the FP64
+oracle's CPU time, the SM clocks seen during the timed region, and the paged
+decode, deep-context and prefill workloads measured the same way.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 run under torch.distributed.run: every rank decodes its own layers
+(weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+S_ROWS, HQ, HKV, D, N_CACHE, N_SEL, SIGMA = 8, 24, 2, 256, 16384, 2048, 1.0 / 16.0
+WORKLOAD = ("sparse-candidate INT8 decode: S=8 rows, 24 query / 2 KV heads, head_dim 256, "
+            "16384-token int8 cache per layer with per-channel scales, 2048 sorted unique "
+            "candidates per row, softmax scale 1/16")
+# H200 attention time incl. merge for this workload (onnxruntime PR 33707, Performance, 8 rows)
+H200_US_PER_CALL = 13.2
+
+
+def call_bytes(S=S_ROWS, Hq=HQ, Hkv=HKV, Dh=D, n_sel=N_SEL):
+    kv = S * Hkv * n_sel * Dh * 2
+    return dict(kv=kv, q=S * Hq * Dh * 2, idx=S * n_sel * 4, scales=2 * Hkv * Dh * 4,
+                out=S * Hq * Dh * 2)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and the reference arm)
+# --------------------------------------------------------------------------
+
+def cpu_worker(spec: str):
+    """Runs in a child process with single-threaded BLAS: time the FP64 oracle
+    on whole calls of the headline workload until `budget` seconds passed."""
+    import numpy as np  # noqa: F401
+    import oracle
+    import workloads as W
+    a = json.loads(spec)
+    c = W.sparse_decode(S_ROWS, seed=a["seed"])
+    t0 = time.perf_counter()
+    calls = 0
+    while True:
+        oracle.sparse_attention(c.q, c.k_codes, c.v_codes, c.k_scale, c.v_scale, c.scale_kind,
+                                c.idx, c.sigma)
+        calls += 1
+        if time.perf_counter() - t0 >= a["budget"] or calls >= a["max_calls"]:
+            break
+    dt = time.perf_counter() - t0
+    print(json.dumps(dict(calls=calls, seconds=dt)))
+
+
+def run_cpu_oracle(budget_s: float, max_calls: int = 1000000, seed: int = 0):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    spec = json.dumps(dict(budget=budget_s, max_calls=max_calls, seed=seed))
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", spec],
+                       capture_output=True, text=True, env=env, cwd=ROOT)
+    if r.returncode != 0:
+        raise RuntimeError(f"cpu oracle worker failed: {r.stderr[-2000:]}")
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    b = sum(call_bytes().values())
+    gbs = res["calls"] * b / res["seconds"] / 1e9
+    return dict(value=gbs, unit="GB/s", cores=1, kind="oracle", calls=res["calls"],
+                seconds=res["seconds"], seconds_per_call=res["seconds"] / res["calls"],
+                sample=f"{res['calls']} whole call(s) of the headline workload (one layer, S=8 "
+                       f"rows x 24 heads x 2048 candidates), FP64 NumPy oracle, single-threaded "
+                       f"BLAS, {res['seconds']:.1f} s")
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.idx = gpu_index
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, start: bool):
+        if start:
+            self.t_start = time.time()
+        else:
+            self.t_stop = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [ln.split(",") for ln in out.strip().splitlines() if ln.count(",") >= 8]
+        if not rows:
+            return None
+
+        def when(r):
+            try:
+                import datetime
+                return datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return None
+        inside = [r for r in rows if when(r) is not None and self.t_start is not None
+                  and self.t_start <= when(r) <= (self.t_stop or 1e30)]
+        window = "timed region" if inside else "around the timed region"
+        rows = inside or rows
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].strip().lower() == "active"})
+        return dict(sm_mhz=statistics.median(sm) if sm else None,
+                    sm_max_mhz=max(mx) if mx else None, reasons=reasons, samples=len(rows),
+                    window=window)
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+def kernel_sources_digest():
+    h = hashlib.sha256()
+    for f in ("decode_kernel.cuh", "device.cuh"):
+        with open(os.path.join(ROOT, "int8_kv_cache_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(name: str):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, or None
+    when the kernel source changed since the capture."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            d = json.load(f)
+    except OSError:
+        return None
+    e = d.get(name)
+    if not e or e.get("kernel_digest") != kernel_sources_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def time_graph(torch, graph, replays: int, stream):
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def capture(torch, fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # eager once (also sets kernel attributes) before capture
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def gpu_arm(args, rank, world, local_rank, dist):
+    import numpy as np
+    import torch
+
+    import int8_kv_cache_gb300 as K
+    import workloads as W
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream()
+    props = torch.cuda.get_device_properties(dev)
+    peaks, peak_src = measured_peaks()
+    l2 = int(getattr(props, "L2_cache_size", 0) or 0)
+    L = args.layers
+
+    # ---- inputs: L layers, each its own cache / rows / lists (seeded) ----
+    layers = []
+    for li in range(L):
+        c = W.sparse_decode(S_ROWS, seed=1000 * rank + li)
+        t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+        layers.append(dict(q=t(c.q), k=t(c.k_codes), v=t(c.v_codes), ks=t(c.k_scale),
+                           vs=t(c.v_scale), idx=t(c.idx), case=c if li == 0 else None,
+                           out=torch.empty((S_ROWS, HQ, D), dtype=torch.float16, device=dev)))
+    working_set = sum(x["k"].numel() + x["v"].numel() for x in layers)
+    ns, chunk, wsb, wave = K.decode_plan(K.PATH_DSA, K.CACHE_INT8, N_SEL, S_ROWS, HQ, HKV, D,
+                                         K.GEOM_POW2_TILES)
+    ws = torch.empty(max(wsb // 4, 4), dtype=torch.float32, device=dev)
+    kind = W.SCALE_PER_CHANNEL
+
+    def step():
+        for x in layers:
+            K.dsa_decode(x["q"], x["k"], x["v"], x["ks"], x["vs"], kind, x["idx"], SIGMA,
+                         num_splits=ns, chunk=chunk, workspace=ws, out=x["out"])
+
+    def step_partials():
+        for x in layers:
+            K.dsa_decode(x["q"], x["k"], x["v"], x["ks"], x["vs"], kind, x["idx"], SIGMA,
+                         num_splits=ns, chunk=chunk, workspace=ws, partials_only=True)
+
+    g = capture(torch, step, stream)
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            g.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark(True)
+    t = time_graph(torch, g, args.steps, stream)
+    clocks.mark(False)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    if dist is not None:
+        tt = torch.tensor([t], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+
+    b = call_bytes()
+    bytes_call = sum(b.values())
+    calls = args.steps * L * world
+    value = calls * bytes_call / t / 1e9
+    us_per_call = t / (args.steps * L) * 1e6
+    launches = args.steps * L * (2 if ns > 1 else 1)
+
+    # ---- the decode kernel alone: graph of partials-only launches ----
+    gp = capture(torch, step_partials, stream)
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            gp.replay()
+    reps = max(20, min(args.steps, 500))
+    tp = time_graph(torch, gp, reps, stream)
+    t_kernel = tp / (reps * L)
+    kernel_bytes = b["kv"] + b["q"] + b["idx"] + b["scales"]
+    achieved = kernel_bytes / t_kernel / 1e9
+    traffic = ncu_traffic("dsa_decode_S8")
+
+    # ---- end to end through the public API with host buffers ----
+    hq = [x["q"].cpu().pin_memory() for x in layers]
+    hidx = [x["idx"].cpu().pin_memory() for x in layers]
+    hout = [torch.empty((S_ROWS, HQ, D), dtype=torch.float16).pin_memory() for _ in layers]
+    e2e_steps = max(3, min(args.steps, 100))
+
+    def e2e_step():
+        for i, x in enumerate(layers):
+            x["q"].copy_(hq[i], non_blocking=True)
+            x["idx"].copy_(hidx[i], non_blocking=True)
+            K.dsa_decode(x["q"], x["k"], x["v"], x["ks"], x["vs"], kind, x["idx"], SIGMA,
+                         num_splits=ns, chunk=chunk, workspace=ws, out=x["out"])
+            hout[i].copy_(x["out"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        s1.record(stream)
+    s1.synchronize()
+    te = s0.elapsed_time(s1) / 1e3
+    if dist is not None:
+        tt = torch.tensor([te], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        te = float(tt.item())
+    e2e = dict(value=e2e_steps * L * world * bytes_call / te / 1e9, unit="GB/s",
+               h2d_bytes_per_step=L * (b["q"] + b["idx"]), d2h_bytes_per_step=L * b["out"],
+               us_per_call=te / (e2e_steps * L) * 1e6, steps=e2e_steps,
+               note="per step: pinned-host copies of every layer's query rows and lists, the "
+                    "dsa_decode calls of the Python binding, the output copied back")
+
+    out = {
+        "metric": "INT8 split-KV decode us/call and achieved HBM GB/s (% of GB300 peak)",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 5),
+        "us_per_call": round(us_per_call, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": round(H200_US_PER_CALL / us_per_call, 3),
+        "vs_baseline_basis": "H200 attention time incl. merge for 8 rows, 13.2 us/call "
+                             "(onnxruntime PR 33707, Performance; another machine: context)",
+        "dtype": "int8 KV, fp16 MMA, fp32 accumulate", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers_per_step": L, "calls_per_step": L,
+                   "num_splits": ns, "chunk": chunk, "wave_ctas": wave,
+                   "geometry": "power-of-two tiles rule", "bytes_per_call": bytes_call,
+                   "l2_policy": f"inputs larger than L2: {working_set / 1e6:.0f} MB of caches "
+                                f"over the step vs L2 {l2 / 1e6:.0f} MB",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "gpu_launches": launches,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "kernel": "decode_kernel<256,2,sparse,int8,hi+lo>",
+                     "us_per_launch": round(t_kernel * 1e6, 3),
+                     "bytes_per_launch": kernel_bytes, "peak_source": f"{peak_src} hbm_gbs"},
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if not args.no_extra:
+        out["other_configs"] = extra_configs(torch, K, W, np, dev, stream, peaks, args)
+    return out
+
+
+def extra_configs(torch, K, W, np, dev, stream, peaks, args):
+    """Paged decode, deep-context split sweep and prefill, each as a CUDA graph
+    of R calls over R distinct input copies (working set > L2 where the
+    workload allows)."""
+    res = {}
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    hbm = peaks["hbm_gbs"]
+
+    def bench_graph(fn, R, reps=50):
+        g = capture(torch, fn, stream)
+        for _ in range(3):
+            with torch.cuda.stream(stream):
+                g.replay()
+        return time_graph(torch, g, reps, stream) / (reps * R)
+
+    # ---- paged decode: 16 sequences, lengths U[512, 8192], 32/8 heads, D 128 ----
+    c = W.paged_decode(seed=0)
+    B, Hq, Dh = c.q.shape
+    nb, bs, Hkv, _ = c.k_cache.shape
+    cap = c.block_table.shape[1] * bs
+    R = 3
+    copies = [dict(k=t(c.k_cache), v=t(c.v_cache)) for _ in range(R)]
+    q, ks, vs = t(c.q), t(c.k_scale), t(c.v_scale)
+    bt, lens, sink = t(c.block_table), t(c.seq_lens), t(c.sink)
+    ns, chunk, wsb, wave = K.decode_plan(K.PATH_PAGED, K.CACHE_INT8, cap, B, Hq, Hkv, Dh,
+                                         K.GEOM_WAVE)
+    ws = torch.empty(max(wsb // 4, 4), dtype=torch.float32, device=dev)
+    out = torch.empty_like(q)
+    tokens = int(c.seq_lens.sum())
+    byts = tokens * Hkv * Dh * 2 + B * Hq * Dh * 4 + int(np.ceil(c.seq_lens / bs).sum()) * 4 \
+        + 2 * Hkv * Dh * 4
+
+    def fn():
+        for x in copies:
+            K.paged_decode(q, x["k"], x["v"], ks, vs, c.scale_kind, bt, lens, c.sigma, sink,
+                           num_splits=ns, chunk=chunk, workspace=ws, out=out)
+    sec = bench_graph(fn, R)
+    res["paged_decode"] = dict(
+        workload="paged INT8 decode: 16 sequences, lengths U[512,8192] (sum %d), block 16, "
+                 "permuted block table, 32/8 heads, head_dim 128, per-channel scales, sink"
+                 % tokens,
+        us_per_call=round(sec * 1e6, 2), gbs=round(byts / sec / 1e9, 1),
+        frac_of_hbm=round(byts / sec / 1e9 / hbm, 4), bytes_per_call=byts, num_splits=ns,
+        chunk=chunk, rotating_copies=R)
+    del copies
+
+    # ---- deep-context split sweep: 16 rows, cap 4096, live 2600, 16/2 heads ----
+    for cache in ("int8", "fp16"):
+        c = W.deep_context(seed=0, cache=cache)
+        B, Hq, Dh = c.q.shape
+        nb, bs, Hkv, _ = c.k_cache.shape
+        esz = 1 if cache == "int8" else 2
+        R = 20 if cache == "int8" else 10
+        copies = [dict(k=t(c.k_cache), v=t(c.v_cache)) for _ in range(R)]
+        q, ks, vs, bt, lens = t(c.q), t(c.k_scale), t(c.v_scale), t(c.block_table), t(c.seq_lens)
+        byts = B * 2600 * Hkv * Dh * 2 * esz + B * Hq * Dh * 4 + B * (2600 // 16 + 1) * 4
+        dt = K.CACHE_INT8 if cache == "int8" else K.CACHE_FP16
+        row = {}
+        for label, ovr in (("adaptive", 0), ("chunk128", 128), ("chunk256", 256),
+                           ("chunk512", 512)):
+            ns, chunk, wsb, wave = K.decode_plan(K.PATH_PAGED, dt, 4096, B, Hq, Hkv, Dh,
+                                                 K.GEOM_WAVE, ovr)
+            ws = torch.empty(max(wsb // 4, 4), dtype=torch.float32, device=dev)
+            out = torch.empty_like(q)
+
+            def fn():
+                for x in copies:
+                    K.paged_decode(q, x["k"], x["v"], ks, vs, c.scale_kind, bt, lens, c.sigma,
+                                   num_splits=ns, chunk=chunk, workspace=ws, out=out)
+            sec = bench_graph(fn, R, reps=100)
+            row[label] = dict(us_per_call=round(sec * 1e6, 2), gbs=round(byts / sec / 1e9, 1),
+                              frac_of_hbm=round(byts / sec / 1e9 / hbm, 4), num_splits=ns,
+                              chunk=chunk)
+        res[f"deep_context_{cache}"] = dict(
+            workload=f"deep context: 16 rows, {cache} cache, live 2600 of cap 4096, 16/2 heads, "
+                     "head_dim 128", bytes_per_call=byts, rotating_copies=R, **row)
+        del copies
+
+    # ---- sparse prefill: 2048 rows over an 8192-token cache, 24/2 heads, D 256 ----
+    c = W.sparse_prefill(seed=0)
+    d = dict(q=t(c.q), k=t(c.k_codes), v=t(c.v_codes), ks=t(c.k_scale), vs=t(c.v_scale),
+             idx=t(c.idx))
+    out = torch.empty_like(d["q"])
+
+    def fn():
+        K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"], c.sigma,
+                      out=out)
+    sec = bench_graph(fn, 1, reps=10)
+    n_att = int((c.idx >= 0).sum())
+    flops = n_att * 24 * 256 * 4
+    gathered = n_att * 2 * 256 * 2
+    peak_tf = peaks["bf16_tflops"]
+    res["sparse_prefill"] = dict(
+        workload="sparse prefill: 2048 rows at positions 6144+i over an 8192-token int8 cache, "
+                 "2048 candidates per row, 24/2 heads, head_dim 256",
+        ms_per_call=round(sec * 1e3, 4), tflops=round(flops / sec / 1e12, 2),
+        frac_of_tensor=round(flops / sec / 1e12 / peak_tf, 4), tensor_peak=peak_tf,
+        gathered_gbs=round(gathered / sec / 1e9, 1), flops_per_call=flops)
+    return res
+
+
+def reference_arm(args, rank, world):
+    """The FP64 oracle on the host cores, each step a bounded sample (whole
+    calls of the headline workload for about args-determined seconds)."""
+    if rank != 0:
+        return None
+    per_step = max(0.5, min(10.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        run_cpu_oracle(per_step, max_calls=1)
+    tot_s, tot_calls = 0.0, 0
+    for _ in range(args.steps):
+        r = run_cpu_oracle(per_step)
+        tot_s += r["seconds"]
+        tot_calls += r["calls"]
+    b = sum(call_bytes().values())
+    v = tot_calls * b / tot_s / 1e9
+    sample = (f"{tot_calls} whole call(s) of the headline workload over {args.steps} step(s), "
+              "FP64 NumPy oracle, single-threaded BLAS")
+    return {"metric": "INT8 split-KV decode us/call and achieved HBM GB/s (% of GB300 peak)",
+            "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": tot_s / args.steps * 1e3,
+            "us_per_call": tot_s / tot_calls * 1e6, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD}, "impl": "reference",
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    if args.cpu_worker is not None:
+        cpu_worker(args.cpu_worker)
+        return
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        res = reference_arm(args, rank, world)
+        if res is not None:
+            print(json.dumps(res))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        dist = tdist
+    res = gpu_arm(args, rank, world, local_rank, dist)
+    if rank == 0:
+        try:
+            res["cpu_baseline"] = None if args.no_cpu_baseline else run_cpu_oracle(10.0)
+        except Exception as e:  # the GPU figure stands without it
+            res["cpu_baseline"] = {"error": str(e)[:300]}
+        print(json.dumps(res))
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

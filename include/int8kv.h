@@ -1,0 +1,260 @@
+/*
+ * int8kv.h -- C ABI of libint8kv.so: split-KV GQA decode attention over an
+ * INT8-quantized KV cache on GB300 (sm_103a).
+ *
+ * The operation (all entry points below compute parts of it):
+ *   For each query row r and query head h, with KV head g = h / G and
+ *   G = Hq / Hkv (contiguous GQA groups):
+ *     K_t = k_scale * code_K[t, g, :]   V_t = v_scale * code_V[t, g, :]
+ *         (per-tensor scale: one number; per-channel: scale[g, d])
+ *     s_t = softmax_scale * dot(Q[r, h, :], K_t)       (natural-log units)
+ *     O[r, h, :] = sum_t exp(s_t - m) V_t / sum_t exp(s_t - m),  m = max_t s_t
+ *     lse[r, h]  = m + ln sum_t exp(s_t - m)
+ *     optional head sink s_h:  O <- O / (1 + exp(s_h - lse))
+ *   over the candidate set of the row: the valid entries of a sparse index
+ *   list (onnxruntime PR 33707 "INT8-KV DynamicSparseAttention", Summary of
+ *   Changes §1-§2) or the first min(seq_len, cap) tokens of a paged
+ *   block-table cache (onnxruntime PR 29912 "PagedAttention: quantized KV
+ *   cache ...", CUDA kernels: paged decode, ApplyHeadSink).  The decode calls
+ *   split each row's candidates into chunks, run an online softmax per chunk
+ *   and merge the partials with a log-sum-exp combine (PR 33707 §2); the split
+ *   count comes from the capacity and the row count only (onnx-genai PR 1350
+ *   "adaptive split-KV sizing", Summary).
+ *
+ * Conventions shared by every entry point
+ *   - Device pointers are CUDA device addresses of the current device.  The
+ *     caller owns every buffer; the library allocates nothing, never
+ *     synchronises the host and enqueues work only on `stream` (a
+ *     cudaStream_t passed as void*; NULL = the legacy default stream).
+ *   - fp16 tensors are passed as uint16_t* (IEEE binary16 bit patterns).
+ *   - Layouts are dense row-major with the shapes given per argument.
+ *   - Alignment: q, out, caches and per-channel scales must be 16-byte
+ *     aligned; index lists, block tables, lengths, lse, sinks and flags
+ *     4-byte aligned; the workspace 16-byte aligned.
+ *   - Argument errors are reported by the return value before anything is
+ *     enqueued.  A launch failure returns I8KV_ECUDA.  Data-dependent
+ *     conditions found on the device are OR-ed into the optional `flags`
+ *     word (I8KV_FLAG_*) and never stop the kernel.
+ *   - Every call with the same shapes and geometry enqueues the same
+ *     kernels with the same launch configuration, so calls can be captured
+ *     in a CUDA graph; live lengths are read on the device.
+ */
+#ifndef INT8KV_H_
+#define INT8KV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+typedef enum {
+  I8KV_OK = 0,
+  I8KV_EINVAL = 1,        /* bad argument: NULL required pointer, negative size, bad enum,
+                             non-finite or negative softmax scale, geometry that misses the cap */
+  I8KV_EUNSUPPORTED = 2,  /* valid but not served: head_dim not 64/128/256, G > 16,
+                             softmax_scale > 1, block_size not a multiple of 16, ... */
+  I8KV_EALIGN = 3,        /* a pointer breaks the alignment rule above */
+  I8KV_EWORKSPACE = 4,    /* workspace NULL or smaller than split_workspace_bytes() */
+  I8KV_ECUDA = 5          /* a CUDA runtime call or kernel launch failed */
+} i8kv_status;
+
+/* ---- enumerations ------------------------------------------------------- */
+#define I8KV_SCALE_PER_TENSOR 1  /* k_scale / v_scale: one float                 */
+#define I8KV_SCALE_PER_CHANNEL 2 /* k_scale / v_scale: float [Hkv, D]             */
+
+#define I8KV_CACHE_INT8 1 /* codes in [-128, 127], dequantised with the scales */
+#define I8KV_CACHE_FP16 2 /* paged_decode only: values taken as is, scales ignored */
+
+#define I8KV_GEOM_WAVE 0       /* onnx-genai PR 1350 rule (num_splits from one wave)        */
+#define I8KV_GEOM_POW2_TILES 1 /* onnxruntime PR 33707 rule (power-of-two tiles per split)  */
+
+#define I8KV_PATH_DSA 1   /* sparse-candidate decode kernel */
+#define I8KV_PATH_PAGED 2 /* paged decode kernel            */
+
+#define I8KV_MAX_SPLITS 32 /* at most 32 splits (onnxruntime PR 33707, §2) */
+
+/* bits OR-ed into the optional device `flags` word */
+#define I8KV_FLAG_LEN_CLAMPED 0x1u /* a seq_len was > cap (clamped) or < 0 (taken as 0)       */
+#define I8KV_FLAG_QUERY_RANGE 0x2u /* some Q*k_scale is not finite or beyond +-65504: the FP16
+                                      query of that CTA is not exact to the stated bound      */
+#define I8KV_FLAG_BAD_BLOCK 0x4u   /* a block-table entry inside the live length is outside
+                                      [0, num_blocks): those tokens were skipped              */
+
+/* Human-readable name of a status code (static storage). */
+const char* i8kv_status_string(int status);
+
+/* Library ABI version (major*100 + minor). */
+int32_t i8kv_version(void);
+
+/* The cudaError_t value behind the calling thread's most recent I8KV_ECUDA
+ * (0 if there was none). */
+int32_t i8kv_last_cuda_error(void);
+
+/*
+ * split_geometry -- pure host integer arithmetic, no CUDA call.
+ *
+ * Chooses the number of splits and the chunk length (in candidates or tokens)
+ * from the capacity `cap` (list length or max_blocks*block_size) and the number
+ * of independent work units `units` (rows x KV heads), never from a live length.
+ *   mode I8KV_GEOM_WAVE (onnx-genai PR 1350, Summary):
+ *     n = min(ceil(wave_ctas / units), ceil(cap / min_chunk), max_splits);
+ *     chunk = ceil(cap / n) rounded up to a multiple of `granule`;
+ *     n = ceil(cap / chunk).  override_value > 0 pins the chunk instead:
+ *     n = min(ceil(cap / override_value), max_splits), then as above.
+ *   mode I8KV_GEOM_POW2_TILES (onnxruntime PR 33707, §2): tiles = ceil(cap /
+ *     granule); tiles_per_split = smallest power of two with
+ *     ceil(tiles / tps) * units <= wave_ctas (override_value > 0: that tps as a
+ *     target); n = min(ceil(tiles / tps), max_splits); tiles_eff = ceil(tiles /
+ *     n); n = ceil(tiles / tiles_eff); chunk = tiles_eff * granule.
+ *   cap <= 0 gives n = 1, chunk = granule.
+ * Outputs: *num_splits in [1, max_splits], *chunk a multiple of granule with
+ * num_splits * chunk >= cap and (num_splits - 1) * chunk < cap.
+ * Errors: I8KV_EINVAL for units, wave_ctas, granule, min_chunk or max_splits < 1,
+ * override_value < 0, an unknown mode or NULL outputs.
+ */
+i8kv_status split_geometry(int64_t cap, int32_t units, int32_t wave_ctas, int32_t granule,
+                           int32_t min_chunk, int32_t max_splits, int32_t mode,
+                           int32_t override_value, int32_t* num_splits, int32_t* chunk);
+
+/*
+ * split_workspace_bytes -- bytes of the split workspace for `units` work units
+ * of G query heads of dimension D and `num_splits` splits.  Layout (fp32):
+ *   acc [units, num_splits, G, D]   un-normalised partial outputs, value-scaled
+ *   m   [units, num_splits, G]      running maximum (natural log)
+ *   l   [units, num_splits, G]      running sum of exp(s - m)
+ * The partial vectors come first so that they stay 16-byte aligned
+ * (onnxruntime PR 33707, §2).  Returns 0 for num_splits <= 1 or bad sizes.
+ */
+size_t split_workspace_bytes(int32_t units, int32_t num_splits, int32_t G, int32_t D);
+
+/*
+ * decode_plan -- the geometry a decode call uses when it is given
+ * num_splits = 0 (automatic), for the current device.
+ *   path: I8KV_PATH_DSA or I8KV_PATH_PAGED; cache_dtype: I8KV_CACHE_INT8 or
+ *   I8KV_CACHE_FP16 (paged only); cap: max_sel (DSA) or max_blocks*block_size
+ *   (paged); rows: S (DSA) or B (paged); mode / override_value as in
+ *   split_geometry.  wave_ctas = SM count x resident CTAs per SM of the
+ *   selected decode kernel (queried from the CUDA occupancy API and cached per
+ *   device); granule = 64 (POW2_TILES) or 16 (WAVE); min_chunk = 128;
+ *   max_splits = I8KV_MAX_SPLITS.
+ * Outputs: *num_splits, *chunk, *workspace_bytes (0 when one split), and, if
+ * wave_ctas is not NULL, the wave used.  Errors as for the decode calls'
+ * shape checks, I8KV_ECUDA if the device cannot be queried.
+ */
+i8kv_status decode_plan(int32_t path, int32_t cache_dtype, int64_t cap, int32_t rows,
+                        int32_t Hq, int32_t Hkv, int32_t D, int32_t mode,
+                        int32_t override_value, int32_t* num_splits, int32_t* chunk,
+                        size_t* workspace_bytes, int32_t* wave_ctas);
+
+/*
+ * dsa_decode -- sparse-candidate decode (onnxruntime PR 33707, Summary of
+ * Changes §2: split-K decode over a per-row candidate list of an INT8 cache).
+ *   q        [S, Hq, D] fp16                 query rows
+ *   k_cache  [N, Hkv, D] int8, v_cache same  the main cache (token-major)
+ *   k_scale, v_scale, scale_kind             fp32 [1] or [Hkv, D]
+ *   idx      [S, max_sel] int32              row r attends the entries of
+ *            idx[r, :] that lie in [0, N), in list order, duplicates counted;
+ *            any other value is skipped (padding: -1)
+ *   softmax_scale                            sigma, 0 <= sigma <= 1 (the FP16
+ *            query / probability path is bounded for sigma <= 1: PR 33707 §1)
+ *   head_sink [Hq] fp32 or NULL              per-head sink logit (PR 29912)
+ *   num_splits, chunk                        geometry: split k of row r covers
+ *            list positions [k*chunk, (k+1)*chunk); requires num_splits in
+ *            [1, 32], chunk > 0 and a multiple of 16, num_splits*chunk >=
+ *            max_sel.  num_splits = 0: automatic (decode_plan, POW2_TILES rule,
+ *            chunk ignored).
+ *   workspace, workspace_bytes               >= split_workspace_bytes(S*Hkv,
+ *            num_splits, G, D) when num_splits > 1 (may be NULL otherwise)
+ *   out      [S, Hq, D] fp16                 output.  NULL with num_splits > 1:
+ *            write the split partials to the workspace only and enqueue no
+ *            combine (the caller runs split_combine later, e.g. after gathering
+ *            partials of one row computed on several devices)
+ *   lse      [S, Hq] fp32 or NULL            log-sum-exp of the attended scores
+ *            (without the sink); -inf for an empty candidate set (O = 0)
+ *   flags    device uint32 or NULL           I8KV_FLAG_* bits are OR-ed in
+ * Work: one kernel over (S*Hkv units) x num_splits CTAs writing partials, then
+ * the split_combine kernel; with one split the decode kernel writes O directly.
+ * S = 0 or max_sel = 0 enqueues nothing for S = 0 and writes O = 0, lse = -inf
+ * for max_sel = 0.
+ */
+i8kv_status dsa_decode(const uint16_t* q, const int8_t* k_cache, const int8_t* v_cache,
+                       const float* k_scale, const float* v_scale, int32_t scale_kind,
+                       const int32_t* idx, int32_t S, int32_t Hq, int32_t Hkv, int32_t D,
+                       int64_t N, int32_t max_sel, float softmax_scale, const float* head_sink,
+                       int32_t num_splits, int32_t chunk, void* workspace,
+                       size_t workspace_bytes, uint16_t* out, float* lse, uint32_t* flags,
+                       void* stream);
+
+/*
+ * dsa_prefill -- the tensor-core multi-row variant over gathered candidates
+ * (onnxruntime PR 33707, Summary of Changes §1: grid (rows, KV heads), no
+ * splits, the probability tile as a single FP16 tile).  Arguments as for
+ * dsa_decode without the geometry and the workspace; any S >= 0.
+ */
+i8kv_status dsa_prefill(const uint16_t* q, const int8_t* k_cache, const int8_t* v_cache,
+                        const float* k_scale, const float* v_scale, int32_t scale_kind,
+                        const int32_t* idx, int32_t S, int32_t Hq, int32_t Hkv, int32_t D,
+                        int64_t N, int32_t max_sel, float softmax_scale,
+                        const float* head_sink, uint16_t* out, float* lse, uint32_t* flags,
+                        void* stream);
+
+/*
+ * paged_decode -- split-KV decode over a paged block-table cache
+ * (onnxruntime PR 29912, CUDA kernels: "split-KV, block-table-aware decode
+ * with native head-sink ... and on-the-fly cache dequantization").
+ *   q            [B, Hq, D] fp16              one query row per sequence
+ *   k_cache, v_cache [num_blocks, block_size, Hkv, D] int8 or fp16
+ *   cache_dtype  I8KV_CACHE_INT8 or I8KV_CACHE_FP16 (scales ignored, may be NULL)
+ *   block_table  [B, max_blocks] int32        token t of sequence b is row
+ *                block_table[b, t / block_size] * block_size + t % block_size
+ *   seq_lens     [B] int32, DEVICE memory     live lengths, clamped to
+ *                cap = max_blocks * block_size (I8KV_FLAG_LEN_CLAMPED)
+ *   block_size   a multiple of 16
+ *   num_splits, chunk  as for dsa_decode over token positions, with cap =
+ *                max_blocks*block_size; num_splits = 0: automatic (WAVE rule)
+ *   slots_out    [B, cap] int32 or NULL       debug output: the gathered row of
+ *                every token position, -1 past the live length
+ *   other arguments as for dsa_decode.
+ */
+i8kv_status paged_decode(const uint16_t* q, const void* k_cache, const void* v_cache,
+                         int32_t cache_dtype, const float* k_scale, const float* v_scale,
+                         int32_t scale_kind, const int32_t* block_table,
+                         const int32_t* seq_lens, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                         int32_t block_size, int32_t max_blocks, int64_t num_blocks,
+                         float softmax_scale, const float* head_sink, int32_t num_splits,
+                         int32_t chunk, void* workspace, size_t workspace_bytes, uint16_t* out,
+                         float* lse, int32_t* slots_out, uint32_t* flags, void* stream);
+
+/*
+ * split_combine -- log-sum-exp merge of split partials plus the head sink
+ * (onnxruntime PR 33707 §2: the merge kernel; PR 29912: ApplyHeadSink):
+ *   M = max_k m_k;  L = sum_k l_k exp(m_k - M);  O = sum_k acc_k exp(m_k - M) / L
+ *   lse = M + ln L;  O <- O / (1 + exp(s_h - lse)) if a sink is given.
+ * Splits with m_k = -inf are skipped (their acc is not read); all skipped:
+ * O = 0, lse = -inf.
+ *   acc [units, num_splits, G, D], m, l [units, num_splits, G] fp32 (the
+ *   workspace layout of split_workspace_bytes); unit u = row * Hkv + g;
+ *   G = Hq / Hkv; out [units*G, D] fp16 (= [rows, Hq, D]); lse [units*G] or
+ *   NULL; head_sink [Hq] or NULL, indexed by h = (u % Hkv) * G + j.
+ *   num_splits in [1, 32]; D in {64, 128, 256}.
+ */
+i8kv_status split_combine(const float* acc, const float* m, const float* l, int32_t units,
+                          int32_t num_splits, int32_t Hq, int32_t Hkv, int32_t D,
+                          const float* head_sink, uint16_t* out, float* lse, void* stream);
+
+/*
+ * int8_to_fp16 -- the decode kernels' in-register int8 -> fp16 conversion
+ * applied to a buffer (byte permutes into the mantissa of 1024 + 128, then one
+ * fp16x2 subtraction of 1152: exact for all 256 codes; onnxruntime PR 29912,
+ * "int8->fp16 conversion fast path").  in [n] int8, out [n] fp16, n a multiple
+ * of 4, both 16-byte aligned.  For tests of the conversion.
+ */
+i8kv_status int8_to_fp16(const int8_t* in, uint16_t* out, int64_t n, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* INT8KV_H_ */

@@ -1,0 +1,260 @@
+"""Python binding of ``libint8kv.so``: split-KV GQA decode attention over an
+INT8-quantized KV cache on GB300.
+
+Every function here has the name and the meaning of the C entry point of the
+same name in ``include/int8kv.h``.  The binding only marshals arguments: it
+reads shapes from the tensors, checks dtype / device / contiguity, passes raw
+device pointers and the current CUDA stream, and turns a non-zero status into
+an exception.  All computation runs in the library's CUDA kernels; there is
+no fallback.  PyTorch provides device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "Int8KVError", "load", "library_path", "split_geometry", "split_workspace_bytes",
+    "decode_plan", "dsa_decode", "dsa_prefill", "paged_decode", "split_combine", "int8_to_fp16",
+    "SCALE_PER_TENSOR", "SCALE_PER_CHANNEL", "CACHE_INT8", "CACHE_FP16", "GEOM_WAVE",
+    "GEOM_POW2_TILES", "PATH_DSA", "PATH_PAGED", "MAX_SPLITS", "FLAG_LEN_CLAMPED",
+    "FLAG_QUERY_RANGE", "FLAG_BAD_BLOCK",
+]
+
+SCALE_PER_TENSOR = 1
+SCALE_PER_CHANNEL = 2
+CACHE_INT8 = 1
+CACHE_FP16 = 2
+GEOM_WAVE = 0
+GEOM_POW2_TILES = 1
+PATH_DSA = 1
+PATH_PAGED = 2
+MAX_SPLITS = 32
+FLAG_LEN_CLAMPED = 0x1
+FLAG_QUERY_RANGE = 0x2
+FLAG_BAD_BLOCK = 0x4
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB: Optional[ctypes.CDLL] = None
+
+_c_i32, _c_i64, _c_f32, _c_sz, _c_vp = (ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                                        ctypes.c_size_t, ctypes.c_void_p)
+_P_I32 = ctypes.POINTER(ctypes.c_int32)
+_P_SZ = ctypes.POINTER(ctypes.c_size_t)
+
+_SIGNATURES = {
+    "i8kv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "i8kv_version": (_c_i32, []),
+    "i8kv_last_cuda_error": (_c_i32, []),
+    "split_geometry": (_c_i32, [_c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                                _P_I32, _P_I32]),
+    "split_workspace_bytes": (_c_sz, [_c_i32, _c_i32, _c_i32, _c_i32]),
+    "decode_plan": (_c_i32, [_c_i32, _c_i32, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                             _c_i32, _P_I32, _P_I32, _P_SZ, _P_I32]),
+    "dsa_decode": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i32, _c_vp, _c_i32, _c_i32,
+                            _c_i32, _c_i32, _c_i64, _c_i32, _c_f32, _c_vp, _c_i32, _c_i32, _c_vp,
+                            _c_sz, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "dsa_prefill": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i32, _c_vp, _c_i32, _c_i32,
+                             _c_i32, _c_i32, _c_i64, _c_i32, _c_f32, _c_vp, _c_vp, _c_vp, _c_vp,
+                             _c_vp]),
+    "paged_decode": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_i32, _c_vp, _c_vp, _c_i32, _c_vp, _c_vp,
+                              _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_f32,
+                              _c_vp, _c_i32, _c_i32, _c_vp, _c_sz, _c_vp, _c_vp, _c_vp, _c_vp,
+                              _c_vp]),
+    "split_combine": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                               _c_vp, _c_vp, _c_vp, _c_vp]),
+    "int8_to_fp16": (_c_i32, [_c_vp, _c_vp, _c_i64, _c_vp]),
+}
+
+
+class Int8KVError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        self.status = status
+        msg = f"{fn}: {load().i8kv_status_string(status).decode()} (status {status})"
+        if detail:
+            msg += f"; {detail}"
+        super().__init__(msg)
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libint8kv.so")
+
+
+def load() -> ctypes.CDLL:
+    """Load the in-tree library (build it with ``__graft_entry__.build()``)."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build the CUDA library first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        detail = ""
+        if status == 5:
+            detail = f"cudaError {load().i8kv_last_cuda_error()}"
+        raise Int8KVError(fn, status, detail)
+
+
+def _t(x: Optional[torch.Tensor], dtype, name: str, device=None) -> Optional[int]:
+    """Device pointer of a contiguous CUDA tensor of the given dtype (None -> NULL)."""
+    if x is None:
+        return None
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if dtype is not None and x.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name}: expected {dtype}, got {x.dtype}")
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+# --------------------------------------------------------------------------
+# host-only calls
+# --------------------------------------------------------------------------
+
+def split_geometry(cap: int, units: int, wave_ctas: int, granule: int, min_chunk: int,
+                   max_splits: int, mode: int, override_value: int = 0):
+    """(num_splits, chunk) -- pure host integer arithmetic in the library."""
+    n, c = ctypes.c_int32(), ctypes.c_int32()
+    _check("split_geometry", load().split_geometry(cap, units, wave_ctas, granule, min_chunk,
+                                                   max_splits, mode, override_value,
+                                                   ctypes.byref(n), ctypes.byref(c)))
+    return n.value, c.value
+
+
+def split_workspace_bytes(units: int, num_splits: int, G: int, D: int) -> int:
+    return int(load().split_workspace_bytes(units, num_splits, G, D))
+
+
+def decode_plan(path: int, cache_dtype: int, cap: int, rows: int, Hq: int, Hkv: int, D: int,
+                mode: int, override_value: int = 0):
+    """(num_splits, chunk, workspace_bytes, wave_ctas) on the current device."""
+    n, c, w = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    ws = ctypes.c_size_t()
+    _check("decode_plan", load().decode_plan(path, cache_dtype, cap, rows, Hq, Hkv, D, mode,
+                                             override_value, ctypes.byref(n), ctypes.byref(c),
+                                             ctypes.byref(ws), ctypes.byref(w)))
+    return n.value, c.value, int(ws.value), w.value
+
+
+# --------------------------------------------------------------------------
+# device calls
+# --------------------------------------------------------------------------
+
+def dsa_decode(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, idx,
+               softmax_scale: float, head_sink=None, num_splits: int = 0, chunk: int = 0,
+               workspace=None, out=None, lse=None, flags=None, stream=None,
+               partials_only: bool = False):
+    """Sparse-candidate decode.  q [S, Hq, D] fp16; caches [N, Hkv, D] int8;
+    idx [S, max_sel] int32.  Returns ``out`` ([S, Hq, D] fp16).  With
+    ``partials_only`` (and num_splits > 1) only the workspace partials are
+    written (out is NULL at the C ABI) and None is returned."""
+    S, Hq, D = q.shape
+    N, Hkv, _ = k_cache.shape
+    max_sel = idx.shape[1]
+    if out is None and not partials_only:
+        out = torch.empty_like(q)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("dsa_decode", load().dsa_decode(
+        _t(q, torch.float16, "q"), _t(k_cache, torch.int8, "k_cache"),
+        _t(v_cache, torch.int8, "v_cache"), _t(k_scale, torch.float32, "k_scale"),
+        _t(v_scale, torch.float32, "v_scale"), scale_kind, _t(idx, torch.int32, "idx"), S, Hq,
+        Hkv, D, N, max_sel, softmax_scale, _t(head_sink, torch.float32, "head_sink"), num_splits,
+        chunk, _t(workspace, None, "workspace"), ws_bytes, _t(out, torch.float16, "out"),
+        _t(lse, torch.float32, "lse"), _t(flags, torch.int32, "flags"), _stream(stream)))
+    return out
+
+
+def dsa_prefill(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, idx,
+                softmax_scale: float, head_sink=None, out=None, lse=None, flags=None,
+                stream=None):
+    """Sparse-candidate prefill (tensor-core path, no splits)."""
+    S, Hq, D = q.shape
+    N, Hkv, _ = k_cache.shape
+    max_sel = idx.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _check("dsa_prefill", load().dsa_prefill(
+        _t(q, torch.float16, "q"), _t(k_cache, torch.int8, "k_cache"),
+        _t(v_cache, torch.int8, "v_cache"), _t(k_scale, torch.float32, "k_scale"),
+        _t(v_scale, torch.float32, "v_scale"), scale_kind, _t(idx, torch.int32, "idx"), S, Hq,
+        Hkv, D, N, max_sel, softmax_scale, _t(head_sink, torch.float32, "head_sink"),
+        _t(out, torch.float16, "out"), _t(lse, torch.float32, "lse"),
+        _t(flags, torch.int32, "flags"), _stream(stream)))
+    return out
+
+
+def paged_decode(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, block_table, seq_lens,
+                 softmax_scale: float, head_sink=None, num_splits: int = 0, chunk: int = 0,
+                 workspace=None, out=None, lse=None, slots_out=None, flags=None, stream=None):
+    """Paged decode.  q [B, Hq, D] fp16; caches [num_blocks, block_size, Hkv, D]
+    int8 or fp16; block_table [B, max_blocks] int32; seq_lens [B] int32 (device)."""
+    B, Hq, D = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    max_blocks = block_table.shape[1]
+    if k_cache.dtype == torch.int8:
+        cache_dtype = CACHE_INT8
+    elif k_cache.dtype == torch.float16:
+        cache_dtype = CACHE_FP16
+    else:
+        raise TypeError(f"k_cache: int8 or float16 expected, got {k_cache.dtype}")
+    if out is None:
+        out = torch.empty_like(q)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("paged_decode", load().paged_decode(
+        _t(q, torch.float16, "q"), _t(k_cache, k_cache.dtype, "k_cache"),
+        _t(v_cache, k_cache.dtype, "v_cache"), cache_dtype, _t(k_scale, torch.float32, "k_scale"),
+        _t(v_scale, torch.float32, "v_scale"), scale_kind,
+        _t(block_table, torch.int32, "block_table"), _t(seq_lens, torch.int32, "seq_lens"), B,
+        Hq, Hkv, D, bs, max_blocks, nb, softmax_scale, _t(head_sink, torch.float32, "head_sink"),
+        num_splits, chunk, _t(workspace, None, "workspace"), ws_bytes,
+        _t(out, torch.float16, "out"), _t(lse, torch.float32, "lse"),
+        _t(slots_out, torch.int32, "slots_out"), _t(flags, torch.int32, "flags"),
+        _stream(stream)))
+    return out
+
+
+def split_combine(acc, m, l, Hq: int, Hkv: int, head_sink=None, out=None, lse=None,
+                  stream=None):
+    """Combine partials acc [units, splits, G, D], m, l [units, splits, G] (fp32)."""
+    units, ns, G, D = acc.shape
+    if out is None:
+        out = torch.empty((units * G, D), dtype=torch.float16, device=acc.device)
+    _check("split_combine", load().split_combine(
+        _t(acc, torch.float32, "acc"), _t(m, torch.float32, "m"), _t(l, torch.float32, "l"),
+        units, ns, Hq, Hkv, D, _t(head_sink, torch.float32, "head_sink"),
+        _t(out, torch.float16, "out"), _t(lse, torch.float32, "lse"), _stream(stream)))
+    return out
+
+
+def int8_to_fp16(x, out=None, stream=None):
+    """The decode kernels' int8 -> fp16 conversion over a buffer (n % 4 == 0)."""
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float16, device=x.device)
+    _check("int8_to_fp16", load().int8_to_fp16(_t(x, torch.int8, "x"),
+                                               _t(out, torch.float16, "out"), x.numel(),
+                                               _stream(stream)))
+    return out

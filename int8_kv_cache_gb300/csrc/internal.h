@@ -1,0 +1,67 @@
+// Host-side interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace i8kv {
+
+enum class Path : int { kDsa = 1, kPaged = 2 };
+
+struct DecodeParams {
+  const void* q;             // fp16 [rows, Hq, D]
+  const void* k;             // cache base (int8 or fp16)
+  const void* v;
+  const float* k_scale;      // [1] or [Hkv, D]; unused for an fp16 cache
+  const float* v_scale;
+  const int32_t* idx;        // DSA: [rows, max_sel]
+  const int32_t* block_table;  // paged: [rows, max_blocks]
+  const int32_t* seq_lens;     // paged: [rows]
+  const float* sink;         // [Hq] or nullptr
+  void* out;                 // fp16 [rows, Hq, D]
+  float* lse;                // [rows, Hq] or nullptr
+  float* ws_acc;             // [units, splits, G, D]
+  float* ws_m;               // [units, splits, G]
+  float* ws_l;               // [units, splits, G]
+  int32_t* slots_out;        // paged debug [rows, cap] or nullptr
+  uint32_t* flags;           // or nullptr
+  int64_t cache_rows;        // DSA: N; paged: num_blocks (in blocks)
+  int32_t rows, Hq, Hkv, G;
+  int32_t max_sel;           // DSA list length (cap)
+  int32_t bs, max_blocks;    // paged
+  int32_t num_splits, chunk;
+  int32_t per_channel;       // 1: scales [Hkv, D]; 0: one scale
+  float sigma;
+};
+
+struct KernelKey {
+  Path path;
+  int D;
+  int nt;          // 8-head tiles: 1 (G <= 8) or 2 (G <= 16)
+  bool fp16_cache;
+  bool p_lo;       // probability tile as fp16 high + low parts
+};
+
+// Launch one decode / prefill kernel: grid (rows * Hkv, num_splits), 128 threads.
+cudaError_t launch_decode(const KernelKey& key, const DecodeParams& p, cudaStream_t stream);
+
+// Resident CTAs per SM of that kernel (occupancy API), or -1 if no such kernel.
+int decode_occupancy(const KernelKey& key);
+
+// Per-path launchers (one per translation unit).
+cudaError_t launch_dsa_decode(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
+                              int* occupancy);
+cudaError_t launch_dsa_prefill(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
+                               int* occupancy);
+cudaError_t launch_paged_int8(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
+                              int* occupancy);
+cudaError_t launch_paged_fp16(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
+                              int* occupancy);
+
+cudaError_t launch_combine(const float* acc, const float* m, const float* l, int units,
+                           int num_splits, int Hq, int Hkv, int D, const float* sink, void* out,
+                           float* lse, cudaStream_t stream);
+cudaError_t launch_int8_to_fp16(const int8_t* in, uint16_t* out, int64_t n, cudaStream_t stream);
+
+}  // namespace i8kv

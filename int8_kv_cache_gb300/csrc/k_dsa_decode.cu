@@ -1,0 +1,9 @@
+// Instantiations of the decode kernel: DSA sparse-candidate decode (probability tile as fp16 high + low parts).
+#include "decode_kernel.cuh"
+
+namespace i8kv {
+cudaError_t launch_dsa_decode(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
+                           int* occupancy) {
+  return dispatch_decode<false, false, true>(key, p, s, occupancy);
+}
+}  // namespace i8kv

@@ -1,0 +1,148 @@
+"""The C ABI without a GPU: the library builds and loads, exports every symbol
+that include/int8kv.h declares, its host-only geometry is bit-exact with the
+oracle, and argument errors come back as status codes before any CUDA call."""
+import ctypes
+import itertools
+import os
+import re
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import int8_kv_cache_gb300 as K
+    if not os.path.exists(K.library_path()):
+        from int8_kv_cache_gb300 import build
+        build.build()
+    return K.load()
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "int8kv.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*"
+                                 r"([A-Za-z_][A-Za-z0-9_]*)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_five_calls():
+    names = _declared_functions()
+    for n in ["dsa_decode", "dsa_prefill", "paged_decode", "split_combine", "split_geometry"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.i8kv_version() >= 100
+    assert lib.i8kv_status_string(0) == b"ok"
+    assert lib.i8kv_status_string(4).startswith(b"workspace")
+
+
+def test_geometry_bit_exact_with_oracle(lib):
+    import int8_kv_cache_gb300 as K
+    caps = [0, 1, 16, 17, 64, 65, 127, 128, 129, 509, 520, 2048, 2112, 2600, 4096, 8192, 32768]
+    for cap, units, wave, mode, ov in itertools.product(
+            caps, [1, 2, 8, 16, 32, 128, 4096], [1, 152, 216, 304, 396, 512, 608, 1216],
+            [oracle.MODE_WAVE, oracle.MODE_POW2_TILES], [0, 1, 2, 3, 128, 256, 512]):
+        granule = 64 if mode == oracle.MODE_POW2_TILES else 16
+        want = oracle.split_geometry(cap, units, wave, granule, 128, 32, mode, ov)
+        got = K.split_geometry(cap, units, wave, granule, 128, 32, mode, ov)
+        assert got == want, (cap, units, wave, mode, ov)
+
+
+def test_geometry_printed_examples_through_the_abi(golden_dir):
+    import json
+    import int8_kv_cache_gb300 as K
+    with open(os.path.join(golden_dir, "geometry_examples.json")) as f:
+        for c in json.load(f)["cases"]:
+            a = c["args"]
+            n, chunk = K.split_geometry(a["cap"], a["units"], a["wave"], a["granule"],
+                                        a["min_chunk"], a["max_splits"], a["mode"], a["override"])
+            assert (n, chunk) == (c["expect"]["num_splits"], c["expect"]["chunk"]), c["name"]
+
+
+def test_geometry_rejects_bad_arguments(lib):
+    n, c = ctypes.c_int32(), ctypes.c_int32()
+    assert lib.split_geometry(100, 0, 10, 1, 1, 32, 0, 0, ctypes.byref(n), ctypes.byref(c)) == 1
+    assert lib.split_geometry(100, 1, 10, 1, 1, 32, 9, 0, ctypes.byref(n), ctypes.byref(c)) == 1
+    assert lib.split_geometry(100, 1, 10, 1, 1, 32, 0, -1, ctypes.byref(n), ctypes.byref(c)) == 1
+    assert lib.split_geometry(100, 1, 10, 1, 1, 32, 0, 0, None, ctypes.byref(c)) == 1
+
+
+def test_workspace_bytes(lib):
+    assert lib.split_workspace_bytes(16, 1, 12, 256) == 0
+    assert lib.split_workspace_bytes(16, 16, 12, 256) == 16 * 16 * 12 * (256 + 2) * 4
+    assert lib.split_workspace_bytes(0, 4, 4, 64) == 0
+
+
+# fake, aligned, never-dereferenced device addresses: every call below must be
+# rejected by host validation before any CUDA call
+P = 0x10000
+P8 = 0x10008
+
+
+def _dsa(lib, **kw):
+    a = dict(q=P, k=P, v=P, ks=P, vs=P, kind=2, idx=P, S=1, Hq=8, Hkv=2, D=128, N=100, max_sel=64,
+             sigma=0.1, sink=None, ns=1, chunk=64, ws=None, wsb=0, out=P, lse=None, flags=None,
+             stream=None)
+    a.update(kw)
+    return lib.dsa_decode(a["q"], a["k"], a["v"], a["ks"], a["vs"], a["kind"], a["idx"], a["S"],
+                          a["Hq"], a["Hkv"], a["D"], a["N"], a["max_sel"], a["sigma"], a["sink"],
+                          a["ns"], a["chunk"], a["ws"], a["wsb"], a["out"], a["lse"], a["flags"],
+                          a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=96), 2), (dict(Hq=9), 1), (dict(Hq=36, Hkv=2), 2), (dict(sigma=2.0), 2),
+    (dict(sigma=float("nan")), 1), (dict(sigma=-0.5), 1), (dict(kind=3), 1), (dict(ks=None), 1),
+    (dict(q=None), 1), (dict(idx=None), 1), (dict(q=P8), 3), (dict(out=P8), 3),
+    (dict(ns=33, chunk=16), 1), (dict(ns=1, chunk=48), 1), (dict(ns=1, chunk=24), 1),
+    (dict(ns=2, chunk=64), 4), (dict(S=-1), 1), (dict(max_sel=-3), 1),
+])
+def test_dsa_decode_validation(lib, kw, status):
+    assert _dsa(lib, **kw) == status
+
+
+def test_paged_decode_validation(lib):
+    def call(**kw):
+        a = dict(q=P, k=P, v=P, dt=1, ks=P, vs=P, kind=1, bt=P, lens=P, B=2, Hq=4, Hkv=1, D=64,
+                 bs=16, mb=8, nb=20, sigma=0.125, sink=None, ns=1, chunk=128, ws=None, wsb=0,
+                 out=P, lse=None, slots=None, flags=None, stream=None)
+        a.update(kw)
+        return lib.paged_decode(a["q"], a["k"], a["v"], a["dt"], a["ks"], a["vs"], a["kind"],
+                                a["bt"], a["lens"], a["B"], a["Hq"], a["Hkv"], a["D"], a["bs"],
+                                a["mb"], a["nb"], a["sigma"], a["sink"], a["ns"], a["chunk"],
+                                a["ws"], a["wsb"], a["out"], a["lse"], a["slots"], a["flags"],
+                                a["stream"])
+    assert call(bs=8) == 2
+    assert call(bs=24) == 2
+    assert call(dt=3) == 1
+    assert call(lens=None) == 1
+    assert call(ks=None) == 1
+    assert call(dt=2, ks=None, vs=None, ns=2, chunk=64) == 4  # fp16 cache needs no scales
+    assert call(ns=1, chunk=64) == 1  # 1 x 64 < cap 128
+    assert call(sigma=1.5) == 2
+
+
+def test_combine_and_convert_validation(lib):
+    assert lib.split_combine(P, P, P, 4, 0, 8, 2, 128, None, P, None, None) == 1
+    assert lib.split_combine(P, P, P, 4, 33, 8, 2, 128, None, P, None, None) == 1
+    assert lib.split_combine(P, P, P, 4, 4, 8, 2, 100, None, P, None, None) == 2
+    assert lib.int8_to_fp16(P, P, 6, None) == 1
+    assert lib.int8_to_fp16(P8, P, 8, None) == 3
+
+
+def test_zero_work_is_a_no_op(lib):
+    # S = 0 / B = 0 / units = 0: validated, nothing enqueued, OK without a GPU
+    assert _dsa(lib, S=0) == 0
+    assert lib.split_combine(P, P, P, 0, 4, 8, 2, 128, None, P, None, None) == 0
+    assert lib.int8_to_fp16(P, P, 0, None) == 0
