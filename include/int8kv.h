@@ -246,6 +246,39 @@ i8kv_status split_combine(const float* acc, const float* m, const float* l, int3
                           const float* head_sink, uint16_t* out, float* lse, void* stream);
 
 /*
+ * dsa_decode_static_workspace -- dsa_decode without a caller-supplied
+ * workspace, for callers that cannot allocate device memory when they call
+ * (an engine's enqueue step that must not allocate, code with no access to the
+ * application's allocator, loops that must never enter the allocator).  The
+ * pages have no counterpart; this is a convenience of this library.
+ *   Arguments and results as for dsa_decode, without workspace and
+ *   workspace_bytes.  The split partials go to a device array inside the
+ *   library of I8KV_STATIC_WORKSPACE_BYTES bytes, allocated when CUDA loads the
+ *   library's device code on a device and held on every such device until the
+ *   process exits.  Nothing is allocated or freed by the call itself.
+ *   - A geometry whose partials need more than I8KV_STATIC_WORKSPACE_BYTES
+ *     (split_workspace_bytes(S*Hkv, num_splits, G, D)) returns
+ *     I8KV_EWORKSPACE before anything is enqueued.
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *     first call before any stream capture.
+ *   - All calls on a device share the one array.  Calls whose kernels can run
+ *     at the same time on the GPU (different streams without ordering between
+ *     them) race on it and give wrong results; calls ordered on one stream are
+ *     fine.  Nothing in it needs clearing between calls: each call writes every
+ *     entry it reads back.
+ */
+#define I8KV_STATIC_WORKSPACE_BYTES (4u * 1024u * 1024u)
+i8kv_status dsa_decode_static_workspace(const uint16_t* q, const int8_t* k_cache,
+                                        const int8_t* v_cache, const float* k_scale,
+                                        const float* v_scale, int32_t scale_kind,
+                                        const int32_t* idx, int32_t S, int32_t Hq, int32_t Hkv,
+                                        int32_t D, int64_t N, int32_t max_sel,
+                                        float softmax_scale, const float* head_sink,
+                                        int32_t num_splits, int32_t chunk, uint16_t* out,
+                                        float* lse, uint32_t* flags, void* stream);
+
+/*
  * int8_to_fp16 -- the decode kernels' in-register int8 -> fp16 conversion
  * applied to a buffer (byte permutes into the mantissa of 1024 + 128, then one
  * fp16x2 subtraction of 1152: exact for all 256 codes; onnxruntime PR 29912,

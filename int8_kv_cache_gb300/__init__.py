@@ -19,6 +19,7 @@ import torch
 __all__ = [
     "Int8KVError", "load", "library_path", "split_geometry", "split_workspace_bytes",
     "decode_plan", "dsa_decode", "dsa_prefill", "paged_decode", "split_combine", "int8_to_fp16",
+    "dsa_decode_static_workspace", "STATIC_WORKSPACE_BYTES",
     "SCALE_PER_TENSOR", "SCALE_PER_CHANNEL", "CACHE_INT8", "CACHE_FP16", "GEOM_WAVE",
     "GEOM_POW2_TILES", "PATH_DSA", "PATH_PAGED", "MAX_SPLITS", "FLAG_LEN_CLAMPED",
     "FLAG_QUERY_RANGE", "FLAG_BAD_BLOCK",
@@ -36,6 +37,7 @@ MAX_SPLITS = 32
 FLAG_LEN_CLAMPED = 0x1
 FLAG_QUERY_RANGE = 0x2
 FLAG_BAD_BLOCK = 0x4
+STATIC_WORKSPACE_BYTES = 4 * 1024 * 1024
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB: Optional[ctypes.CDLL] = None
@@ -67,6 +69,10 @@ _SIGNATURES = {
     "split_combine": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                _c_vp, _c_vp, _c_vp, _c_vp]),
     "int8_to_fp16": (_c_i32, [_c_vp, _c_vp, _c_i64, _c_vp]),
+    "dsa_decode_static_workspace": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i32, _c_vp,
+                                             _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_i32,
+                                             _c_f32, _c_vp, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp,
+                                             _c_vp]),
 }
 
 
@@ -257,4 +263,26 @@ def int8_to_fp16(x, out=None, stream=None):
     _check("int8_to_fp16", load().int8_to_fp16(_t(x, torch.int8, "x"),
                                                _t(out, torch.float16, "out"), x.numel(),
                                                _stream(stream)))
+    return out
+
+
+def dsa_decode_static_workspace(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, idx,
+                                softmax_scale: float, head_sink=None, num_splits: int = 0,
+                                chunk: int = 0, out=None, lse=None, flags=None, stream=None):
+    """dsa_decode with the split partials in the library's own fixed device
+    array (STATIC_WORKSPACE_BYTES), for callers that cannot allocate scratch
+    memory when they call; calls that may run concurrently on the GPU must not
+    use it (they share the array)."""
+    S, Hq, D = q.shape
+    N, Hkv, _ = k_cache.shape
+    max_sel = idx.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _check("dsa_decode_static_workspace", load().dsa_decode_static_workspace(
+        _t(q, torch.float16, "q"), _t(k_cache, torch.int8, "k_cache"),
+        _t(v_cache, torch.int8, "v_cache"), _t(k_scale, torch.float32, "k_scale"),
+        _t(v_scale, torch.float32, "v_scale"), scale_kind, _t(idx, torch.int32, "idx"), S, Hq,
+        Hkv, D, N, max_sel, softmax_scale, _t(head_sink, torch.float32, "head_sink"), num_splits,
+        chunk, _t(out, torch.float16, "out"), _t(lse, torch.float32, "lse"),
+        _t(flags, torch.int32, "flags"), _stream(stream)))
     return out
