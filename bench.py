@@ -59,7 +59,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--layers", type=int, default=32)
-    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--extra", default="all", choices=["all", "paged", "deep", "prefill", "none"],
+                    help="which other workloads to measure besides the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -371,7 +372,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
         "clocks": clk,
         "e2e": e2e,
     }
-    if not args.no_extra:
+    if args.extra != "none":
         out["other_configs"] = extra_configs(torch, K, W, np, dev, stream, peaks, args)
     return out
 
@@ -391,7 +392,18 @@ def extra_configs(torch, K, W, np, dev, stream, peaks, args):
                 g.replay()
         return time_graph(torch, g, reps, stream) / (reps * R)
 
-    # ---- paged decode: 16 sequences, lengths U[512, 8192], 32/8 heads, D 128 ----
+    if args.extra in ("all", "paged"):
+        res["paged_decode"] = _paged(torch, K, W, np, t, dev, bench_graph, hbm)
+    if args.extra in ("all", "deep"):
+        for cache in ("int8", "fp16"):
+            res[f"deep_context_{cache}"] = _deep(torch, K, W, np, t, dev, bench_graph, hbm, cache)
+    if args.extra in ("all", "prefill"):
+        res["sparse_prefill"] = _prefill(torch, K, W, np, t, bench_graph, peaks)
+    return res
+
+
+def _paged(torch, K, W, np, t, dev, bench_graph, hbm):
+    """Paged decode: 16 sequences, lengths U[512, 8192], 32/8 heads, D 128."""
     c = W.paged_decode(seed=0)
     B, Hq, Dh = c.q.shape
     nb, bs, Hkv, _ = c.k_cache.shape
@@ -413,48 +425,47 @@ def extra_configs(torch, K, W, np, dev, stream, peaks, args):
             K.paged_decode(q, x["k"], x["v"], ks, vs, c.scale_kind, bt, lens, c.sigma, sink,
                            num_splits=ns, chunk=chunk, workspace=ws, out=out)
     sec = bench_graph(fn, R)
-    res["paged_decode"] = dict(
+    return dict(
         workload="paged INT8 decode: 16 sequences, lengths U[512,8192] (sum %d), block 16, "
                  "permuted block table, 32/8 heads, head_dim 128, per-channel scales, sink"
                  % tokens,
         us_per_call=round(sec * 1e6, 2), gbs=round(byts / sec / 1e9, 1),
         frac_of_hbm=round(byts / sec / 1e9 / hbm, 4), bytes_per_call=byts, num_splits=ns,
-        chunk=chunk, rotating_copies=R)
-    del copies
+        chunk=chunk, wave_ctas=wave, rotating_copies=R)
 
-    # ---- deep-context split sweep: 16 rows, cap 4096, live 2600, 16/2 heads ----
-    for cache in ("int8", "fp16"):
-        c = W.deep_context(seed=0, cache=cache)
-        B, Hq, Dh = c.q.shape
-        nb, bs, Hkv, _ = c.k_cache.shape
-        esz = 1 if cache == "int8" else 2
-        R = 20 if cache == "int8" else 10
-        copies = [dict(k=t(c.k_cache), v=t(c.v_cache)) for _ in range(R)]
-        q, ks, vs, bt, lens = t(c.q), t(c.k_scale), t(c.v_scale), t(c.block_table), t(c.seq_lens)
-        byts = B * 2600 * Hkv * Dh * 2 * esz + B * Hq * Dh * 4 + B * (2600 // 16 + 1) * 4
-        dt = K.CACHE_INT8 if cache == "int8" else K.CACHE_FP16
-        row = {}
-        for label, ovr in (("adaptive", 0), ("chunk128", 128), ("chunk256", 256),
-                           ("chunk512", 512)):
-            ns, chunk, wsb, wave = K.decode_plan(K.PATH_PAGED, dt, 4096, B, Hq, Hkv, Dh,
-                                                 K.GEOM_WAVE, ovr)
-            ws = torch.empty(max(wsb // 4, 4), dtype=torch.float32, device=dev)
-            out = torch.empty_like(q)
 
-            def fn():
-                for x in copies:
-                    K.paged_decode(q, x["k"], x["v"], ks, vs, c.scale_kind, bt, lens, c.sigma,
-                                   num_splits=ns, chunk=chunk, workspace=ws, out=out)
-            sec = bench_graph(fn, R, reps=100)
-            row[label] = dict(us_per_call=round(sec * 1e6, 2), gbs=round(byts / sec / 1e9, 1),
-                              frac_of_hbm=round(byts / sec / 1e9 / hbm, 4), num_splits=ns,
-                              chunk=chunk)
-        res[f"deep_context_{cache}"] = dict(
-            workload=f"deep context: 16 rows, {cache} cache, live 2600 of cap 4096, 16/2 heads, "
-                     "head_dim 128", bytes_per_call=byts, rotating_copies=R, **row)
-        del copies
+def _deep(torch, K, W, np, t, dev, bench_graph, hbm, cache):
+    """Deep-context split sweep: 16 rows, cap 4096, live 2600, 16/2 heads."""
+    c = W.deep_context(seed=0, cache=cache)
+    B, Hq, Dh = c.q.shape
+    nb, bs, Hkv, _ = c.k_cache.shape
+    esz = 1 if cache == "int8" else 2
+    R = 20 if cache == "int8" else 10
+    copies = [dict(k=t(c.k_cache), v=t(c.v_cache)) for _ in range(R)]
+    q, ks, vs, bt, lens = t(c.q), t(c.k_scale), t(c.v_scale), t(c.block_table), t(c.seq_lens)
+    byts = B * 2600 * Hkv * Dh * 2 * esz + B * Hq * Dh * 4 + B * (2600 // 16 + 1) * 4
+    dt = K.CACHE_INT8 if cache == "int8" else K.CACHE_FP16
+    row = {}
+    for label, ovr in (("adaptive", 0), ("chunk128", 128), ("chunk256", 256), ("chunk512", 512)):
+        ns, chunk, wsb, wave = K.decode_plan(K.PATH_PAGED, dt, 4096, B, Hq, Hkv, Dh,
+                                             K.GEOM_WAVE, ovr)
+        ws = torch.empty(max(wsb // 4, 4), dtype=torch.float32, device=dev)
+        out = torch.empty_like(q)
 
-    # ---- sparse prefill: 2048 rows over an 8192-token cache, 24/2 heads, D 256 ----
+        def fn():
+            for x in copies:
+                K.paged_decode(q, x["k"], x["v"], ks, vs, c.scale_kind, bt, lens, c.sigma,
+                               num_splits=ns, chunk=chunk, workspace=ws, out=out)
+        sec = bench_graph(fn, R, reps=100)
+        row[label] = dict(us_per_call=round(sec * 1e6, 2), gbs=round(byts / sec / 1e9, 1),
+                          frac_of_hbm=round(byts / sec / 1e9 / hbm, 4), num_splits=ns,
+                          chunk=chunk)
+    return dict(workload=f"deep context: 16 rows, {cache} cache, live 2600 of cap 4096, 16/2 "
+                         "heads, head_dim 128", bytes_per_call=byts, rotating_copies=R, **row)
+
+
+def _prefill(torch, K, W, np, t, bench_graph, peaks):
+    """Sparse prefill: 2048 rows over an 8192-token cache, 24/2 heads, D 256."""
     c = W.sparse_prefill(seed=0)
     d = dict(q=t(c.q), k=t(c.k_codes), v=t(c.v_codes), ks=t(c.k_scale), vs=t(c.v_scale),
              idx=t(c.idx))
@@ -468,13 +479,12 @@ def extra_configs(torch, K, W, np, dev, stream, peaks, args):
     flops = n_att * 24 * 256 * 4
     gathered = n_att * 2 * 256 * 2
     peak_tf = peaks["bf16_tflops"]
-    res["sparse_prefill"] = dict(
+    return dict(
         workload="sparse prefill: 2048 rows at positions 6144+i over an 8192-token int8 cache, "
                  "2048 candidates per row, 24/2 heads, head_dim 256",
         ms_per_call=round(sec * 1e3, 4), tflops=round(flops / sec / 1e12, 2),
         frac_of_tensor=round(flops / sec / 1e12 / peak_tf, 4), tensor_peak=peak_tf,
         gathered_gbs=round(gathered / sec / 1e9, 1), flops_per_call=flops)
-    return res
 
 
 def reference_arm(args, rank, world):

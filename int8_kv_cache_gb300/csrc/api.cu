@@ -125,6 +125,7 @@ i8kv_status check_geometry(int64_t cap, int32_t ns, int32_t chunk) {
   if (ns < 1 || ns > I8KV_MAX_SPLITS) return I8KV_EINVAL;
   if (chunk < 16 || chunk % 16 != 0) return I8KV_EINVAL;
   if (static_cast<int64_t>(ns) * chunk < cap) return I8KV_EINVAL;
+  if (static_cast<int64_t>(ns) * chunk > INT32_MAX) return I8KV_EINVAL;  // positions are 32-bit
   return I8KV_OK;
 }
 
@@ -387,6 +388,9 @@ i8kv_status paged_decode(const uint16_t* q, const void* k_cache, const void* v_c
   p.Hkv = Hkv;
   p.G = G;
   p.bs = block_size;
+  p.bs_log2 = -1;
+  for (int sh = 4; sh < 31; ++sh)
+    if (block_size == (1 << sh)) p.bs_log2 = sh;
   p.max_blocks = max_blocks;
   p.num_splits = num_splits;
   p.chunk = chunk;

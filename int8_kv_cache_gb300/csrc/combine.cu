@@ -5,10 +5,11 @@
 // split-K partials; onnxruntime PR 29912, CUDA kernels: ApplyHeadSink):
 //   M = max_k m_k;  L = sum_k l_k e^(m_k - M);  O = sum_k acc_k e^(m_k - M) / L;
 //   lse = M + ln L;  O <- O / (1 + e^(s_h - lse)).
-// One warp per (unit, query head): lane k holds split k's (m, l) (at most 32
-// splits), the warp reduces M and L with shuffles, then every lane accumulates
-// D/32 channels over the splits with vector loads.  Splits with m = -inf are
-// skipped without reading their accumulator.
+// One 128-thread CTA per (unit, query head): every thread owns D/128 channels
+// (one or two; half the threads idle at D = 64) and issues the loads of all its
+// splits at once, so the whole merge costs one L2 round trip.  Each warp reads
+// the (m, l) of all splits (lane k holds split k) and reduces M and L with
+// shuffles.  Splits with m = -inf are skipped without reading their accumulator.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -17,20 +18,42 @@
 
 namespace i8kv {
 
+constexpr int kCombineThreads = 128;
+
 template <int D>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const float* __restrict__ acc, const float* __restrict__ m,
                const float* __restrict__ l, int units, int ns, int Hkv, int G,
                const float* __restrict__ sink, __half* __restrict__ out, float* __restrict__ lse) {
-  constexpr int V = D / 32;  // channels per lane: 2, 4 or 8
-  const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
+  constexpr int V = D >= kCombineThreads ? D / kCombineThreads : 1;  // channels per thread
+  const int wid = blockIdx.x;  // (unit, head) pair
   const int lane = threadIdx.x & 31;
-  if (wid >= units * G) return;
+  grid_dependency_wait();  // the partials come from the preceding decode kernel
+  grid_dependents_launch();  // the next kernel of the stream may launch and wait
   const int u = wid / G, j = wid - (wid / G) * G;
   const long long ml0 = (long long)u * ns * G + j;  // split k at ml0 + k*G
+  const int c0 = threadIdx.x * V;                    // first channel of this thread
+  const bool has = c0 < D;
 
+  // all loads first: (m, l) of every split, and this thread's accumulator
+  // channels of every split (up to 32)
   const float mk = lane < ns ? m[ml0 + (long long)lane * G] : neg_inf();
   const float lk = lane < ns ? l[ml0 + (long long)lane * G] : 0.f;
+  float a[32][V];
+  const float* base = acc + ((long long)u * ns * G + j) * D + c0;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    if (k < ns && has) {
+      const float* src = base + (long long)k * G * D;
+      if constexpr (V == 2) {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        a[k][0] = v.x;
+        a[k][1] = v.y;
+      } else {
+        a[k][0] = *src;
+      }
+    }
+  }
   float M = mk;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -42,21 +65,16 @@ combine_kernel(const float* __restrict__ acc, const float* __restrict__ m,
   float o[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) o[i] = 0.f;
-  for (int k = 0; k < ns; ++k) {
-    const float fk = __shfl_sync(0xffffffffu, f, k);
-    if (fk == 0.f) continue;  // warp-uniform
-    const float* src = acc + (((long long)u * ns + k) * G + j) * D + lane * V;
-    if constexpr (V == 2) {
-      const float2 a = *reinterpret_cast<const float2*>(src);
-      o[0] += fk * a.x; o[1] += fk * a.y;
-    } else {
 #pragma unroll
-      for (int i = 0; i < V; i += 4) {
-        const float4 a = *reinterpret_cast<const float4*>(src + i);
-        o[i] += fk * a.x; o[i + 1] += fk * a.y; o[i + 2] += fk * a.z; o[i + 3] += fk * a.w;
-      }
+  for (int k = 0; k < 32; ++k) {
+    if (k < ns) {
+      const float fk = __shfl_sync(0xffffffffu, f, k);
+      // an empty split (fk = 0) may hold anything: select, do not multiply
+#pragma unroll
+      for (int i = 0; i < V; ++i) o[i] += fk != 0.f ? fk * a[k][i] : 0.f;
     }
   }
+  if (!has) return;
   const int h = (u % Hkv) * G + j;
   float lse_v = neg_inf(), scale = 0.f;
   if (L > 0.f) {
@@ -64,29 +82,37 @@ combine_kernel(const float* __restrict__ acc, const float* __restrict__ m,
     scale = 1.f / L;
     if (sink != nullptr) scale *= 1.f / (1.f + expf(sink[h] - lse_v));
   }
-  __half* dst = out + (long long)wid * D + lane * V;
-#pragma unroll
-  for (int i = 0; i < V; i += 2) {
-    *reinterpret_cast<__half2*>(dst + i) = __floats2half2_rn(o[i] * scale, o[i + 1] * scale);
+  __half* dst = out + (long long)wid * D + c0;
+  if constexpr (V == 2) {
+    *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(o[0] * scale, o[1] * scale);
+  } else {
+    *dst = __float2half_rn(o[0] * scale);
   }
-  if (lane == 0 && lse != nullptr) lse[wid] = lse_v;
+  if (threadIdx.x == 0 && lse != nullptr) lse[wid] = lse_v;
 }
 
 cudaError_t launch_combine(const float* acc, const float* m, const float* l, int units,
                            int num_splits, int Hq, int Hkv, int D, const float* sink, void* out,
                            float* lse, cudaStream_t stream) {
   const int G = Hq / Hkv;
-  const long long warps = (long long)units * G;
-  if (warps == 0) return cudaSuccess;
-  const unsigned blocks = (unsigned)((warps + 3) / 4);
+  const long long pairs = (long long)units * G;
+  if (pairs == 0) return cudaSuccess;
   __half* o = reinterpret_cast<__half*>(out);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)pairs);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   switch (D) {
-    case 64: combine_kernel<64><<<blocks, 128, 0, stream>>>(acc, m, l, units, num_splits, Hkv, G, sink, o, lse); break;
-    case 128: combine_kernel<128><<<blocks, 128, 0, stream>>>(acc, m, l, units, num_splits, Hkv, G, sink, o, lse); break;
-    case 256: combine_kernel<256><<<blocks, 128, 0, stream>>>(acc, m, l, units, num_splits, Hkv, G, sink, o, lse); break;
+    case 64: return cudaLaunchKernelEx(&cfg, combine_kernel<64>, acc, m, l, units, num_splits, Hkv, G, sink, o, lse);
+    case 128: return cudaLaunchKernelEx(&cfg, combine_kernel<128>, acc, m, l, units, num_splits, Hkv, G, sink, o, lse);
+    case 256: return cudaLaunchKernelEx(&cfg, combine_kernel<256>, acc, m, l, units, num_splits, Hkv, G, sink, o, lse);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 // Each thread converts four codes with the decode kernels' conversion.

@@ -49,35 +49,62 @@ namespace i8kv {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kSlice = 16;  // tokens per warp step (the MMA M dimension)
+constexpr int kSub = 16;  // tokens per MMA tile (the M dimension of QK^T)
 
-template <int D, bool FP16C>
+template <int D, int NT, bool FP16C>
 struct Tile {
   static constexpr int kElem = FP16C ? 2 : 1;
   static constexpr int kRowBytes = D * kElem;        // one cache row of one KV head
-  static constexpr int kRS = kRowBytes + 16;         // padded shared-memory row stride
   static constexpr int kChunks = kRowBytes / 16;     // 16-byte chunks per row (<= 32)
+  // Tokens per warp step: two 16-token tiles where the registers allow it.
+  static constexpr int SUB = (kRowBytes <= 128 && D * NT <= 256) ? 2 : 1;
+  static constexpr int kStep = kSub * SUB;
   static constexpr int kRowsPerCopy = 32 / kChunks;  // rows covered by one warp-wide copy
-  static constexpr int kCopies = kSlice / kRowsPerCopy;
-  static constexpr int kSliceBytes = kSlice * kRS;   // K (or V) of one slice
-  static constexpr int kStages = kRowBytes <= 128 ? 4 : 3;
-  static constexpr int kWarpRing = kStages * 2 * kSliceBytes;
+  static constexpr int kCopies = kStep / kRowsPerCopy;
+  static constexpr int kTileBytes = kStep * kRowBytes;   // K (or V) of one step, dense
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kQStride = D + 8;             // Q' staging row (halves), padded
+  static constexpr int kQBytes = 16 * kQStride * 2;
+  static constexpr int kMaskBytes = kWarps * 4 * 4;
+  // resident CTAs per SM the registers allow (16, 12 or 8 warps per SM)
+  static constexpr int kRegBlocks = D * NT >= 512 ? 2 : (D * NT >= 256 ? 3 : 4);
+  static constexpr int kPerCta = 227 * 1024 / kRegBlocks - 1024 - kQBytes - kMaskBytes;
+  // ring depth per warp: the largest of 4, 3, 2 stages that fits that budget
+  static constexpr int kStages = kWarps * 4 * kStageBytes <= kPerCta ? 4
+                               : (kWarps * 3 * kStageBytes <= kPerCta ? 3 : 2);
+  static constexpr int kWarpRing = kStages * kStageBytes;
   static constexpr int kRingBytes = kWarps * kWarpRing;
-  static constexpr int kMaskBytes = kWarps * kStages * 4;
-  static constexpr int kQBytes = 16 * D * 2;         // Q' staging, 16 heads x D fp16
   static constexpr int kLoopBytes = kRingBytes + kMaskBytes + kQBytes;
-  // end-of-CTA merge: m, l [4][16]; acc [4][16][D]; weights [4][16]; M, L [16]
-  static constexpr int kMergeBytes = (64 + 64 + kWarps * 16 * D + 64 + 16 + 16) * 4;
+  // end-of-CTA merge: every thread's accumulator fragment (E floats, padded by
+  // 4 for conflict-free 16-byte access) plus m, l of the 4 warps x 16 heads
+  static constexpr int kE = (D / 16) * NT * 4;
+  static constexpr int kMergeBytes = (kThreads * (kE + 4) + 2 * kWarps * 16) * 4;
   static constexpr int kSmem = kLoopBytes > kMergeBytes ? kLoopBytes : kMergeBytes;
+  static constexpr int kSmemBlocks = 227 * 1024 / (kSmem + 1024);
+  static constexpr int kMinBlocks = kSmemBlocks < kRegBlocks ? kSmemBlocks : kRegBlocks;
   static_assert(kChunks <= 32 && 32 % kChunks == 0, "row layout");
-  static_assert(kSmem <= 227 * 1024, "shared memory");
+  static_assert(kCopies >= 1, "copy layout");
+  static_assert(kSmem <= 227 * 1024 && kMinBlocks >= 1, "shared memory");
 };
 
+// XOR swizzle of the 16-byte chunks of a dense shared-memory row, so that the
+// 8 rows of an ldmatrix phase (and the rows a copy instruction writes) fall in
+// distinct bank groups.
+template <int ROW_BYTES>
+__device__ __forceinline__ int swz(int r) {
+  if constexpr (ROW_BYTES >= 128) {
+    return r & 7;
+  } else {
+    return (r >> 1) & 3;  // 64-byte rows: two rows per 128-byte bank line
+  }
+}
+
 template <int D, int NT, bool PAGED, bool FP16C, bool PLO>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, (Tile<D, NT, FP16C>::kMinBlocks))
 decode_kernel(const DecodeParams p) {
-  using T = Tile<D, FP16C>;
+  using T = Tile<D, NT, FP16C>;
   constexpr int KC = D / 16;  // k-chunks of QK^T and m-tiles of PV
+  constexpr int SUB = T::SUB;
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int lane = threadIdx.x & 31;
@@ -89,54 +116,247 @@ decode_kernel(const DecodeParams p) {
   const int row = unit / p.Hkv;
   const int g = unit - row * p.Hkv;
   const int G = p.G;
+  grid_dependency_wait();  // inputs may come from the previous kernel of the stream
+  // Let the combine launch now: its CTAs take SM slots as this grid's CTAs
+  // leave and wait there (griddepcontrol.wait) until this grid completes.
+  grid_dependents_launch();
+
+  // Query rows of the group and their key scales, 8 channels per thread and
+  // step, loaded first so that their latency overlaps the length and gather-key
+  // loads below.
+  constexpr int kQSteps = (NT * D + kThreads - 1) / kThreads;
+  uint4 q_raw[kQSteps];
+  float4 ks_raw[kQSteps][2];
+  {
+    const __half* qrow = reinterpret_cast<const __half*>(p.q) + ((long long)row * p.Hq + g * G) * D;
+#pragma unroll
+    for (int i = 0; i < kQSteps; ++i) {
+      const int e = threadIdx.x + i * kThreads;
+      const int h = (e * 8) / D, d0 = (e * 8) % D;
+      q_raw[i] = make_uint4(0u, 0u, 0u, 0u);
+      ks_raw[i][0] = ks_raw[i][1] = make_float4(1.f, 1.f, 1.f, 1.f);
+      if (e < NT * D && h < G) {
+        q_raw[i] = *reinterpret_cast<const uint4*>(qrow + h * D + d0);
+        if constexpr (!FP16C) {
+          if (p.per_channel) {
+            ks_raw[i][0] = *reinterpret_cast<const float4*>(p.k_scale + g * D + d0);
+            ks_raw[i][1] = *reinterpret_cast<const float4*>(p.k_scale + g * D + d0 + 4);
+          } else {
+            const float k0 = p.k_scale[0];
+            ks_raw[i][0] = ks_raw[i][1] = make_float4(k0, k0, k0, k0);
+          }
+        }
+      }
+    }
+  }
+
+  // v_scale of the channels this thread writes in the epilogue (warp w writes
+  // m-tiles [w*KC/4, (w+1)*KC/4)), loaded now so the epilogue does not wait
+  constexpr int MT_PER_WARP = KC / kWarps;
+  float vs_a[MT_PER_WARP], vs_b[MT_PER_WARP];
+#pragma unroll
+  for (int i = 0; i < MT_PER_WARP; ++i) {
+    vs_a[i] = vs_b[i] = 1.f;
+    if constexpr (!FP16C) {
+      const int mt = warp * MT_PER_WARP + i;
+      const int da = 16 * mt + 2 * grp;  // int8 channel order of the PV fragments
+      if (p.per_channel) {
+        const float2 v2 = *reinterpret_cast<const float2*>(p.v_scale + g * D + da);
+        vs_a[i] = v2.x;
+        vs_b[i] = v2.y;
+      } else {
+        vs_a[i] = vs_b[i] = p.v_scale[0];
+      }
+    }
+  }
 
   // ---------------- candidate range of this split ----------------
-  const long long lo = (long long)split * p.chunk;
-  long long hi;
-  int live = 0;
+  // (positions fit 32 bits: the host checks num_splits * chunk <= INT32_MAX)
+  const int lo = split * p.chunk;
+  // nominal end of the split (capacity-bounded); the live end follows below
+  const int cap = PAGED ? p.max_blocks * p.bs : p.max_sel;
+  const int nhi = min(lo + p.chunk, cap);
+  int len = 0;
+  if constexpr (PAGED) len = p.seq_lens[row];  // in flight while the keys are fetched
+
+  // ---------------- per-warp gather pipeline ----------------
+  // Warp w takes the steps w, w+4, w+8, ... of kStep consecutive positions.
+  int* wmask = reinterpret_cast<int*>(smem + T::kRingBytes) + warp * 4;
+  const uint32_t ring_addr = smem_addr(smem + warp * T::kWarpRing);
+
+  const char* kbase = reinterpret_cast<const char*>(p.k);
+  const char* vbase = reinterpret_cast<const char*>(p.v);
+  const long long row_stride = (long long)p.Hkv * T::kRowBytes;  // bytes between tokens
+  const int chunk_id = lane % T::kChunks;
+  const int row_in_copy = lane / T::kChunks;
+  const long long lane_off = (long long)g * T::kRowBytes + chunk_id * 16;
+
+  auto step_pos = [&](int k) -> int { return lo + T::kStep * (warp + kWarps * k); };
+  // block of a 16-aligned position and the row offset of that position in its
+  // block (block_size is a multiple of 16; a shift when it is a power of two)
+  const int bs_shift = p.bs_log2;
+  auto block_of = [&](int pos) -> int { return bs_shift >= 0 ? pos >> bs_shift : pos / p.bs; };
+  auto offset_in_block = [&](int pos) -> int {
+    return bs_shift >= 0 ? pos & (p.bs - 1) : pos % p.bs;
+  };
+  auto steps_below = [&](int end) -> int {
+    const int n = end > lo ? (end - lo + T::kStep - 1) / T::kStep : 0;
+    return n > warp ? (n - warp + kWarps - 1) / kWarps : 0;
+  };
+
+  // The per-step gather key, loaded ahead of the copies: the list entry of
+  // position (lane % kStep) of the step (sparse), or the block id of 16-token
+  // tile (lane % SUB) of the step (paged; block_size is a multiple of 16).
+  // The first keys are fetched against the nominal end, before the live length
+  // of a paged sequence is known.
+  int fetch_hi = nhi;
+  int fetch_n = steps_below(nhi);
+  auto fetch = [&](int k) -> int {
+    if (k >= fetch_n) return -1;
+    const int pos0 = step_pos(k);
+    if constexpr (PAGED) {
+      const int pos = pos0 + kSub * (lane % SUB);
+      return pos < fetch_hi ? __ldg(p.block_table + (long long)row * p.max_blocks + block_of(pos))
+                            : -1;
+    } else {
+      const int pos = pos0 + (lane % T::kStep);
+      return pos < fetch_hi ? __ldg(p.idx + (long long)row * p.max_sel + pos) : -1;
+    }
+  };
+  int pf[T::kStages + 1];
+#pragma unroll
+  for (int k = 0; k <= T::kStages; ++k) pf[k] = fetch(k);
+
+  // live end of the split
+  int hi = nhi;
   if constexpr (PAGED) {
-    const int cap = p.max_blocks * p.bs;
-    int len = p.seq_lens[row];
     if (len > cap || len < 0) {
       if (g == 0 && split == 0 && threadIdx.x == 0) flag_or(p.flags, I8KV_FLAG_LEN_CLAMPED);
       len = len < 0 ? 0 : cap;
     }
-    live = len;
-    hi = lo + p.chunk < (long long)len ? lo + p.chunk : (long long)len;
+    hi = min(nhi, len);
     // debug output: the gathered row of every token of this split's nominal range
     if (p.slots_out != nullptr && g == 0) {
-      const long long nhi = lo + p.chunk < (long long)cap ? lo + p.chunk : (long long)cap;
-      for (long long t = lo + threadIdx.x; t < nhi; t += kThreads) {
+      for (int t = lo + threadIdx.x; t < nhi; t += kThreads) {
         int v = -1;
-        if (t < live) {
+        if (t < len) {
           const int blk = p.block_table[(long long)row * p.max_blocks + t / p.bs];
-          v = blk * p.bs + (int)(t % p.bs);
+          v = blk * p.bs + t % p.bs;
         }
         p.slots_out[(long long)row * cap + t] = v;
       }
     }
-  } else {
-    hi = lo + p.chunk < (long long)p.max_sel ? lo + p.chunk : (long long)p.max_sel;
   }
-  const int npos = hi > lo ? (int)(hi - lo) : 0;
+  const int npos = hi > lo ? hi - lo : 0;
+  const int my_n = steps_below(hi);
+  fetch_hi = hi;
+  fetch_n = my_n;
+
+  auto issue = [&](int k, int key) {
+    if (k < my_n) {
+      const int pos0 = step_pos(k);
+      const int st = k % T::kStages;
+      const uint32_t dK = ring_addr + st * T::kStageBytes;
+      const uint32_t dV = dK + T::kTileBytes;
+      unsigned mask;
+      if constexpr (PAGED) {
+        const int nvalid = min(hi - pos0, T::kStep);
+        mask = nvalid >= 32 ? 0xFFFFFFFFu : ((1u << nvalid) - 1u);
+        bool bad_blk = false;
+#pragma unroll
+        for (int s = 0; s < SUB; ++s) {
+          const int blk = __shfl_sync(0xffffffffu, key, s);
+          if (blk < 0 || (long long)blk >= p.cache_rows) {
+            if (((mask >> (kSub * s)) & 0xFFFFu) != 0u) bad_blk = true;
+            mask &= ~(0xFFFFu << (kSub * s));
+          }
+        }
+        if (bad_blk && lane == 0) flag_or(p.flags, I8KV_FLAG_BAD_BLOCK);
+        // first cache row of each 16-token tile: block * block_size + offset
+        long long tile_row[SUB];
+#pragma unroll
+        for (int s = 0; s < SUB; ++s)
+          tile_row[s] = (long long)__shfl_sync(0xffffffffu, key, s) * p.bs +
+                        offset_in_block(pos0 + kSub * s);
+#pragma unroll
+        for (int i = 0; i < T::kCopies; ++i) {
+          const int r = row_in_copy + i * T::kRowsPerCopy;
+          const bool ok = (mask >> r) & 1u;
+          const long long off = ok ? (tile_row[r / kSub] + (r % kSub)) * row_stride + lane_off : 0;
+          const uint32_t so = r * T::kRowBytes + ((chunk_id ^ swz<T::kRowBytes>(r)) << 4);
+          cp_async16(dK + so, kbase + off, ok ? 16u : 0u);
+          cp_async16(dV + so, vbase + off, ok ? 16u : 0u);
+        }
+      } else {
+        const bool ok_mine = key >= 0 && (long long)key < p.cache_rows;
+        mask = __ballot_sync(0xffffffffu, ok_mine);
+        if constexpr (T::kStep == 16) mask &= 0xFFFFu;
+#pragma unroll
+        for (int i = 0; i < T::kCopies; ++i) {
+          const int r = row_in_copy + i * T::kRowsPerCopy;
+          const int t = __shfl_sync(0xffffffffu, key, r);
+          const bool ok = (mask >> r) & 1u;
+          const long long off = ok ? (long long)t * row_stride + lane_off : 0;
+          const uint32_t so = r * T::kRowBytes + ((chunk_id ^ swz<T::kRowBytes>(r)) << 4);
+          cp_async16(dK + so, kbase + off, ok ? 16u : 0u);
+          cp_async16(dV + so, vbase + off, ok ? 16u : 0u);
+        }
+      }
+      if (lane == 0) wmask[st] = (int)mask;
+    }
+    cp_async_commit();
+  };
+
+  // Start the gathers first: the query staging below overlaps their latency.
+#pragma unroll
+  for (int k = 0; k < T::kStages - 1; ++k) issue(k, pf[k]);
+  int q0 = pf[T::kStages - 1], q1 = pf[T::kStages];
+
+  // A CTA without candidates (an empty split) publishes the empty partial
+  // (m = -inf, l = 0) or, with one split, O = 0 and lse = -inf.  The branch is
+  // uniform over the CTA.
+  if (npos == 0) {
+    cp_async_wait_all();
+    const long long head0 = (long long)row * p.Hq + g * G;
+    for (int e = threadIdx.x; e < G * (p.num_splits == 1 ? D : 1); e += kThreads) {
+      if (p.num_splits == 1) {
+        const int h = e / D, d = e % D;
+        reinterpret_cast<__half*>(p.out)[(head0 + h) * D + d] = __float2half_rn(0.f);
+        if (d == 0 && p.lse != nullptr) p.lse[head0 + h] = neg_inf();
+      } else {
+        const long long base = ((long long)unit * p.num_splits + split) * G + e;
+        p.ws_m[base] = neg_inf();
+        p.ws_l[base] = 0.f;
+      }
+    }
+    return;
+  }
 
   // ---------------- Q' = fp16(Q * k_scale), staged through shared memory ----------------
   __half* sq = reinterpret_cast<__half*>(smem + T::kRingBytes + T::kMaskBytes);
   {
-    const __half* qrow = reinterpret_cast<const __half*>(p.q) + ((long long)row * p.Hq + g * G) * D;
     bool bad = false;
-    for (int e = threadIdx.x; e < 8 * NT * D; e += kThreads) {
-      const int h = e / D, d = e - (e / D) * D;
-      float x = 0.f;
-      if (h < G) {
-        x = __half2float(qrow[h * D + d]);
-        if constexpr (!FP16C) {
-          const float ks = p.per_channel ? p.k_scale[g * D + d] : p.k_scale[0];
-          x *= ks;
-          bad |= !(fabsf(x) <= 65504.f);
+#pragma unroll
+    for (int i = 0; i < kQSteps; ++i) {
+      const int e = threadIdx.x + i * kThreads;
+      if (e >= NT * D) break;
+      const int h = (e * 8) / D, d0 = (e * 8) % D;
+      uint4 packed = q_raw[i];
+      if constexpr (!FP16C) {
+        const __half2* qh = reinterpret_cast<const __half2*>(&q_raw[i]);
+        const float ks[8] = {ks_raw[i][0].x, ks_raw[i][0].y, ks_raw[i][0].z, ks_raw[i][0].w,
+                             ks_raw[i][1].x, ks_raw[i][1].y, ks_raw[i][1].z, ks_raw[i][1].w};
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __half22float2(qh[j]);
+          const float x0 = f.x * ks[2 * j], x1 = f.y * ks[2 * j + 1];
+          bad |= !(fabsf(x0) <= 65504.f) || !(fabsf(x1) <= 65504.f);
+          w[j] = pack_h2(x0, x1);
         }
+        packed = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      sq[h * D + d] = __float2half_rn(x);
+      *reinterpret_cast<uint4*>(sq + h * T::kQStride + d0) = packed;
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0) flag_or(p.flags, I8KV_FLAG_QUERY_RANGE);
   }
@@ -146,88 +366,19 @@ decode_kernel(const DecodeParams p) {
   uint32_t qf[NT][KC][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const uint32_t* qw = reinterpret_cast<const uint32_t*>(sq + (nt * 8 + grp) * D);
+    const __half* qh = sq + (nt * 8 + grp) * T::kQStride;
 #pragma unroll
     for (int kc = 0; kc < KC; ++kc) {
       if constexpr (FP16C) {
-        qf[nt][kc][0] = qw[(16 * kc + 2 * tig) / 2];
-        qf[nt][kc][1] = qw[(16 * kc + 2 * tig + 8) / 2];
+        qf[nt][kc][0] = *reinterpret_cast<const uint32_t*>(qh + 16 * kc + 2 * tig);
+        qf[nt][kc][1] = *reinterpret_cast<const uint32_t*>(qh + 16 * kc + 2 * tig + 8);
       } else {
-        qf[nt][kc][0] = qw[(16 * kc + 4 * tig) / 2];
-        qf[nt][kc][1] = qw[(16 * kc + 4 * tig + 2) / 2];
+        const uint2 v = *reinterpret_cast<const uint2*>(qh + 16 * kc + 4 * tig);
+        qf[nt][kc][0] = v.x;
+        qf[nt][kc][1] = v.y;
       }
     }
   }
-
-  // ---------------- per-warp gather pipeline ----------------
-  const int nslices = (npos + kSlice - 1) / kSlice;
-  const int my_n = nslices > warp ? (nslices - warp + kWarps - 1) / kWarps : 0;
-  uint8_t* wring = smem + warp * T::kWarpRing;
-  int* wmask = reinterpret_cast<int*>(smem + T::kRingBytes) + warp * T::kStages;
-  const uint32_t ring_addr = smem_addr(wring);
-
-  const char* kbase = reinterpret_cast<const char*>(p.k);
-  const char* vbase = reinterpret_cast<const char*>(p.v);
-  const long long row_stride = (long long)p.Hkv * T::kRowBytes;  // bytes between tokens
-  const int chunk_id = lane % T::kChunks;
-  const int row_in_copy = lane / T::kChunks;
-  const long long lane_off = (long long)g * T::kRowBytes + chunk_id * 16;
-
-  auto slice_pos = [&](int k) -> long long { return lo + (long long)kSlice * (warp + kWarps * k); };
-
-  // The per-slice gather key, loaded ahead of the copies: the list entry of
-  // row (lane & 15) of the slice (sparse), or the block id (paged).
-  auto fetch = [&](int k) -> int {
-    if (k >= my_n) return -1;
-    const long long pos0 = slice_pos(k);
-    if constexpr (PAGED) {
-      return __ldg(p.block_table + (long long)row * p.max_blocks + pos0 / p.bs);
-    } else {
-      const long long pos = pos0 + (lane & 15);
-      return pos < hi ? __ldg(p.idx + (long long)row * p.max_sel + pos) : -1;
-    }
-  };
-
-  auto issue = [&](int k, int key) {
-    if (k < my_n) {
-      const long long pos0 = slice_pos(k);
-      const int st = k % T::kStages;
-      const uint32_t dK = ring_addr + st * 2 * T::kSliceBytes;
-      const uint32_t dV = dK + T::kSliceBytes;
-      int mask;
-      if constexpr (PAGED) {
-        int nvalid = hi - pos0 < kSlice ? (int)(hi - pos0) : kSlice;
-        if (key < 0 || (long long)key >= p.cache_rows) {
-          if (lane == 0) flag_or(p.flags, I8KV_FLAG_BAD_BLOCK);
-          nvalid = 0;
-        }
-        mask = nvalid >= kSlice ? 0xFFFF : ((1 << nvalid) - 1);
-        const long long rbase = (long long)key * p.bs + (pos0 % p.bs);
-#pragma unroll
-        for (int i = 0; i < T::kCopies; ++i) {
-          const int r = row_in_copy + i * T::kRowsPerCopy;
-          const bool ok = r < nvalid;
-          const long long off = ok ? (rbase + r) * row_stride + lane_off : 0;
-          cp_async16(dK + r * T::kRS + chunk_id * 16, kbase + off, ok ? 16u : 0u);
-          cp_async16(dV + r * T::kRS + chunk_id * 16, vbase + off, ok ? 16u : 0u);
-        }
-      } else {
-        const bool ok_mine = key >= 0 && (long long)key < p.cache_rows;
-        mask = (int)(__ballot_sync(0xffffffffu, ok_mine) & 0xFFFFu);
-#pragma unroll
-        for (int i = 0; i < T::kCopies; ++i) {
-          const int r = row_in_copy + i * T::kRowsPerCopy;
-          const int t = __shfl_sync(0xffffffffu, key, r);
-          const bool ok = (mask >> r) & 1;
-          const long long off = ok ? (long long)t * row_stride + lane_off : 0;
-          cp_async16(dK + r * T::kRS + chunk_id * 16, kbase + off, ok ? 16u : 0u);
-          cp_async16(dV + r * T::kRS + chunk_id * 16, vbase + off, ok ? 16u : 0u);
-        }
-      }
-      if (lane == 0) wmask[st] = mask;
-    }
-    cp_async_commit();
-  };
 
   // accumulators: O^T m-tiles [KC][NT][4]; online-softmax state per (nt, head pair)
   float acc[KC][NT][4];
@@ -245,42 +396,53 @@ decode_kernel(const DecodeParams p) {
   }
 
   // ldmatrix lane address: matrix m = lane/8 covers tokens (lane%8) + 8*(m&1)
-  // of 16-byte chunk (m>>1) (+ 2 per step)
-  const uint32_t ld_off = ((lane & 7) + 8 * ((lane >> 3) & 1)) * T::kRS + (lane >> 4) * 16;
+  // of the tile and 16-byte chunk 2*c2 + (m>>1)
+  const int ld_row = (lane & 7) + 8 * ((lane >> 3) & 1);
+  const int ld_sw = swz<T::kRowBytes>(ld_row);
+  const int ld_hi = lane >> 4;
+  const uint32_t ld_base = ld_row * T::kRowBytes;
   const float sigma = p.sigma;
 
-  {
-    int pf[T::kStages + 1];
-#pragma unroll
-    for (int k = 0; k <= T::kStages; ++k) pf[k] = fetch(k);
-#pragma unroll
-    for (int k = 0; k < T::kStages - 1; ++k) issue(k, pf[k]);
-    int q0 = pf[T::kStages - 1], q1 = pf[T::kStages];
+  for (int k = 0; k < my_n; ++k) {
+    issue(k + T::kStages - 1, q0);
+    q0 = q1;
+    q1 = fetch(k + T::kStages + 1);
+    cp_async_wait<T::kStages - 1>();
+    __syncwarp();
 
-    for (int k = 0; k < my_n; ++k) {
-      issue(k + T::kStages - 1, q0);
-      q0 = q1;
-      q1 = fetch(k + T::kStages + 1);
-      cp_async_wait<T::kStages - 1>();
-      __syncwarp();
+    const int st = k % T::kStages;
+    const uint32_t sK = ring_addr + st * T::kStageBytes;
+    const uint32_t sV = sK + T::kTileBytes;
+    const unsigned mask = (unsigned)wmask[st];
 
-      const int st = k % T::kStages;
-      const uint32_t sK = ring_addr + st * 2 * T::kSliceBytes;
-      const uint32_t sV = sK + T::kSliceBytes;
-      const int mask = wmask[st];
-
-      // ---- S^T = K Q'^T ----
-      float sacc[NT][4];
+    // ---- S^T = K Q'^T per 16-token tile (with SUB = 1, two accumulator
+    // chains over the k-chunks, summed after) ----
+    float sacc[SUB][NT][4], sacc2[NT][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+    for (int s = 0; s < SUB; ++s)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[s][nt][e] = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc2[nt][e] = 0.f;
+#pragma unroll
+    for (int s = 0; s < SUB; ++s) {
+      const uint32_t tK = sK + s * kSub * T::kRowBytes;
 #pragma unroll
       for (int c2 = 0; c2 < T::kChunks / 2; ++c2) {
         uint32_t r0, r1, r2, r3;
-        ldsm_x4(sK + ld_off + 32 * c2, r0, r1, r2, r3);
+        ldsm_x4(tK + ld_base + (((2 * c2 + ld_hi) ^ ld_sw) << 4), r0, r1, r2, r3);
         if constexpr (FP16C) {
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma16816(sacc[nt], r0, r1, r2, r3, qf[nt][c2][0], qf[nt][c2][1]);
+          for (int nt = 0; nt < NT; ++nt) {
+            if (SUB == 1 && (c2 & 1))
+              mma16816(sacc2[nt], r0, r1, r2, r3, qf[nt][c2][0], qf[nt][c2][1]);
+            else
+              mma16816(sacc[s][nt], r0, r1, r2, r3, qf[nt][c2][0], qf[nt][c2][1]);
+          }
         } else {
           const uint32_t x0 = flip_i8x4(r0), x1 = flip_i8x4(r1);
           const uint32_t x2 = flip_i8x4(r2), x3 = flip_i8x4(r3);
@@ -289,73 +451,112 @@ decode_kernel(const DecodeParams p) {
             const uint32_t a2 = i8x2_to_h2(x0, 0x4342u), a3 = i8x2_to_h2(x1, 0x4342u);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
-              mma16816(sacc[nt], a0, a1, a2, a3, qf[nt][2 * c2][0], qf[nt][2 * c2][1]);
+              mma16816(sacc[s][nt], a0, a1, a2, a3, qf[nt][2 * c2][0], qf[nt][2 * c2][1]);
           }
           {
             const uint32_t a0 = i8x2_to_h2(x2, 0x4140u), a1 = i8x2_to_h2(x3, 0x4140u);
             const uint32_t a2 = i8x2_to_h2(x2, 0x4342u), a3 = i8x2_to_h2(x3, 0x4342u);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma16816(sacc[nt], a0, a1, a2, a3, qf[nt][2 * c2 + 1][0], qf[nt][2 * c2 + 1][1]);
+            for (int nt = 0; nt < NT; ++nt) {
+              if (SUB == 1)
+                mma16816(sacc2[nt], a0, a1, a2, a3, qf[nt][2 * c2 + 1][0], qf[nt][2 * c2 + 1][1]);
+              else
+                mma16816(sacc[s][nt], a0, a1, a2, a3, qf[nt][2 * c2 + 1][0], qf[nt][2 * c2 + 1][1]);
+            }
           }
         }
       }
+    }
+    if constexpr (SUB == 1) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[0][nt][e] += sacc2[nt][e];
+    }
 
-      // ---- online softmax (natural log domain) and the probability tile ----
-      const bool v_top = (mask >> grp) & 1;
-      const bool v_bot = (mask >> (grp + 8)) & 1;
-      uint32_t ph[NT][2], pl[NT][2];
+    // ---- online softmax (natural log domain) over the step's tokens ----
+    uint32_t ph[SUB][NT][2], pl[SUB][NT][2];
+    float alpha[NT][2];
+    bool changed = false;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float s[4];
-        s[0] = v_top ? sacc[nt][0] * sigma : neg_inf();
-        s[1] = v_top ? sacc[nt][1] * sigma : neg_inf();
-        s[2] = v_bot ? sacc[nt][2] * sigma : neg_inf();
-        s[3] = v_bot ? sacc[nt][3] * sigma : neg_inf();
-        float pr[4];
+    for (int nt = 0; nt < NT; ++nt) {
+      float sc[SUB][4];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {  // head 2*tig + j of this n-tile
-          float mx = fmaxf(s[j], s[2 + j]);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float mnew = fmaxf(mrun[nt][j], mx);
-          const float base = mnew == neg_inf() ? 0.f : mnew;
-          const float alpha = fast_exp2((mrun[nt][j] - base) * kLog2e);
-          pr[j] = fast_exp2((s[j] - base) * kLog2e);
-          pr[2 + j] = fast_exp2((s[2 + j] - base) * kLog2e);
-          lrun[nt][j] = lrun[nt][j] * alpha + pr[j] + pr[2 + j];
-          mrun[nt][j] = mnew;
+      for (int s = 0; s < SUB; ++s) {
+        const bool v_top = (mask >> (kSub * s + grp)) & 1u;
+        const bool v_bot = (mask >> (kSub * s + grp + 8)) & 1u;
+        sc[s][0] = v_top ? sacc[s][nt][0] * sigma : neg_inf();
+        sc[s][1] = v_top ? sacc[s][nt][1] * sigma : neg_inf();
+        sc[s][2] = v_bot ? sacc[s][nt][2] * sigma : neg_inf();
+        sc[s][3] = v_bot ? sacc[s][nt][3] * sigma : neg_inf();
+      }
+      float pr[SUB][4];
 #pragma unroll
-          for (int mt = 0; mt < KC; ++mt) {
-            acc[mt][nt][j] *= alpha;
-            acc[mt][nt][2 + j] *= alpha;
-          }
+      for (int j = 0; j < 2; ++j) {  // head 2*tig + j of this n-tile
+        float mx = fmaxf(sc[0][j], sc[0][2 + j]);
+#pragma unroll
+        for (int s = 1; s < SUB; ++s) mx = fmaxf(mx, fmaxf(sc[s][j], sc[s][2 + j]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mnew = fmaxf(mrun[nt][j], mx);
+        const float base = mnew == neg_inf() ? 0.f : mnew;
+        changed |= mnew != mrun[nt][j];
+        alpha[nt][j] = fast_exp2((mrun[nt][j] - base) * kLog2e);
+        float lsum = 0.f;
+#pragma unroll
+        for (int s = 0; s < SUB; ++s) {
+          pr[s][j] = fast_exp2((sc[s][j] - base) * kLog2e);
+          pr[s][2 + j] = fast_exp2((sc[s][2 + j] - base) * kLog2e);
+          lsum += pr[s][j] + pr[s][2 + j];
         }
+        lrun[nt][j] = lrun[nt][j] * alpha[nt][j] + lsum;
+        mrun[nt][j] = mnew;
+      }
+      // probability tile p * 2^15 (high part, and for decode the residual)
+#pragma unroll
+      for (int s = 0; s < SUB; ++s) {
         __half hh[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) hh[e] = __float2half_rn(pr[e] * kProbScale);
-        ph[nt][0] = movm_t(pack_h2(hh[0], hh[1]));
-        ph[nt][1] = movm_t(pack_h2(hh[2], hh[3]));
+        for (int e = 0; e < 4; ++e) hh[e] = __float2half_rn(pr[s][e] * kProbScale);
+        ph[s][nt][0] = movm_t(pack_h2(hh[0], hh[1]));
+        ph[s][nt][1] = movm_t(pack_h2(hh[2], hh[3]));
         if constexpr (PLO) {
           __half hl[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) hl[e] = __float2half_rn(pr[e] * kProbScale - __half2float(hh[e]));
-          pl[nt][0] = movm_t(pack_h2(hl[0], hl[1]));
-          pl[nt][1] = movm_t(pack_h2(hl[2], hl[3]));
+          for (int e = 0; e < 4; ++e)
+            hl[e] = __float2half_rn(pr[s][e] * kProbScale - __half2float(hh[e]));
+          pl[s][nt][0] = movm_t(pack_h2(hl[0], hl[1]));
+          pl[s][nt][1] = movm_t(pack_h2(hl[2], hl[3]));
         }
       }
+    }
+    // rescale the accumulators only when some running maximum moved
+    if (__any_sync(0xffffffffu, changed)) {
+#pragma unroll
+      for (int mt = 0; mt < KC; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          acc[mt][nt][0] *= alpha[nt][0];
+          acc[mt][nt][2] *= alpha[nt][0];
+          acc[mt][nt][1] *= alpha[nt][1];
+          acc[mt][nt][3] *= alpha[nt][1];
+        }
+    }
 
-      // ---- O^T += V^T P^T ----
+    // ---- O^T += V^T P^T, one 16-token tile at a time ----
+#pragma unroll
+    for (int s = 0; s < SUB; ++s) {
+      const uint32_t tV = sV + s * kSub * T::kRowBytes;
 #pragma unroll
       for (int c2 = 0; c2 < T::kChunks / 2; ++c2) {
         uint32_t r0, r1, r2, r3;
-        ldsm_x4_t(sV + ld_off + 32 * c2, r0, r1, r2, r3);
+        ldsm_x4_t(tV + ld_base + (((2 * c2 + ld_hi) ^ ld_sw) << 4), r0, r1, r2, r3);
         if constexpr (FP16C) {
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            mma16816(acc[c2][nt], r0, r2, r1, r3, ph[nt][0], ph[nt][1]);
-            if constexpr (PLO) mma16816(acc[c2][nt], r0, r2, r1, r3, pl[nt][0], pl[nt][1]);
+            mma16816(acc[c2][nt], r0, r2, r1, r3, ph[s][nt][0], ph[s][nt][1]);
+            if constexpr (PLO) mma16816(acc[c2][nt], r0, r2, r1, r3, pl[s][nt][0], pl[s][nt][1]);
           }
         } else {
           const uint32_t x0 = flip_i8x4(r0), x1 = flip_i8x4(r1);
@@ -365,8 +566,9 @@ decode_kernel(const DecodeParams p) {
             const uint32_t a2 = i8x2_to_h2(x1, 0x4240u), a3 = i8x2_to_h2(x1, 0x4341u);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              mma16816(acc[2 * c2][nt], a0, a1, a2, a3, ph[nt][0], ph[nt][1]);
-              if constexpr (PLO) mma16816(acc[2 * c2][nt], a0, a1, a2, a3, pl[nt][0], pl[nt][1]);
+              mma16816(acc[2 * c2][nt], a0, a1, a2, a3, ph[s][nt][0], ph[s][nt][1]);
+              if constexpr (PLO)
+                mma16816(acc[2 * c2][nt], a0, a1, a2, a3, pl[s][nt][0], pl[s][nt][1]);
             }
           }
           {
@@ -374,110 +576,158 @@ decode_kernel(const DecodeParams p) {
             const uint32_t a2 = i8x2_to_h2(x3, 0x4240u), a3 = i8x2_to_h2(x3, 0x4341u);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              mma16816(acc[2 * c2 + 1][nt], a0, a1, a2, a3, ph[nt][0], ph[nt][1]);
+              mma16816(acc[2 * c2 + 1][nt], a0, a1, a2, a3, ph[s][nt][0], ph[s][nt][1]);
               if constexpr (PLO)
-                mma16816(acc[2 * c2 + 1][nt], a0, a1, a2, a3, pl[nt][0], pl[nt][1]);
+                mma16816(acc[2 * c2 + 1][nt], a0, a1, a2, a3, pl[s][nt][0], pl[s][nt][1]);
             }
           }
         }
       }
-      __syncwarp();
     }
+    __syncwarp();
   }
   cp_async_wait_all();
-  __syncthreads();  // every warp is done with its ring: reuse the memory for the merge
 
   // ---------------- merge the four warps' partials ----------------
-  float* mw = reinterpret_cast<float*>(smem);  // [4][16]
-  float* lw = mw + 64;                         // [4][16]
-  float* aw = lw + 64;                         // [4][16][D]
-  float* fw = aw + kWarps * 16 * D;            // [4][16]
-  float* Ms = fw + 64;                         // [16]
-  float* Ls = Ms + 16;                         // [16]
+  // (m, l) per head of every warp; l is first summed over the 8 lanes that
+  // share a head pair.
+  float* mw = reinterpret_cast<float*>(smem + kThreads * (T::kE + 4) * 4);  // [4][16]
+  float* lw = mw + kWarps * 16;                                           // [4][16]
+  float lsum[NT][2];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       float l = lrun[nt][j];
       l += __shfl_xor_sync(0xffffffffu, l, 4);
       l += __shfl_xor_sync(0xffffffffu, l, 8);
       l += __shfl_xor_sync(0xffffffffu, l, 16);
-      if (grp == 0) {
+      lsum[nt][j] = l;
+    }
+  __syncthreads();  // every warp is done with its ring: reuse the memory
+  if (grp == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
         mw[warp * 16 + nt * 8 + 2 * tig + j] = mrun[nt][j];
-        lw[warp * 16 + nt * 8 + 2 * tig + j] = l;
+        lw[warp * 16 + nt * 8 + 2 * tig + j] = lsum[nt][j];
       }
-    }
-#pragma unroll
-    for (int mt = 0; mt < KC; ++mt) {
-      const int h = nt * 8 + 2 * tig;
-      int da, db;
-      if constexpr (FP16C) {
-        da = 16 * mt + grp;
-        db = da + 8;
-      } else {
-        da = 16 * mt + 2 * grp;
-        db = da + 1;
-      }
-      float* a0 = aw + (warp * 16 + h) * D;
-      float* a1 = a0 + D;
-      a0[da] = acc[mt][nt][0];
-      a0[db] = acc[mt][nt][2];
-      a1[da] = acc[mt][nt][1];
-      a1[db] = acc[mt][nt][3];
-    }
   }
-  if (NT == 1) {  // heads 8..15 of the merge area are never written: keep them inert
-    for (int e = threadIdx.x; e < kWarps * 8; e += kThreads) {
-      mw[(e / 8) * 16 + 8 + (e % 8)] = neg_inf();
-      lw[(e / 8) * 16 + 8 + (e % 8)] = 0.f;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x < 16) {
-    const int h = threadIdx.x;
-    float M = neg_inf();
+  // each thread's fragment, thread-major: [thread][E (+4 pad)]
+  float* frag = reinterpret_cast<float*>(smem);
+  {
+    float4* mine = reinterpret_cast<float4*>(frag + threadIdx.x * (T::kE + 4));
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * 16 + h]);
-    float L = 0.f;
+    for (int mt = 0; mt < KC; ++mt)
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float f = M == neg_inf() ? 0.f : fast_exp2((mw[w * 16 + h] - M) * kLog2e);
-      fw[w * 16 + h] = f;
-      L += f * lw[w * 16 + h];
-    }
-    Ms[h] = M;
-    Ls[h] = L;
+      for (int nt = 0; nt < NT; ++nt)
+        mine[mt * NT + nt] = make_float4(acc[mt][nt][0], acc[mt][nt][1], acc[mt][nt][2],
+                                         acc[mt][nt][3]);
   }
   __syncthreads();
 
-  const bool direct = p.num_splits == 1;
-  const long long out_head0 = (long long)row * p.Hq + g * G;
-  for (int e = threadIdx.x; e < G * D; e += kThreads) {
-    const int h = e / D, d = e - (e / D) * D;
-    float a = 0.f;
+  // Warp w finishes m-tiles [w*KC/4, (w+1)*KC/4) of the fragment of its lane
+  // index: weights f_w' = exp(m_w' - M) per head, then sum over the 4 warps.
+  float fwt[NT][2][kWarps], Mh[NT][2], Lh[NT][2];
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) a += fw[w * 16 + h] * aw[(w * 16 + h) * D + d];
-    float vs = 1.f;
-    if constexpr (!FP16C) vs = p.per_channel ? p.v_scale[g * D + d] : p.v_scale[0];
-    const float M = Ms[h], L = Ls[h];
-    if (direct) {
-      float o = 0.f;
-      float lse = neg_inf();
-      if (L > 0.f) {
-        lse = M + logf(L);
-        o = (a * kInvProbScale / L) * vs;
-        if (p.sink != nullptr) o *= 1.f / (1.f + expf(p.sink[g * G + h] - lse));
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int h = nt * 8 + 2 * tig + j;
+      float M = neg_inf();
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * 16 + h]);
+      float L = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float f = M == neg_inf() ? 0.f : fast_exp2((mw[w * 16 + h] - M) * kLog2e);
+        fwt[nt][j][w] = f;
+        L += f * lw[w * 16 + h];
       }
-      reinterpret_cast<__half*>(p.out)[(out_head0 + h) * D + d] = __float2half_rn(o);
-      if (d == 0 && p.lse != nullptr) p.lse[out_head0 + h] = lse;
+      Mh[nt][j] = M;
+      Lh[nt][j] = L;
+    }
+
+  const bool direct = p.num_splits == 1;
+  const long long head0 = (long long)row * p.Hq + g * G;
+#pragma unroll
+  for (int i = 0; i < MT_PER_WARP; ++i) {
+    const int mt = warp * MT_PER_WARP + i;
+    int da, db;  // the two channels of this thread in m-tile mt
+    if constexpr (FP16C) {
+      da = 16 * mt + grp;
+      db = da + 8;
     } else {
-      const long long base = ((long long)unit * p.num_splits + split) * G + h;
-      if (L > 0.f) p.ws_acc[base * D + d] = (a * kInvProbScale) * vs;
-      if (d == 0) {
-        p.ws_m[base] = L > 0.f ? M : neg_inf();
-        p.ws_l[base] = L;
+      da = 16 * mt + 2 * grp;
+      db = da + 1;
+    }
+    const float vsa = vs_a[i], vsb = vs_b[i];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float4 v = reinterpret_cast<const float4*>(
+            frag + (w * 32 + lane) * (T::kE + 4))[mt * NT + nt];
+        a.x += fwt[nt][0][w] * v.x;  // (head 2tig,   channel da)
+        a.y += fwt[nt][1][w] * v.y;  // (head 2tig+1, channel da)
+        a.z += fwt[nt][0][w] * v.z;  // (head 2tig,   channel db)
+        a.w += fwt[nt][1][w] * v.w;  // (head 2tig+1, channel db)
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int h = nt * 8 + 2 * tig + j;
+        if (h >= G) continue;
+        const float va = j == 0 ? a.x : a.y;
+        const float vb = j == 0 ? a.z : a.w;
+        const float M = Mh[nt][j], L = Lh[nt][j];
+        if (direct) {
+          float oa = 0.f, ob = 0.f;
+          if (L > 0.f) {
+            float sc = kInvProbScale / L;
+            if (p.sink != nullptr) sc *= 1.f / (1.f + expf(p.sink[g * G + h] - (M + logf(L))));
+            oa = va * sc * vsa;
+            ob = vb * sc * vsb;
+          }
+          __half* o = reinterpret_cast<__half*>(p.out) + (head0 + h) * D;
+          if constexpr (FP16C) {
+            o[da] = __float2half_rn(oa);
+            o[db] = __float2half_rn(ob);
+          } else {
+            *reinterpret_cast<__half2*>(o + da) = __floats2half2_rn(oa, ob);
+          }
+        } else if (L > 0.f) {
+          const long long base = ((long long)unit * p.num_splits + split) * G + h;
+          float* o = p.ws_acc + base * D;
+          if constexpr (FP16C) {
+            o[da] = (va * kInvProbScale) * vsa;
+            o[db] = (vb * kInvProbScale) * vsb;
+          } else {
+            *reinterpret_cast<float2*>(o + da) =
+                make_float2((va * kInvProbScale) * vsa, (vb * kInvProbScale) * vsb);
+          }
+        }
       }
     }
+  }
+  // per-head scalars: m and l of the split, or the lse of the row
+  if (warp == 0 && grp == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int h = nt * 8 + 2 * tig + j;
+        if (h >= G) continue;
+        const float M = Mh[nt][j], L = Lh[nt][j];
+        if (direct) {
+          if (p.lse != nullptr) p.lse[head0 + h] = L > 0.f ? M + logf(L) : neg_inf();
+        } else {
+          const long long base = ((long long)unit * p.num_splits + split) * G + h;
+          p.ws_m[base] = L > 0.f ? M : neg_inf();
+          p.ws_l[base] = L;
+        }
+      }
   }
 }
 
@@ -487,7 +737,7 @@ decode_kernel(const DecodeParams p) {
 
 template <int D, int NT, bool PAGED, bool FP16C, bool PLO>
 cudaError_t run_decode(const DecodeParams& p, cudaStream_t s, int* occupancy) {
-  using T = Tile<D, FP16C>;
+  using T = Tile<D, NT, FP16C>;
   auto kern = decode_kernel<D, NT, PAGED, FP16C, PLO>;
   // the opt-in shared-memory size is a per-function attribute: set it once per device
   static std::atomic<unsigned long long> done{0};
@@ -498,14 +748,27 @@ cudaError_t run_decode(const DecodeParams& p, cudaStream_t s, int* occupancy) {
   if (!(done.load() & bit)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
     if (e != cudaSuccess) return e;
+    // ask for the largest shared-memory carveout, so that the resident CTAs per
+    // SM that the occupancy API reports are the ones the launch gets
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     done.fetch_or(bit);
   }
   if (occupancy != nullptr) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, kern, kThreads, T::kSmem);
   }
-  const dim3 grid((unsigned)(p.rows * p.Hkv), (unsigned)p.num_splits);
-  kern<<<grid, kThreads, T::kSmem, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.rows * p.Hkv), (unsigned)p.num_splits);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = T::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <bool PAGED, bool FP16C, bool PLO>

@@ -30,6 +30,7 @@ struct DecodeParams {
   int32_t rows, Hq, Hkv, G;
   int32_t max_sel;           // DSA list length (cap)
   int32_t bs, max_blocks;    // paged
+  int32_t bs_log2;           // log2(bs) when bs is a power of two, else -1
   int32_t num_splits, chunk;
   int32_t per_channel;       // 1: scales [Hkv, D]; 0: one scale
   float sigma;
