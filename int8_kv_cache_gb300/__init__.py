@@ -215,9 +215,12 @@ def dsa_prefill(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, idx,
 
 def paged_decode(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, block_table, seq_lens,
                  softmax_scale: float, head_sink=None, num_splits: int = 0, chunk: int = 0,
-                 workspace=None, out=None, lse=None, slots_out=None, flags=None, stream=None):
+                 workspace=None, out=None, lse=None, slots_out=None, flags=None, stream=None,
+                 partials_only: bool = False):
     """Paged decode.  q [B, Hq, D] fp16; caches [num_blocks, block_size, Hkv, D]
-    int8 or fp16; block_table [B, max_blocks] int32; seq_lens [B] int32 (device)."""
+    int8 or fp16; block_table [B, max_blocks] int32; seq_lens [B] int32 (device).
+    With ``partials_only`` (and num_splits > 1) only the workspace partials are
+    written and None is returned."""
     B, Hq, D = q.shape
     nb, bs, Hkv, _ = k_cache.shape
     max_blocks = block_table.shape[1]
@@ -227,7 +230,7 @@ def paged_decode(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, block_t
         cache_dtype = CACHE_FP16
     else:
         raise TypeError(f"k_cache: int8 or float16 expected, got {k_cache.dtype}")
-    if out is None:
+    if out is None and not partials_only:
         out = torch.empty_like(q)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("paged_decode", load().paged_decode(

@@ -47,11 +47,9 @@
 
 namespace i8kv {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
 constexpr int kSub = 16;  // tokens per MMA tile (the M dimension of QK^T)
 
-template <int D, int NT, bool FP16C>
+template <int D, int NT, bool FP16C, bool PAGED>
 struct Tile {
   static constexpr int kElem = FP16C ? 2 : 1;
   static constexpr int kRowBytes = D * kElem;        // one cache row of one KV head
@@ -65,26 +63,39 @@ struct Tile {
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kQStride = D + 8;             // Q' staging row (halves), padded
   static constexpr int kQBytes = 16 * kQStride * 2;
-  static constexpr int kMaskBytes = kWarps * 4 * 4;
-  // resident CTAs per SM the registers allow (16, 12 or 8 warps per SM)
-  static constexpr int kRegBlocks = D * NT >= 512 ? 2 : (D * NT >= 256 ? 3 : 4);
-  static constexpr int kPerCta = 227 * 1024 / kRegBlocks - 1024 - kQBytes - kMaskBytes;
-  // ring depth per warp: the largest of 4, 3, 2 stages that fits that budget
-  static constexpr int kStages = kWarps * 4 * kStageBytes <= kPerCta ? 4
-                               : (kWarps * 3 * kStageBytes <= kPerCta ? 3 : 2);
+  // 4-warp groups per SM the registers allow (16, 12 or 8 warps per SM) ...
+  static constexpr int kRegGroups = D * NT >= 512 ? 2 : (D * NT >= 256 ? 3 : 4);
+  static constexpr int kPerGroup = 227 * 1024 / kRegGroups - 1024 - kQBytes - 256;
+  // ... the ring depth per warp: the largest of 4, 3, 2 stages that fits ...
+  static constexpr int kStages = 4 * 4 * kStageBytes <= kPerGroup ? 4
+                               : (4 * 3 * kStageBytes <= kPerGroup ? 3 : 2);
   static constexpr int kWarpRing = kStages * kStageBytes;
+  // ... and the CTA shape: the sparse-candidate kernel puts them all in one
+  // CTA per SM (4 to 16 warps: fewer, larger CTAs for its short splits); the
+  // paged kernel keeps 4-warp CTAs, several per SM, so that the splits of
+  // sequences of very different lengths spread more evenly over the SMs.
+  static constexpr int kSmemGroups = (227 * 1024 - 1024 - kQBytes - 256) / (4 * kWarpRing);
+  static constexpr int kFitGroups = kSmemGroups < kRegGroups ? kSmemGroups : kRegGroups;
+  static constexpr int kGroups = PAGED ? 1 : kFitGroups;
+  static constexpr int kWarps = 4 * kGroups;
+  static constexpr int kThreads = 32 * kWarps;
+  static constexpr int kMaskBytes = kWarps * 4 * 4;
   static constexpr int kRingBytes = kWarps * kWarpRing;
   static constexpr int kLoopBytes = kRingBytes + kMaskBytes + kQBytes;
   // end-of-CTA merge: every thread's accumulator fragment (E floats, padded by
-  // 4 for conflict-free 16-byte access) plus m, l of the 4 warps x 16 heads
+  // 4 for conflict-free 16-byte access) plus m, l of the warps x 16 heads
   static constexpr int kE = (D / 16) * NT * 4;
-  static constexpr int kMergeBytes = (kThreads * (kE + 4) + 2 * kWarps * 16) * 4;
-  static constexpr int kSmem = kLoopBytes > kMergeBytes ? kLoopBytes : kMergeBytes;
-  static constexpr int kSmemBlocks = 227 * 1024 / (kSmem + 1024);
-  static constexpr int kMinBlocks = kSmemBlocks < kRegBlocks ? kSmemBlocks : kRegBlocks;
+  static constexpr int kMergeBytes = (kThreads * (kE + 4) + 3 * kWarps * 16 + 32) * 4;
+  // value scales of the group's KV head, staged with the query and read by the
+  // epilogue (after both the ring and the merge area)
+  static constexpr int kVsOffset = kLoopBytes > kMergeBytes ? kLoopBytes : kMergeBytes;
+  static constexpr int kSmem = kVsOffset + D * 4;
   static_assert(kChunks <= 32 && 32 % kChunks == 0, "row layout");
   static_assert(kCopies >= 1, "copy layout");
-  static_assert(kSmem <= 227 * 1024 && kMinBlocks >= 1, "shared memory");
+  static_assert(kGroups >= 1 && kThreads <= 1024, "CTA shape");
+  // resident CTAs per SM the launch bounds promise (the register budget)
+  static constexpr int kMinBlocks = PAGED ? kFitGroups : 1;
+  static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
 // XOR swizzle of the 16-byte chunks of a dense shared-memory row, so that the
@@ -100,9 +111,12 @@ __device__ __forceinline__ int swz(int r) {
 }
 
 template <int D, int NT, bool PAGED, bool FP16C, bool PLO>
-__global__ void __launch_bounds__(kThreads, (Tile<D, NT, FP16C>::kMinBlocks))
+__global__ void __launch_bounds__((Tile<D, NT, FP16C, PAGED>::kThreads),
+                                  (Tile<D, NT, FP16C, PAGED>::kMinBlocks))
 decode_kernel(const DecodeParams p) {
-  using T = Tile<D, NT, FP16C>;
+  using T = Tile<D, NT, FP16C, PAGED>;
+  constexpr int kWarps = T::kWarps;
+  constexpr int kThreads = T::kThreads;
   constexpr int KC = D / 16;  // k-chunks of QK^T and m-tiles of PV
   constexpr int SUB = T::SUB;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -117,9 +131,6 @@ decode_kernel(const DecodeParams p) {
   const int g = unit - row * p.Hkv;
   const int G = p.G;
   grid_dependency_wait();  // inputs may come from the previous kernel of the stream
-  // Let the combine launch now: its CTAs take SM slots as this grid's CTAs
-  // leave and wait there (griddepcontrol.wait) until this grid completes.
-  grid_dependents_launch();
 
   // Query rows of the group and their key scales, 8 channels per thread and
   // step, loaded first so that their latency overlaps the length and gather-key
@@ -150,25 +161,13 @@ decode_kernel(const DecodeParams p) {
     }
   }
 
-  // v_scale of the channels this thread writes in the epilogue (warp w writes
-  // m-tiles [w*KC/4, (w+1)*KC/4)), loaded now so the epilogue does not wait
-  constexpr int MT_PER_WARP = KC / kWarps;
-  float vs_a[MT_PER_WARP], vs_b[MT_PER_WARP];
-#pragma unroll
-  for (int i = 0; i < MT_PER_WARP; ++i) {
-    vs_a[i] = vs_b[i] = 1.f;
-    if constexpr (!FP16C) {
-      const int mt = warp * MT_PER_WARP + i;
-      const int da = 16 * mt + 2 * grp;  // int8 channel order of the PV fragments
-      if (p.per_channel) {
-        const float2 v2 = *reinterpret_cast<const float2*>(p.v_scale + g * D + da);
-        vs_a[i] = v2.x;
-        vs_b[i] = v2.y;
-      } else {
-        vs_a[i] = vs_b[i] = p.v_scale[0];
-      }
-    }
+  // value scales of this KV head, staged in shared memory for the epilogue
+  float* svs = reinterpret_cast<float*>(smem + T::kVsOffset);
+  if constexpr (!FP16C) {
+    for (int d = threadIdx.x; d < D; d += kThreads)
+      svs[d] = p.per_channel ? p.v_scale[g * D + d] : p.v_scale[0];
   }
+  constexpr int MT_ITERS = (KC + kWarps - 1) / kWarps;
 
   // ---------------- candidate range of this split ----------------
   // (positions fit 32 bits: the host checks num_splits * chunk <= INT32_MAX)
@@ -591,8 +590,8 @@ decode_kernel(const DecodeParams p) {
   // ---------------- merge the four warps' partials ----------------
   // (m, l) per head of every warp; l is first summed over the 8 lanes that
   // share a head pair.
-  float* mw = reinterpret_cast<float*>(smem + kThreads * (T::kE + 4) * 4);  // [4][16]
-  float* lw = mw + kWarps * 16;                                           // [4][16]
+  float* mw = reinterpret_cast<float*>(smem + kThreads * (T::kE + 4) * 4);  // [warps][16]
+  float* lw = mw + kWarps * 16;                                           // [warps][16]
   float lsum[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -627,33 +626,33 @@ decode_kernel(const DecodeParams p) {
   }
   __syncthreads();
 
-  // Warp w finishes m-tiles [w*KC/4, (w+1)*KC/4) of the fragment of its lane
-  // index: weights f_w' = exp(m_w' - M) per head, then sum over the 4 warps.
-  float fwt[NT][2][kWarps], Mh[NT][2], Lh[NT][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int h = nt * 8 + 2 * tig + j;
-      float M = neg_inf();
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * 16 + h]);
-      float L = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float f = M == neg_inf() ? 0.f : fast_exp2((mw[w * 16 + h] - M) * kLog2e);
-        fwt[nt][j][w] = f;
-        L += f * lw[w * 16 + h];
-      }
-      Mh[nt][j] = M;
-      Lh[nt][j] = L;
+  // Warp w finishes m-tiles w, w + kWarps, ... of the fragment of its lane
+  // index: weights f_w' = exp(m_w' - M) per head, then sum over the warps.
+  // per-head merge weights f[w][h] = exp(m_w - M), M and L, computed once
+  float* fws = lw + kWarps * 16;  // [warps][16]
+  float* Ms = fws + kWarps * 16;  // [16]
+  float* Ls = Ms + 16;            // [16]
+  if (threadIdx.x < 16) {
+    const int h = threadIdx.x;
+    float M = neg_inf();
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * 16 + h]);
+    float L = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = M == neg_inf() ? 0.f : fast_exp2((mw[w * 16 + h] - M) * kLog2e);
+      fws[w * 16 + h] = f;
+      L += f * lw[w * 16 + h];
     }
+    Ms[h] = M;
+    Ls[h] = L;
+  }
+  __syncthreads();
 
   const bool direct = p.num_splits == 1;
   const long long head0 = (long long)row * p.Hq + g * G;
 #pragma unroll
-  for (int i = 0; i < MT_PER_WARP; ++i) {
-    const int mt = warp * MT_PER_WARP + i;
+  for (int i = 0; i < MT_ITERS; ++i) {
+    const int mt = warp + i * kWarps;
+    if (mt >= KC) break;
     int da, db;  // the two channels of this thread in m-tile mt
     if constexpr (FP16C) {
       da = 16 * mt + grp;
@@ -662,7 +661,11 @@ decode_kernel(const DecodeParams p) {
       da = 16 * mt + 2 * grp;
       db = da + 1;
     }
-    const float vsa = vs_a[i], vsb = vs_b[i];
+    float vsa = 1.f, vsb = 1.f;
+    if constexpr (!FP16C) {
+      vsa = svs[da];
+      vsb = svs[db];
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -670,10 +673,11 @@ decode_kernel(const DecodeParams p) {
       for (int w = 0; w < kWarps; ++w) {
         const float4 v = reinterpret_cast<const float4*>(
             frag + (w * 32 + lane) * (T::kE + 4))[mt * NT + nt];
-        a.x += fwt[nt][0][w] * v.x;  // (head 2tig,   channel da)
-        a.y += fwt[nt][1][w] * v.y;  // (head 2tig+1, channel da)
-        a.z += fwt[nt][0][w] * v.z;  // (head 2tig,   channel db)
-        a.w += fwt[nt][1][w] * v.w;  // (head 2tig+1, channel db)
+        const float f0 = fws[w * 16 + nt * 8 + 2 * tig], f1 = fws[w * 16 + nt * 8 + 2 * tig + 1];
+        a.x += f0 * v.x;  // (head 2tig,   channel da)
+        a.y += f1 * v.y;  // (head 2tig+1, channel da)
+        a.z += f0 * v.z;  // (head 2tig,   channel db)
+        a.w += f1 * v.w;  // (head 2tig+1, channel db)
       }
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -681,7 +685,7 @@ decode_kernel(const DecodeParams p) {
         if (h >= G) continue;
         const float va = j == 0 ? a.x : a.y;
         const float vb = j == 0 ? a.z : a.w;
-        const float M = Mh[nt][j], L = Lh[nt][j];
+        const float M = Ms[h], L = Ls[h];
         if (direct) {
           float oa = 0.f, ob = 0.f;
           if (L > 0.f) {
@@ -719,7 +723,7 @@ decode_kernel(const DecodeParams p) {
       for (int j = 0; j < 2; ++j) {
         const int h = nt * 8 + 2 * tig + j;
         if (h >= G) continue;
-        const float M = Mh[nt][j], L = Lh[nt][j];
+        const float M = Ms[h], L = Ls[h];
         if (direct) {
           if (p.lse != nullptr) p.lse[head0 + h] = L > 0.f ? M + logf(L) : neg_inf();
         } else {
@@ -737,7 +741,7 @@ decode_kernel(const DecodeParams p) {
 
 template <int D, int NT, bool PAGED, bool FP16C, bool PLO>
 cudaError_t run_decode(const DecodeParams& p, cudaStream_t s, int* occupancy) {
-  using T = Tile<D, NT, FP16C>;
+  using T = Tile<D, NT, FP16C, PAGED>;
   auto kern = decode_kernel<D, NT, PAGED, FP16C, PLO>;
   // the opt-in shared-memory size is a per-function attribute: set it once per device
   static std::atomic<unsigned long long> done{0};
@@ -756,11 +760,11 @@ cudaError_t run_decode(const DecodeParams& p, cudaStream_t s, int* occupancy) {
     done.fetch_or(bit);
   }
   if (occupancy != nullptr) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, kern, kThreads, T::kSmem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, kern, T::kThreads, T::kSmem);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.rows * p.Hkv), (unsigned)p.num_splits);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(T::kThreads);
   cfg.dynamicSmemBytes = T::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
