@@ -59,7 +59,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--layers", type=int, default=32)
-    ap.add_argument("--extra", default="all", choices=["all", "paged", "deep", "prefill", "none"],
+    ap.add_argument("--extra", default="all",
+                    choices=["all", "paged", "deep", "prefill", "quantize", "none"],
                     help="which other workloads to measure besides the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
@@ -399,7 +400,35 @@ def extra_configs(torch, K, W, np, dev, stream, peaks, args):
             res[f"deep_context_{cache}"] = _deep(torch, K, W, np, t, dev, bench_graph, hbm, cache)
     if args.extra in ("all", "prefill"):
         res["sparse_prefill"] = _prefill(torch, K, W, np, t, bench_graph, peaks)
+    if args.extra in ("all", "quantize"):
+        res["quantize_on_write"] = _quantize(torch, K, np, t, dev, bench_graph, hbm)
     return res
+
+
+def _quantize(torch, K, np, t, dev, bench_graph, hbm):
+    """Quantize-on-write of one 8192-token prefill chunk (8 KV heads, D 128)
+    into a paged INT8 cache with per-channel scales, R rotating destinations."""
+    rng = np.random.default_rng(0)
+    T, Hkv, Dh, bs = 8192, 8, 128, 16
+    kn = t((rng.standard_normal((T, Hkv, Dh))).astype(np.float16))
+    vn = t((rng.standard_normal((T, Hkv, Dh))).astype(np.float16))
+    ks = t(np.exp(rng.uniform(-4, -2, size=(Hkv, Dh))).astype(np.float32))
+    vs = t(np.exp(rng.uniform(-4, -2, size=(Hkv, Dh))).astype(np.float32))
+    R = 8
+    nb = T // bs
+    caches = [dict(k=torch.zeros((nb, bs, Hkv, Dh), dtype=torch.int8, device=dev),
+                   v=torch.zeros((nb, bs, Hkv, Dh), dtype=torch.int8, device=dev),
+                   s=t(rng.permutation(nb * bs).astype(np.int32))) for _ in range(R)]
+
+    def fn():
+        for c in caches:
+            K.reshape_and_cache(kn, vn, c["s"], c["k"], c["v"], ks, vs, 2)
+    sec = bench_graph(fn, R, reps=50)
+    byts = 2 * T * Hkv * Dh * 2 + 2 * T * Hkv * Dh + T * 4 + 2 * Hkv * Dh * 4
+    return dict(workload="quantize-on-write: 8192 new tokens x 8 KV heads x head_dim 128 (fp16) "
+                         "into a paged INT8 cache at a permuted slot mapping, per-channel scales",
+                us_per_call=round(sec * 1e6, 2), gbs=round(byts / sec / 1e9, 1),
+                frac_of_hbm=round(byts / sec / 1e9 / hbm, 4), bytes_per_call=byts)
 
 
 def _paged(torch, K, W, np, t, dev, bench_graph, hbm):

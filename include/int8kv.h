@@ -82,6 +82,7 @@ typedef enum {
                                       query of that CTA is not exact to the stated bound      */
 #define I8KV_FLAG_BAD_BLOCK 0x4u   /* a block-table entry inside the live length is outside
                                       [0, num_blocks): those tokens were skipped              */
+#define I8KV_FLAG_BAD_SLOT 0x8u    /* reshape_and_cache: a slot >= num_slots was skipped      */
 
 /* Human-readable name of a status code (static storage). */
 const char* i8kv_status_string(int status);
@@ -244,6 +245,30 @@ i8kv_status paged_decode(const uint16_t* q, const void* k_cache, const void* v_c
 i8kv_status split_combine(const float* acc, const float* m, const float* l, int32_t units,
                           int32_t num_splits, int32_t Hq, int32_t Hkv, int32_t D,
                           const float* head_sink, uint16_t* out, float* lse, void* stream);
+
+/*
+ * reshape_and_cache -- quantize-on-write of new key / value rows into a paged
+ * INT8 cache (onnxruntime PR 29912, CUDA kernels: "ReshapeAndCache quantizes on
+ * write").  For every new token n and KV head g, the cache row
+ * (slot_mapping[n], g) receives
+ *     code[d] = clamp(round_half_even(x[d] / scale), -127, 127)
+ * with scale = k_scale / v_scale per tensor ([1]) or per channel ([Hkv, D]); the
+ * quotient is an IEEE fp32 division of the fp16 value widened to fp32; a NaN
+ * quotient stores 0.
+ *   k_new, v_new   [num_tokens, Hkv, D] fp16, device
+ *   slot_mapping   [num_tokens] int32, device: row of the flattened cache
+ *                  (block * block_size + offset); < 0: skipped (padding);
+ *                  >= num_slots: skipped and I8KV_FLAG_BAD_SLOT raised
+ *   k_cache, v_cache [num_slots, Hkv, D] int8 (a paged cache [num_blocks,
+ *                  block_size, Hkv, D] with num_slots = num_blocks * block_size)
+ *   D a multiple of 8; caches, rows and per-channel scales 16-byte aligned.
+ * Scales must be finite and positive (not checked on the device).
+ */
+i8kv_status reshape_and_cache(const uint16_t* k_new, const uint16_t* v_new,
+                              const int32_t* slot_mapping, int32_t num_tokens, int32_t Hkv,
+                              int32_t D, int8_t* k_cache, int8_t* v_cache, int64_t num_slots,
+                              const float* k_scale, const float* v_scale, int32_t scale_kind,
+                              uint32_t* flags, void* stream);
 
 /*
  * dsa_decode_static_workspace -- dsa_decode without a caller-supplied

@@ -19,7 +19,8 @@ import torch
 __all__ = [
     "Int8KVError", "load", "library_path", "split_geometry", "split_workspace_bytes",
     "decode_plan", "dsa_decode", "dsa_prefill", "paged_decode", "split_combine", "int8_to_fp16",
-    "dsa_decode_static_workspace", "STATIC_WORKSPACE_BYTES",
+    "dsa_decode_static_workspace", "STATIC_WORKSPACE_BYTES", "reshape_and_cache",
+    "FLAG_BAD_SLOT",
     "SCALE_PER_TENSOR", "SCALE_PER_CHANNEL", "CACHE_INT8", "CACHE_FP16", "GEOM_WAVE",
     "GEOM_POW2_TILES", "PATH_DSA", "PATH_PAGED", "MAX_SPLITS", "FLAG_LEN_CLAMPED",
     "FLAG_QUERY_RANGE", "FLAG_BAD_BLOCK",
@@ -37,6 +38,7 @@ MAX_SPLITS = 32
 FLAG_LEN_CLAMPED = 0x1
 FLAG_QUERY_RANGE = 0x2
 FLAG_BAD_BLOCK = 0x4
+FLAG_BAD_SLOT = 0x8
 STATIC_WORKSPACE_BYTES = 4 * 1024 * 1024
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -69,6 +71,8 @@ _SIGNATURES = {
     "split_combine": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                _c_vp, _c_vp, _c_vp, _c_vp]),
     "int8_to_fp16": (_c_i32, [_c_vp, _c_vp, _c_i64, _c_vp]),
+    "reshape_and_cache": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_i32, _c_i32, _c_i32, _c_vp, _c_vp,
+                                   _c_i64, _c_vp, _c_vp, _c_i32, _c_vp, _c_vp]),
     "dsa_decode_static_workspace": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i32, _c_vp,
                                              _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_i32,
                                              _c_f32, _c_vp, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp,
@@ -257,6 +261,20 @@ def split_combine(acc, m, l, Hq: int, Hkv: int, head_sink=None, out=None, lse=No
         units, ns, Hq, Hkv, D, _t(head_sink, torch.float32, "head_sink"),
         _t(out, torch.float16, "out"), _t(lse, torch.float32, "lse"), _stream(stream)))
     return out
+
+
+def reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                      scale_kind: int, flags=None, stream=None):
+    """Quantize new rows k_new / v_new [T, Hkv, D] (fp16) into the INT8 caches
+    ([num_slots, Hkv, D] or [num_blocks, block_size, Hkv, D]) at slot_mapping [T]."""
+    T, Hkv, D = k_new.shape
+    num_slots = k_cache.numel() // (Hkv * D)
+    _check("reshape_and_cache", load().reshape_and_cache(
+        _t(k_new, torch.float16, "k_new"), _t(v_new, torch.float16, "v_new"),
+        _t(slot_mapping, torch.int32, "slot_mapping"), T, Hkv, D,
+        _t(k_cache, torch.int8, "k_cache"), _t(v_cache, torch.int8, "v_cache"), num_slots,
+        _t(k_scale, torch.float32, "k_scale"), _t(v_scale, torch.float32, "v_scale"), scale_kind,
+        _t(flags, torch.int32, "flags"), _stream(stream)))
 
 
 def int8_to_fp16(x, out=None, stream=None):

@@ -415,6 +415,28 @@ i8kv_status split_combine(const float* acc, const float* m, const float* l, int3
   return e == cudaSuccess ? I8KV_OK : cuda_fail(e);
 }
 
+i8kv_status reshape_and_cache(const uint16_t* k_new, const uint16_t* v_new,
+                              const int32_t* slot_mapping, int32_t num_tokens, int32_t Hkv,
+                              int32_t D, int8_t* k_cache, int8_t* v_cache, int64_t num_slots,
+                              const float* k_scale, const float* v_scale, int32_t scale_kind,
+                              uint32_t* flags, void* stream) {
+  if (num_tokens < 0 || Hkv < 1 || D < 8 || num_slots < 0) return I8KV_EINVAL;
+  if (D % 8 != 0) return I8KV_EUNSUPPORTED;
+  i8kv_status st = check_scales(k_scale, v_scale, scale_kind);
+  if (st != I8KV_OK) return st;
+  if (num_tokens > 0 && (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr ||
+                         k_cache == nullptr || v_cache == nullptr))
+    return I8KV_EINVAL;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(slot_mapping, 4) || !aligned(flags, 4))
+    return I8KV_EALIGN;
+  if (num_tokens == 0) return I8KV_OK;
+  cudaError_t e = i8kv::launch_reshape_and_cache(
+      k_new, v_new, slot_mapping, num_tokens, Hkv, D, k_cache, v_cache, num_slots, k_scale, v_scale,
+      scale_kind == I8KV_SCALE_PER_CHANNEL, flags, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? I8KV_OK : cuda_fail(e);
+}
+
 i8kv_status int8_to_fp16(const int8_t* in, uint16_t* out, int64_t n, void* stream) {
   if (n < 0 || n % 4 != 0) return I8KV_EINVAL;
   if (n > 0 && (in == nullptr || out == nullptr)) return I8KV_EINVAL;

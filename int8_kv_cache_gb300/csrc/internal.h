@@ -64,5 +64,10 @@ cudaError_t launch_combine(const float* acc, const float* m, const float* l, int
                            int num_splits, int Hq, int Hkv, int D, const float* sink, void* out,
                            float* lse, cudaStream_t stream);
 cudaError_t launch_int8_to_fp16(const int8_t* in, uint16_t* out, int64_t n, cudaStream_t stream);
+cudaError_t launch_reshape_and_cache(const void* k_new, const void* v_new, const int32_t* slots,
+                                     int num_tokens, int Hkv, int D, int8_t* k_cache,
+                                     int8_t* v_cache, long long num_slots, const float* ks,
+                                     const float* vs, int per_channel, uint32_t* flags,
+                                     cudaStream_t stream);
 
 }  // namespace i8kv

@@ -146,3 +146,20 @@ def test_zero_work_is_a_no_op(lib):
     assert _dsa(lib, S=0) == 0
     assert lib.split_combine(P, P, P, 0, 4, 8, 2, 128, None, P, None, None) == 0
     assert lib.int8_to_fp16(P, P, 0, None) == 0
+
+
+def test_reshape_and_cache_validation(lib):
+    def call(**kw):
+        a = dict(k=P, v=P, slots=P, T=4, Hkv=2, D=64, kc=P, vc=P, ns=100, ks=P, vs=P, kind=1,
+                 flags=None, stream=None)
+        a.update(kw)
+        return lib.reshape_and_cache(a["k"], a["v"], a["slots"], a["T"], a["Hkv"], a["D"], a["kc"],
+                                     a["vc"], a["ns"], a["ks"], a["vs"], a["kind"], a["flags"],
+                                     a["stream"])
+    assert call(D=60) == 2      # not a multiple of 8
+    assert call(D=4) == 1
+    assert call(T=-1) == 1
+    assert call(kind=5) == 1
+    assert call(slots=None) == 1
+    assert call(kc=P8) == 3
+    assert call(T=0) == 0       # nothing to do, nothing enqueued

@@ -295,7 +295,7 @@ def random_paged(seed: int, B: int, Hq: int, Hkv: int, D: int, bs: int, max_bloc
     rng = make_rng(seed)
     lens = np.asarray(lens, dtype=np.int32)
     cap = max_blocks * bs
-    nblk = np.minimum((np.maximum(lens, 0) + bs - 1) // bs, max_blocks)
+    nblk = np.minimum((np.maximum(lens, 0) + bs) // bs, max_blocks)  # room for one more token
     P = int(nblk.sum()) + spare_blocks
     q = _normal(rng, (B, Hq, D)).astype(np.float16)
     k = _normal(rng, (P, bs, Hkv, D))
