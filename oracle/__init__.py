@@ -16,6 +16,8 @@ __all__ = [
     "paged_split_partials", "partial", "sparse_attention", "sparse_candidates",
     "sparse_split_partials", "MODE_POW2_TILES", "MODE_WAVE", "split_geometry",
 ]
+from .attention import scores, window_chunk_bounds, window_span, window_start  # noqa: E402
 from .quantize import quantize_rows, reshape_and_cache  # noqa: E402
 
-__all__ += ["quantize_rows", "reshape_and_cache"]
+__all__ += ["quantize_rows", "reshape_and_cache", "scores", "window_chunk_bounds",
+            "window_span", "window_start"]

@@ -41,6 +41,20 @@ them: fp16 queries, int8 codes, fp32 scales):
 An empty candidate set gives O = 0 and lse = -inf (reading: the pages do not
 say; a split with no tiles publishes an empty partial [PR 33707 §2 tests], and
 the whole-row case is taken the same way).
+
+7. Paged-decode variants [PR 29912, CUDA kernels: the paged decode kernel has
+   native head-sink, softcap, sliding-window and on-the-fly dequantisation].
+   The pages name both options without defining them; the readings taken are
+   the usual ones of that runtime's attention operators:
+   - softcap c > 0: every scaled score s becomes c * tanh(s / c) before the
+     softmax (c = 0: off).  The sink logit is not capped.
+   - sliding window w >= 0: the decode query sits at position L - 1 (L the
+     live length) and attends positions [max(0, L - 1 - w), L), i.e. itself
+     and the w positions before it (w = -1: off).
+   In the split form with a window, chunks are counted from the window start
+   rounded down to a multiple of 16 tokens (the tile granule, so that no tile
+   straddles a block), and the split geometry is taken over the span
+   min(cap, w + 16) instead of cap; both depend on w only, never on L.
 """
 from __future__ import annotations
 
@@ -77,14 +91,23 @@ def dequantize(codes: np.ndarray, scale: np.ndarray, scale_kind: int, kv_head: i
 # 4./5. one query head against a candidate set
 # --------------------------------------------------------------------------
 
-def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, sigma: float) -> Tuple[np.ndarray, float]:
+def scores(q: np.ndarray, K: np.ndarray, sigma: float, softcap: float = 0.0) -> np.ndarray:
+    """s_t = sigma * <q, K_t>, then c * tanh(s_t / c) when softcap c > 0."""
+    s = sigma * (K @ np.asarray(q, dtype=np.float64))
+    if softcap > 0.0:
+        s = softcap * np.tanh(s / softcap)
+    return s
+
+
+def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, sigma: float,
+           softcap: float = 0.0) -> Tuple[np.ndarray, float]:
     """Softmax attention of one query vector ``q[D]`` over rows ``K[T, D]``,
     ``V[T, D]`` (float64).  Returns (O[D], lse)."""
     q = np.asarray(q, dtype=np.float64)
     T = K.shape[0]
     if T == 0:
         return np.zeros(V.shape[1], dtype=np.float64), -math.inf
-    s = sigma * (K @ q)
+    s = scores(q, K, sigma, softcap)
     m = float(np.max(s))
     w = np.exp(s - m)
     Z = float(np.sum(w))
@@ -114,18 +137,32 @@ def sparse_candidates(idx_row: np.ndarray, N: int) -> np.ndarray:
     return r[(r >= 0) & (r < N)]
 
 
-def paged_slots(block_table: np.ndarray, seq_lens: np.ndarray, bs: int) -> np.ndarray:
-    """Physical row of every token position: ``out[b, t] = bt[b, t//bs]*bs + t%bs``
-    for t < min(seq_len_b, cap), else -1.  Shape [B, cap], int64."""
+def paged_slots(block_table: np.ndarray, seq_lens: np.ndarray, bs: int,
+                window: int = -1) -> np.ndarray:
+    """Physical row of every attended token position: ``out[b, t] =
+    bt[b, t//bs]*bs + t%bs`` for window_start <= t < min(seq_len_b, cap), else
+    -1.  Shape [B, cap], int64."""
     bt = np.asarray(block_table, dtype=np.int64)
     B, mb = bt.shape
     cap = mb * bs
     out = np.full((B, cap), -1, dtype=np.int64)
     for b in range(B):
         L = live_length(int(seq_lens[b]), cap)
-        for t in range(L):
+        for t in range(window_start(L, window), L):
             out[b, t] = bt[b, t // bs] * bs + t % bs
     return out
+
+
+def window_start(L: int, window: int) -> int:
+    """First attended position of a decode query at position L - 1: L - 1 - w
+    (not below 0) with a window w >= 0, else 0."""
+    return max(0, L - 1 - window) if window >= 0 else 0
+
+
+def window_span(cap: int, window: int) -> int:
+    """Positions the splits of a windowed decode must cover: the window's w + 1
+    positions plus up to 15 before its start (chunks start 16-aligned)."""
+    return min(cap, window + 16) if window >= 0 else cap
 
 
 def live_length(seq_len: int, cap: int) -> int:
@@ -161,7 +198,7 @@ def sparse_attention(q, k_codes, v_codes, k_scale, v_scale, scale_kind, idx, sig
 
 
 def paged_attention(q, k_cache, v_cache, k_scale, v_scale, scale_kind, block_table, seq_lens,
-                    sigma, sink=None):
+                    sigma, sink=None, softcap: float = 0.0, window: int = -1):
     """Paged-cache decode: one query row per sequence.
 
     q [B, Hq, D]; caches [num_blocks, bs, Hkv, D]; block_table [B, max_blocks].
@@ -172,7 +209,7 @@ def paged_attention(q, k_cache, v_cache, k_scale, v_scale, scale_kind, block_tab
     G = Hq // Hkv
     kf = k_cache.reshape(nb * bs, Hkv, D)
     vf = v_cache.reshape(nb * bs, Hkv, D)
-    slots = paged_slots(block_table, seq_lens, bs)
+    slots = paged_slots(block_table, seq_lens, bs, window)
     O = np.zeros((B, Hq, D), dtype=np.float64)
     L = np.full((B, Hq), -math.inf, dtype=np.float64)
     for b in range(B):
@@ -181,7 +218,7 @@ def paged_attention(q, k_cache, v_cache, k_scale, v_scale, scale_kind, block_tab
             K = dequantize(kf[rows, g, :], k_scale, scale_kind, g)
             V = dequantize(vf[rows, g, :], v_scale, scale_kind, g)
             for h in range(g * G, (g + 1) * G):
-                o, lse = attend(q[b, h].astype(np.float64), K, V, sigma)
+                o, lse = attend(q[b, h].astype(np.float64), K, V, sigma, softcap)
                 O[b, h] = apply_head_sink(o, lse, _sink_of(sink, h))
                 L[b, h] = lse
     return O, L
@@ -191,13 +228,13 @@ def paged_attention(q, k_cache, v_cache, k_scale, v_scale, scale_kind, block_tab
 # 6. split form: partials and the log-sum-exp combine
 # --------------------------------------------------------------------------
 
-def partial(q: np.ndarray, K: np.ndarray, V: np.ndarray, sigma: float):
+def partial(q: np.ndarray, K: np.ndarray, V: np.ndarray, sigma: float, softcap: float = 0.0):
     """Un-normalised partial of one chunk: (m, l, a) with a = sum e^(s-m) V.
     An empty chunk gives (-inf, 0, 0)."""
     D = V.shape[1]
     if K.shape[0] == 0:
         return -math.inf, 0.0, np.zeros(D, dtype=np.float64)
-    s = sigma * (K @ np.asarray(q, dtype=np.float64))
+    s = scores(q, K, sigma, softcap)
     m = float(np.max(s))
     w = np.exp(s - m)
     return m, float(np.sum(w)), w @ V
@@ -257,9 +294,27 @@ def sparse_split_partials(q, k_codes, v_codes, k_scale, v_scale, scale_kind, idx
     return m, l, a
 
 
+def window_chunk_bounds(L: int, window: int, chunk: int,
+                        num_splits: int) -> List[Tuple[int, int]]:
+    """Split k of a windowed row covers [b16 + k*chunk, b16 + (k+1)*chunk)
+    intersected with [start, L), where start = window_start(L, window) and b16
+    is start rounded down to a multiple of 16."""
+    start = window_start(L, window)
+    b16 = start - start % 16
+    out = []
+    for k in range(num_splits):
+        lo = max(start, min(b16 + k * chunk, L))
+        hi = max(lo, min(b16 + (k + 1) * chunk, L))
+        out.append((lo, hi))
+    return out
+
+
 def paged_split_partials(q, k_cache, v_cache, k_scale, v_scale, scale_kind, block_table,
-                         seq_lens, sigma, num_splits: int, chunk: int):
-    """Partials of the split form over token positions of each sequence."""
+                         seq_lens, sigma, num_splits: int, chunk: int, softcap: float = 0.0,
+                         window: int = -1):
+    """Partials of the split form over token positions of each sequence
+    (chunks from position 0, or from the window start as in
+    ``window_chunk_bounds``)."""
     B, Hq, D = q.shape
     nb, bs, Hkv, _ = k_cache.shape
     G = Hq // Hkv
@@ -272,13 +327,16 @@ def paged_split_partials(q, k_cache, v_cache, k_scale, v_scale, scale_kind, bloc
     a = np.zeros((B, Hq, num_splits, D))
     for b in range(B):
         Lb = live_length(int(seq_lens[b]), cap)
-        for k, (lo, hi) in enumerate(chunk_bounds(Lb, chunk, num_splits)):
+        bounds = (window_chunk_bounds(Lb, window, chunk, num_splits) if window >= 0
+                  else chunk_bounds(Lb, chunk, num_splits))
+        for k, (lo, hi) in enumerate(bounds):
             rows = slots[b, lo:hi]
             for g in range(Hkv):
                 K = dequantize(kf[rows, g, :], k_scale, scale_kind, g)
                 V = dequantize(vf[rows, g, :], v_scale, scale_kind, g)
                 for h in range(g * G, (g + 1) * G):
-                    m[b, h, k], l[b, h, k], a[b, h, k] = partial(q[b, h], K, V, sigma)
+                    m[b, h, k], l[b, h, k], a[b, h, k] = partial(q[b, h], K, V, sigma,
+                                                                 softcap)
     return m, l, a
 
 
