@@ -60,7 +60,7 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--extra", default="all",
-                    choices=["all", "paged", "deep", "prefill", "quantize", "none"],
+                    choices=["all", "paged", "variants", "deep", "prefill", "quantize", "none"],
                     help="which other workloads to measure besides the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
@@ -395,6 +395,11 @@ def extra_configs(torch, K, W, np, dev, stream, peaks, args):
 
     if args.extra in ("all", "paged"):
         res["paged_decode"] = _paged(torch, K, W, np, t, dev, bench_graph, hbm)
+    if args.extra in ("all", "paged", "variants"):
+        res["paged_decode_softcap"] = _paged(torch, K, W, np, t, dev, bench_graph, hbm,
+                                             softcap=30.0)
+        res["paged_decode_window"] = _paged(torch, K, W, np, t, dev, bench_graph, hbm,
+                                            window=1023)
     if args.extra in ("all", "deep"):
         for cache in ("int8", "fp16"):
             res[f"deep_context_{cache}"] = _deep(torch, K, W, np, t, dev, bench_graph, hbm, cache)
@@ -431,8 +436,9 @@ def _quantize(torch, K, np, t, dev, bench_graph, hbm):
                 frac_of_hbm=round(byts / sec / 1e9 / hbm, 4), bytes_per_call=byts)
 
 
-def _paged(torch, K, W, np, t, dev, bench_graph, hbm):
-    """Paged decode: 16 sequences, lengths U[512, 8192], 32/8 heads, D 128."""
+def _paged(torch, K, W, np, t, dev, bench_graph, hbm, softcap=0.0, window=-1):
+    """Paged decode: 16 sequences, lengths U[512, 8192], 32/8 heads, D 128
+    (optionally with a softcap and a sliding window)."""
     c = W.paged_decode(seed=0)
     B, Hq, Dh = c.q.shape
     nb, bs, Hkv, _ = c.k_cache.shape
@@ -441,23 +447,31 @@ def _paged(torch, K, W, np, t, dev, bench_graph, hbm):
     copies = [dict(k=t(c.k_cache), v=t(c.v_cache)) for _ in range(R)]
     q, ks, vs = t(c.q), t(c.k_scale), t(c.v_scale)
     bt, lens, sink = t(c.block_table), t(c.seq_lens), t(c.sink)
-    ns, chunk, wsb, wave = K.decode_plan(K.PATH_PAGED, K.CACHE_INT8, cap, B, Hq, Hkv, Dh,
-                                         K.GEOM_WAVE)
+    ns, chunk, wsb, wave = K.decode_plan(K.PATH_PAGED, K.CACHE_INT8, K.window_span(cap, window),
+                                         B, Hq, Hkv, Dh, K.GEOM_WAVE)
     ws = torch.empty(max(wsb // 4, 4), dtype=torch.float32, device=dev)
     out = torch.empty_like(q)
-    tokens = int(c.seq_lens.sum())
-    byts = tokens * Hkv * Dh * 2 + B * Hq * Dh * 4 + int(np.ceil(c.seq_lens / bs).sum()) * 4 \
-        + 2 * Hkv * Dh * 4
+    live = np.minimum(c.seq_lens, window + 1) if window >= 0 else c.seq_lens
+    tokens = int(live.sum())
+    first = (c.seq_lens - live) // bs
+    blocks = int(((c.seq_lens + bs - 1) // bs - first).sum())
+    byts = tokens * Hkv * Dh * 2 + B * Hq * Dh * 4 + blocks * 4 + 2 * Hkv * Dh * 4
 
     def fn():
         for x in copies:
             K.paged_decode(q, x["k"], x["v"], ks, vs, c.scale_kind, bt, lens, c.sigma, sink,
-                           num_splits=ns, chunk=chunk, workspace=ws, out=out)
+                           num_splits=ns, chunk=chunk, workspace=ws, out=out, softcap=softcap,
+                           window=window)
     sec = bench_graph(fn, R)
+    opts = ""
+    if softcap > 0:
+        opts += f", softcap {softcap:g}"
+    if window >= 0:
+        opts += f", sliding window {window} (attended sum {tokens})"
     return dict(
         workload="paged INT8 decode: 16 sequences, lengths U[512,8192] (sum %d), block 16, "
-                 "permuted block table, 32/8 heads, head_dim 128, per-channel scales, sink"
-                 % tokens,
+                 "permuted block table, 32/8 heads, head_dim 128, per-channel scales, sink%s"
+                 % (int(c.seq_lens.sum()), opts),
         us_per_call=round(sec * 1e6, 2), gbs=round(byts / sec / 1e9, 1),
         frac_of_hbm=round(byts / sec / 1e9 / hbm, 4), bytes_per_call=byts, num_splits=ns,
         chunk=chunk, wave_ctas=wave, rotating_copies=R)

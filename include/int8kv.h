@@ -230,6 +230,39 @@ i8kv_status paged_decode(const uint16_t* q, const void* k_cache, const void* v_c
                          float* lse, int32_t* slots_out, uint32_t* flags, void* stream);
 
 /*
+ * paged_decode_ex -- paged_decode with the two score options the same page
+ * lists for that kernel (onnxruntime PR 29912, CUDA kernels: "native head-sink,
+ * softcap, sliding-window and on-the-fly cache dequantization").  The page
+ * names them without a definition; the meanings taken are:
+ *   softcap  >= 0, finite.  > 0: each scaled score s becomes
+ *            softcap * tanh(s / softcap) before the softmax; 0: off.  The
+ *            head-sink logit is not capped.
+ *   window   >= -1.  >= 0: the query of sequence b (at position L - 1, L its
+ *            clamped live length) attends positions [max(0, L-1-window), L):
+ *            itself and the window positions before it; -1: off.
+ * With a window the splits count their chunks from the window start rounded
+ * down to a multiple of 16, and num_splits * chunk must cover
+ * I8KV_WINDOW_SPAN(cap, window) (not cap); num_splits = 0 plans over that span
+ * (decode_plan with cap = I8KV_WINDOW_SPAN(cap, window) gives the same
+ * geometry).  slots_out then holds -1 outside the window.  Other arguments,
+ * errors and work as for paged_decode; softcap < 0, non-finite, or
+ * window < -1 -> I8KV_EINVAL.
+ */
+#define I8KV_WINDOW_SPAN(cap, window)                                              \
+  ((window) < 0 || (int64_t)(cap) <= (int64_t)(window) + 16 ? (int64_t)(cap)      \
+                                                            : (int64_t)(window) + 16)
+
+i8kv_status paged_decode_ex(const uint16_t* q, const void* k_cache, const void* v_cache,
+                            int32_t cache_dtype, const float* k_scale, const float* v_scale,
+                            int32_t scale_kind, const int32_t* block_table,
+                            const int32_t* seq_lens, int32_t B, int32_t Hq, int32_t Hkv,
+                            int32_t D, int32_t block_size, int32_t max_blocks, int64_t num_blocks,
+                            float softmax_scale, const float* head_sink, float softcap,
+                            int32_t window, int32_t num_splits, int32_t chunk, void* workspace,
+                            size_t workspace_bytes, uint16_t* out, float* lse,
+                            int32_t* slots_out, uint32_t* flags, void* stream);
+
+/*
  * split_combine -- log-sum-exp merge of split partials plus the head sink
  * (onnxruntime PR 33707 §2: the merge kernel; PR 29912: ApplyHeadSink):
  *   M = max_k m_k;  L = sum_k l_k exp(m_k - M);  O = sum_k acc_k exp(m_k - M) / L

@@ -20,7 +20,7 @@ __all__ = [
     "Int8KVError", "load", "library_path", "split_geometry", "split_workspace_bytes",
     "decode_plan", "dsa_decode", "dsa_prefill", "paged_decode", "split_combine", "int8_to_fp16",
     "dsa_decode_static_workspace", "STATIC_WORKSPACE_BYTES", "reshape_and_cache",
-    "FLAG_BAD_SLOT",
+    "FLAG_BAD_SLOT", "paged_decode_ex", "window_span",
     "SCALE_PER_TENSOR", "SCALE_PER_CHANNEL", "CACHE_INT8", "CACHE_FP16", "GEOM_WAVE",
     "GEOM_POW2_TILES", "PATH_DSA", "PATH_PAGED", "MAX_SPLITS", "FLAG_LEN_CLAMPED",
     "FLAG_QUERY_RANGE", "FLAG_BAD_BLOCK",
@@ -68,6 +68,10 @@ _SIGNATURES = {
                               _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_f32,
                               _c_vp, _c_i32, _c_i32, _c_vp, _c_sz, _c_vp, _c_vp, _c_vp, _c_vp,
                               _c_vp]),
+    "paged_decode_ex": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_i32, _c_vp, _c_vp, _c_i32, _c_vp,
+                                 _c_vp, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64,
+                                 _c_f32, _c_vp, _c_f32, _c_i32, _c_i32, _c_i32, _c_vp, _c_sz,
+                                 _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
     "split_combine": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                _c_vp, _c_vp, _c_vp, _c_vp]),
     "int8_to_fp16": (_c_i32, [_c_vp, _c_vp, _c_i64, _c_vp]),
@@ -217,14 +221,20 @@ def dsa_prefill(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, idx,
     return out
 
 
+def window_span(cap: int, window: int) -> int:
+    """Positions the splits of a windowed paged decode cover (I8KV_WINDOW_SPAN)."""
+    return cap if window < 0 or cap <= window + 16 else window + 16
+
+
 def paged_decode(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, block_table, seq_lens,
                  softmax_scale: float, head_sink=None, num_splits: int = 0, chunk: int = 0,
                  workspace=None, out=None, lse=None, slots_out=None, flags=None, stream=None,
-                 partials_only: bool = False):
+                 partials_only: bool = False, softcap: float = 0.0, window: int = -1):
     """Paged decode.  q [B, Hq, D] fp16; caches [num_blocks, block_size, Hkv, D]
     int8 or fp16; block_table [B, max_blocks] int32; seq_lens [B] int32 (device).
     With ``partials_only`` (and num_splits > 1) only the workspace partials are
-    written and None is returned."""
+    written and None is returned.  ``softcap`` > 0 or ``window`` >= 0 go through
+    the C entry point paged_decode_ex, the defaults through paged_decode."""
     B, Hq, D = q.shape
     nb, bs, Hkv, _ = k_cache.shape
     max_blocks = block_table.shape[1]
@@ -237,17 +247,27 @@ def paged_decode(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, block_t
     if out is None and not partials_only:
         out = torch.empty_like(q)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check("paged_decode", load().paged_decode(
-        _t(q, torch.float16, "q"), _t(k_cache, k_cache.dtype, "k_cache"),
-        _t(v_cache, k_cache.dtype, "v_cache"), cache_dtype, _t(k_scale, torch.float32, "k_scale"),
-        _t(v_scale, torch.float32, "v_scale"), scale_kind,
-        _t(block_table, torch.int32, "block_table"), _t(seq_lens, torch.int32, "seq_lens"), B,
-        Hq, Hkv, D, bs, max_blocks, nb, softmax_scale, _t(head_sink, torch.float32, "head_sink"),
-        num_splits, chunk, _t(workspace, None, "workspace"), ws_bytes,
-        _t(out, torch.float16, "out"), _t(lse, torch.float32, "lse"),
-        _t(slots_out, torch.int32, "slots_out"), _t(flags, torch.int32, "flags"),
-        _stream(stream)))
+    head = (_t(q, torch.float16, "q"), _t(k_cache, k_cache.dtype, "k_cache"),
+            _t(v_cache, k_cache.dtype, "v_cache"), cache_dtype,
+            _t(k_scale, torch.float32, "k_scale"), _t(v_scale, torch.float32, "v_scale"),
+            scale_kind, _t(block_table, torch.int32, "block_table"),
+            _t(seq_lens, torch.int32, "seq_lens"), B, Hq, Hkv, D, bs, max_blocks, nb,
+            softmax_scale, _t(head_sink, torch.float32, "head_sink"))
+    tail = (num_splits, chunk, _t(workspace, None, "workspace"), ws_bytes,
+            _t(out, torch.float16, "out"), _t(lse, torch.float32, "lse"),
+            _t(slots_out, torch.int32, "slots_out"), _t(flags, torch.int32, "flags"),
+            _stream(stream))
+    if softcap == 0.0 and window == -1:
+        _check("paged_decode", load().paged_decode(*head, *tail))
+    else:
+        _check("paged_decode_ex", load().paged_decode_ex(*head, float(softcap), int(window),
+                                                         *tail))
     return out
+
+
+def paged_decode_ex(*args, softcap: float = 0.0, window: int = -1, **kw):
+    """paged_decode with the softcap / sliding-window options (same arguments)."""
+    return paged_decode(*args, softcap=softcap, window=window, **kw)
 
 
 def split_combine(acc, m, l, Hq: int, Hkv: int, head_sink=None, out=None, lse=None,

@@ -121,11 +121,14 @@ i8kv_status plan(const KernelKey& key, int64_t cap, int32_t units, int32_t mode,
 
 // Geometry given by the caller: num_splits in [1, 32], chunk a positive
 // multiple of 16 with num_splits * chunk >= cap.
-i8kv_status check_geometry(int64_t cap, int32_t ns, int32_t chunk) {
+// span: the positions the splits must cover (cap, or the window span);
+// base_max: the largest first position of split 0 (0, or cap with a window).
+i8kv_status check_geometry(int64_t span, int32_t ns, int32_t chunk, int64_t base_max = 0) {
   if (ns < 1 || ns > I8KV_MAX_SPLITS) return I8KV_EINVAL;
   if (chunk < 16 || chunk % 16 != 0) return I8KV_EINVAL;
-  if (static_cast<int64_t>(ns) * chunk < cap) return I8KV_EINVAL;
-  if (static_cast<int64_t>(ns) * chunk > INT32_MAX) return I8KV_EINVAL;  // positions are 32-bit
+  if (static_cast<int64_t>(ns) * chunk < span) return I8KV_EINVAL;
+  // positions are 32-bit on the device
+  if (base_max + static_cast<int64_t>(ns) * chunk > INT32_MAX) return I8KV_EINVAL;
   return I8KV_OK;
 }
 
@@ -190,6 +193,8 @@ i8kv_status dsa_common(const uint16_t* q, const int8_t* k, const int8_t* v, cons
   p.G = Hq / Hkv;
   p.max_sel = max_sel;
   p.sigma = sigma;
+  p.softcap = 0.f;
+  p.window = -1;
   return I8KV_OK;
 }
 
@@ -329,16 +334,22 @@ i8kv_status dsa_prefill(const uint16_t* q, const int8_t* k_cache, const int8_t* 
   return run(make_key(Path::kDsa, D, p.G, false, false), p, static_cast<cudaStream_t>(stream));
 }
 
-i8kv_status paged_decode(const uint16_t* q, const void* k_cache, const void* v_cache,
+}  // extern "C"
+
+namespace {
+
+i8kv_status paged_common(const uint16_t* q, const void* k_cache, const void* v_cache,
                          int32_t cache_dtype, const float* k_scale, const float* v_scale,
                          int32_t scale_kind, const int32_t* block_table,
                          const int32_t* seq_lens, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
                          int32_t block_size, int32_t max_blocks, int64_t num_blocks,
-                         float softmax_scale, const float* head_sink, int32_t num_splits,
-                         int32_t chunk, void* workspace, size_t workspace_bytes, uint16_t* out,
-                         float* lse, int32_t* slots_out, uint32_t* flags, void* stream) {
+                         float softmax_scale, const float* head_sink, float softcap,
+                         int32_t window, int32_t num_splits, int32_t chunk, void* workspace,
+                         size_t workspace_bytes, uint16_t* out, float* lse, int32_t* slots_out,
+                         uint32_t* flags, void* stream) {
   if (B < 0 || max_blocks < 0 || num_blocks < 0 || block_size < 1 || num_splits < 0)
     return I8KV_EINVAL;
+  if (!(softcap >= 0.f) || !std::isfinite(softcap) || window < -1) return I8KV_EINVAL;
   i8kv_status st = check_heads(Hq, Hkv, D);
   if (st != I8KV_OK) return st;
   if (block_size % 16 != 0) return I8KV_EUNSUPPORTED;
@@ -358,12 +369,13 @@ i8kv_status paged_decode(const uint16_t* q, const void* k_cache, const void* v_c
   if (cap > INT32_MAX) return I8KV_EUNSUPPORTED;
   const int32_t G = Hq / Hkv;
   const KernelKey key = make_key(Path::kPaged, D, G, fp16c, true);
+  const int64_t span = I8KV_WINDOW_SPAN(cap, window);
   if (num_splits == 0) {
-    st = plan(key, cap, std::max(1, B * Hkv), I8KV_GEOM_WAVE, 0, &num_splits, &chunk, nullptr);
+    st = plan(key, span, std::max(1, B * Hkv), I8KV_GEOM_WAVE, 0, &num_splits, &chunk, nullptr);
     if (st != I8KV_OK) return st;
-  } else if ((st = check_geometry(cap, num_splits, chunk)) != I8KV_OK) {
-    return st;
   }
+  if ((st = check_geometry(span, num_splits, chunk, window >= 0 ? cap : 0)) != I8KV_OK)
+    return st;
   DecodeParams p{};
   if ((st = set_workspace(p, workspace, workspace_bytes, B * Hkv, num_splits, G, D)) != I8KV_OK)
     return st;
@@ -395,7 +407,42 @@ i8kv_status paged_decode(const uint16_t* q, const void* k_cache, const void* v_c
   p.num_splits = num_splits;
   p.chunk = chunk;
   p.sigma = softmax_scale;
+  p.softcap = softcap;
+  p.window = window;
   return run(key, p, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+i8kv_status paged_decode(const uint16_t* q, const void* k_cache, const void* v_cache,
+                         int32_t cache_dtype, const float* k_scale, const float* v_scale,
+                         int32_t scale_kind, const int32_t* block_table,
+                         const int32_t* seq_lens, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                         int32_t block_size, int32_t max_blocks, int64_t num_blocks,
+                         float softmax_scale, const float* head_sink, int32_t num_splits,
+                         int32_t chunk, void* workspace, size_t workspace_bytes, uint16_t* out,
+                         float* lse, int32_t* slots_out, uint32_t* flags, void* stream) {
+  return paged_common(q, k_cache, v_cache, cache_dtype, k_scale, v_scale, scale_kind, block_table,
+                      seq_lens, B, Hq, Hkv, D, block_size, max_blocks, num_blocks, softmax_scale,
+                      head_sink, 0.f, -1, num_splits, chunk, workspace, workspace_bytes, out, lse,
+                      slots_out, flags, stream);
+}
+
+i8kv_status paged_decode_ex(const uint16_t* q, const void* k_cache, const void* v_cache,
+                            int32_t cache_dtype, const float* k_scale, const float* v_scale,
+                            int32_t scale_kind, const int32_t* block_table,
+                            const int32_t* seq_lens, int32_t B, int32_t Hq, int32_t Hkv,
+                            int32_t D, int32_t block_size, int32_t max_blocks, int64_t num_blocks,
+                            float softmax_scale, const float* head_sink, float softcap,
+                            int32_t window, int32_t num_splits, int32_t chunk, void* workspace,
+                            size_t workspace_bytes, uint16_t* out, float* lse,
+                            int32_t* slots_out, uint32_t* flags, void* stream) {
+  return paged_common(q, k_cache, v_cache, cache_dtype, k_scale, v_scale, scale_kind, block_table,
+                      seq_lens, B, Hq, Hkv, D, block_size, max_blocks, num_blocks, softmax_scale,
+                      head_sink, softcap, window, num_splits, chunk, workspace, workspace_bytes,
+                      out, lse, slots_out, flags, stream);
 }
 
 i8kv_status split_combine(const float* acc, const float* m, const float* l, int32_t units,

@@ -170,13 +170,25 @@ decode_kernel(const DecodeParams p) {
   constexpr int MT_ITERS = (KC + kWarps - 1) / kWarps;
 
   // ---------------- candidate range of this split ----------------
-  // (positions fit 32 bits: the host checks num_splits * chunk <= INT32_MAX)
-  const int lo = split * p.chunk;
-  // nominal end of the split (capacity-bounded); the live end follows below
+  // (positions fit 32 bits: the host checks cap + num_splits * chunk <= INT32_MAX)
   const int cap = PAGED ? p.max_blocks * p.bs : p.max_sel;
-  const int nhi = min(lo + p.chunk, cap);
   int len = 0;
   if constexpr (PAGED) len = p.seq_lens[row];  // in flight while the keys are fetched
+  // Sliding window (paged only): the query at position len - 1 attends
+  // [wlo, len) with wlo = len - 1 - window; the splits then count their chunks
+  // from wlo rounded down to the 16-token tile granule, so this one case waits
+  // for the length before the first gather keys.
+  int wlo = 0, base = 0;
+  if constexpr (PAGED) {
+    if (p.window >= 0) {
+      const int live = min(max(len, 0), cap);
+      wlo = max(0, live - 1 - p.window);
+      base = wlo & ~15;
+    }
+  }
+  const int lo = base + split * p.chunk;
+  // nominal end of the split (capacity-bounded); the live end follows below
+  const int nhi = min(lo + p.chunk, cap);
 
   // ---------------- per-warp gather pipeline ----------------
   // Warp w takes the steps w, w+4, w+8, ... of kStep consecutive positions.
@@ -234,11 +246,12 @@ decode_kernel(const DecodeParams p) {
       len = len < 0 ? 0 : cap;
     }
     hi = min(nhi, len);
-    // debug output: the gathered row of every token of this split's nominal range
+    // debug output: the gathered row of every attended position of the row,
+    // -1 elsewhere; the row's CTAs of KV head 0 interleave over [0, cap)
     if (p.slots_out != nullptr && g == 0) {
-      for (int t = lo + threadIdx.x; t < nhi; t += kThreads) {
+      for (int t = split * kThreads + threadIdx.x; t < cap; t += p.num_splits * kThreads) {
         int v = -1;
-        if (t < len) {
+        if (t >= wlo && t < len) {
           const int blk = p.block_table[(long long)row * p.max_blocks + t / p.bs];
           v = blk * p.bs + t % p.bs;
         }
@@ -261,6 +274,9 @@ decode_kernel(const DecodeParams p) {
       if constexpr (PAGED) {
         const int nvalid = min(hi - pos0, T::kStep);
         mask = nvalid >= 32 ? 0xFFFFFFFFu : ((1u << nvalid) - 1u);
+        // positions before the window start (first step of split 0 only)
+        const int nbelow = wlo - pos0;
+        if (nbelow > 0) mask &= nbelow >= 32 ? 0u : ~((1u << nbelow) - 1u);
         bool bad_blk = false;
 #pragma unroll
         for (int s = 0; s < SUB; ++s) {
@@ -401,6 +417,8 @@ decode_kernel(const DecodeParams p) {
   const int ld_hi = lane >> 4;
   const uint32_t ld_base = ld_row * T::kRowBytes;
   const float sigma = p.sigma;
+  const float softcap = p.softcap;
+  const float cap_k = 2.f * kLog2e / softcap;  // used only when softcap > 0
 
   for (int k = 0; k < my_n; ++k) {
     issue(k + T::kStages - 1, q0);
@@ -481,13 +499,23 @@ decode_kernel(const DecodeParams p) {
     for (int nt = 0; nt < NT; ++nt) {
       float sc[SUB][4];
 #pragma unroll
+      for (int s = 0; s < SUB; ++s)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[s][e] = sacc[s][nt][e] * sigma;
+      if constexpr (PAGED) {
+        if (softcap > 0.f) {
+#pragma unroll
+          for (int s = 0; s < SUB; ++s)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[s][e] = soft_cap(sc[s][e], softcap, cap_k);
+        }
+      }
+#pragma unroll
       for (int s = 0; s < SUB; ++s) {
         const bool v_top = (mask >> (kSub * s + grp)) & 1u;
         const bool v_bot = (mask >> (kSub * s + grp + 8)) & 1u;
-        sc[s][0] = v_top ? sacc[s][nt][0] * sigma : neg_inf();
-        sc[s][1] = v_top ? sacc[s][nt][1] * sigma : neg_inf();
-        sc[s][2] = v_bot ? sacc[s][nt][2] * sigma : neg_inf();
-        sc[s][3] = v_bot ? sacc[s][nt][3] * sigma : neg_inf();
+        if (!v_top) sc[s][0] = sc[s][1] = neg_inf();
+        if (!v_bot) sc[s][2] = sc[s][3] = neg_inf();
       }
       float pr[SUB][4];
 #pragma unroll

@@ -21,6 +21,22 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// 1/x with the SFU instruction (relative error about 2^-23; 1/inf = +0).
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Softcap c * tanh(x / c) through the identity tanh(y) = 1 - 2 / (1 + e^(2y)),
+// with k = 2 log2(e) / c: e^(2y) = 2^(k x).  Saturates to +-c (2^(k x) = inf or
+// 0); the absolute error is a few ulp of c, and the map has slope <= 1, so it
+// never enlarges an error already in x.
+__device__ __forceinline__ float soft_cap(float x, float c, float k) {
+  const float e = fast_exp2(x * k);
+  return fmaf(-2.f * c, fast_rcp(1.f + e), c);
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -34,6 +34,8 @@ struct DecodeParams {
   int32_t num_splits, chunk;
   int32_t per_channel;       // 1: scales [Hkv, D]; 0: one scale
   float sigma;
+  float softcap;             // paged: > 0 caps scores to softcap * tanh(s / softcap); 0 off
+  int32_t window;            // paged: >= 0 attends [len - 1 - window, len); -1 off
 };
 
 struct KernelKey {

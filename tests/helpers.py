@@ -57,24 +57,38 @@ def run_dsa(c, d=None, num_splits=0, chunk=0, prefill=False, flags=None):
     return out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
 
-def run_paged(c, d=None, num_splits=0, chunk=0, slots=False, flags=None):
+def run_paged(c, d=None, num_splits=0, chunk=0, slots=False, flags=None, softcap=0.0,
+              window=-1, partials=False):
+    """Paged decode through the binding.  Returns (O, lse[, slots]) as float64
+    arrays, or with ``partials`` the workspace partials (m, l [units, ns, G],
+    acc [units, ns, G, D]) of a partials-only call."""
     d = d or paged_to_device(c)
     B, Hq, D = c.q.shape
     nb, bs, Hkv, _ = c.k_cache.shape
+    G = Hq // Hkv
     cap = c.block_table.shape[1] * bs
     out = torch.full((B, Hq, D), float("nan"), dtype=torch.float16, device="cuda")
     lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device="cuda")
     ns = num_splits
     if ns == 0:
         dt = K.CACHE_FP16 if c.k_cache.dtype == np.float16 else K.CACHE_INT8
-        ns, chunk, _, _ = K.decode_plan(K.PATH_PAGED, dt, cap, B, Hq, Hkv, D, K.GEOM_WAVE, 0)
-    wsb = K.split_workspace_bytes(B * Hkv, ns, Hq // Hkv, D)
+        ns, chunk, _, _ = K.decode_plan(K.PATH_PAGED, dt, K.window_span(cap, window), B, Hq, Hkv,
+                                        D, K.GEOM_WAVE, 0)
+    wsb = K.split_workspace_bytes(B * Hkv, ns, G, D)
     ws = torch.full((max(wsb // 4, 1),), float("nan"), dtype=torch.float32, device="cuda")
     so = torch.full((B, cap), -99, dtype=torch.int32, device="cuda") if slots else None
     K.paged_decode(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["bt"], d["lens"],
-                   c.sigma, d["sink"], num_splits=ns, chunk=chunk, workspace=ws, out=out, lse=lse,
-                   slots_out=so, flags=flags)
+                   c.sigma, d["sink"], num_splits=ns, chunk=chunk, workspace=ws,
+                   out=None if partials else out, lse=None if partials else lse, slots_out=so,
+                   flags=flags, partials_only=partials, softcap=softcap, window=window)
     torch.cuda.synchronize()
+    if partials:
+        u = B * Hkv
+        w = ws.cpu().numpy().astype(np.float64)
+        acc = w[:u * ns * G * D].reshape(u, ns, G, D)
+        m = w[u * ns * G * D:u * ns * G * (D + 1)].reshape(u, ns, G)
+        l = w[u * ns * G * (D + 1):u * ns * G * (D + 2)].reshape(u, ns, G)
+        return m, l, acc
     res = (out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64))
     if slots:
         res = res + (so.cpu().numpy(),)
@@ -86,9 +100,10 @@ def oracle_dsa(c):
                                    c.idx, c.sigma, c.sink)
 
 
-def oracle_paged(c):
+def oracle_paged(c, softcap=0.0, window=-1):
     return oracle.paged_attention(c.q, c.k_cache, c.v_cache, c.k_scale, c.v_scale, c.scale_kind,
-                                  c.block_table, c.seq_lens, c.sigma, c.sink)
+                                  c.block_table, c.seq_lens, c.sigma, c.sink, softcap=softcap,
+                                  window=window)
 
 
 def assert_close_oracle(got, ref, what=""):

@@ -163,3 +163,24 @@ def test_reshape_and_cache_validation(lib):
     assert call(slots=None) == 1
     assert call(kc=P8) == 3
     assert call(T=0) == 0       # nothing to do, nothing enqueued
+
+
+def test_paged_decode_ex_validation(lib):
+    def call(**kw):
+        a = dict(softcap=0.0, window=-1, ns=1, chunk=512, mb=32)
+        a.update(kw)
+        return lib.paged_decode_ex(P, P, P, 1, P, P, 2, P, P, 0, 32, 8, 128, 16, a["mb"], 100,
+                                   0.1, None, a["softcap"], a["window"], a["ns"], a["chunk"],
+                                   P, 1 << 30, P, None, None, None, None)
+    assert call() == 0
+    assert call(softcap=-1.0) == 1
+    assert call(softcap=float("nan")) == 1
+    assert call(softcap=float("inf")) == 1
+    assert call(window=-2) == 1
+    # with a window the splits need only cover the span min(cap, window + 16)
+    assert call(window=100, ns=1, chunk=112) == 1       # 112 < 116
+    assert call(window=100, ns=1, chunk=128) == 0
+    assert call(window=100, ns=2, chunk=64) == 0
+    assert call(window=0, ns=1, chunk=16) == 0
+    assert call(window=-1, ns=1, chunk=128) == 1        # no window: the cap 512
+    assert call(window=5000, ns=1, chunk=496) == 1      # wide window: the cap
