@@ -17,7 +17,9 @@ __all__ = [
     "sparse_split_partials", "MODE_POW2_TILES", "MODE_WAVE", "split_geometry",
 ]
 from .attention import scores, window_chunk_bounds, window_span, window_start  # noqa: E402
-from .quantize import quantize_rows, reshape_and_cache  # noqa: E402
+from .attention import e4m3fn_value  # noqa: E402
+from .quantize import e4m3fn_encode, quantize_rows, quantize_rows_fp8, reshape_and_cache  # noqa
 
-__all__ += ["quantize_rows", "reshape_and_cache", "scores", "window_chunk_bounds",
+__all__ += ["quantize_rows", "reshape_and_cache", "e4m3fn_value", "e4m3fn_encode",
+            "quantize_rows_fp8", "scores", "window_chunk_bounds",
             "window_span", "window_start"]

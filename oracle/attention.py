@@ -71,13 +71,38 @@ SCALE_PER_CHANNEL = 2
 # 1. dequantisation
 # --------------------------------------------------------------------------
 
+def e4m3fn_value(code: int) -> float:
+    """Value of one float8 e4m3fn bit pattern (OCP 8-bit floating point, E4M3:
+    sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 is
+    subnormal, m * 2^-9; S.1111.111 is NaN; there are no infinities)."""
+    code = int(code) & 0xFF
+    sign = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return math.nan
+    if e == 0:
+        return sign * m * 2.0 ** -9
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+_E4M3FN_TABLE = np.array([e4m3fn_value(c) for c in range(256)], dtype=np.float64)
+
+
 def dequantize(codes: np.ndarray, scale: np.ndarray, scale_kind: int, kv_head: int) -> np.ndarray:
     """Rows ``codes[..., D]`` of one KV head -> float64 values.
 
     per-tensor: scale[0] * code;  per-channel: scale[kv_head, d] * code.
+    An int8 array holds INT8 codes, a uint8 array float8 e4m3fn bit patterns
+    (whose values the scales multiply the same way) [PR 29912, Schema: the
+    cache element type is one of float16, bfloat16, int8, float8e4m3fn].
     A float16 cache is returned as is (no scale).
     """
-    x = np.asarray(codes).astype(np.float64)
+    codes = np.asarray(codes)
+    if codes.dtype == np.uint8:
+        x = _E4M3FN_TABLE[codes]
+    else:
+        x = codes.astype(np.float64)
     if codes.dtype == np.float16:
         return x
     if scale_kind == SCALE_PER_TENSOR:

@@ -64,6 +64,27 @@ def quantize_int8(x: np.ndarray, scale_kind: int):
     return codes, scale
 
 
+def quantize_fp8(x: np.ndarray, scale_kind: int):
+    """Synthesise a float8 e4m3fn cache (uint8 bit patterns) from fp32 values
+    ``x[..., Hkv, D]``: ``scale = amax / 448`` (the largest finite e4m3fn
+    value) per (kv_head, channel) or per tensor, values ``x / scale`` converted
+    by PyTorch's float8_e4m3fn dtype (round to nearest even).  Test data only."""
+    import torch
+    x = np.asarray(x, dtype=np.float32)
+    lead = tuple(range(x.ndim - 2))
+    if scale_kind == SCALE_PER_CHANNEL:
+        amax = np.abs(x).max(axis=lead)
+    elif scale_kind == SCALE_PER_TENSOR:
+        amax = np.abs(x).max().reshape(1)
+    else:
+        raise ValueError(f"unknown scale kind {scale_kind}")
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    y = x / (scale[0] if scale_kind == SCALE_PER_TENSOR else scale)
+    y = np.clip(y, -448.0, 448.0).astype(np.float32)
+    codes = torch.from_numpy(np.ascontiguousarray(y)).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.numpy().copy(), scale
+
+
 @dataclass
 class SparseCase:
     """Inputs of a sparse-candidate (DSA) call: each query row has its own list."""
@@ -167,20 +188,23 @@ def sparse_decode(S: int, seed: int = 0, Hq: int = 24, Hkv: int = 2, D: int = 25
 
 def paged_decode(seed: int = 0, B: int = 16, len_lo: int = 512, len_hi: int = 8192,
                  bs: int = 16, max_blocks: int = 512, Hq: int = 32, Hkv: int = 8, D: int = 128,
-                 scale_kind: int = SCALE_PER_CHANNEL, sink: bool = True) -> PagedCase:
-    """Paged INT8 decode: lengths uniform in [len_lo, len_hi]; the physical pool
-    holds exactly sum(ceil(len/bs)) blocks and the block table is a random
-    permutation of them (unused entries -1); sigma = 1/sqrt(D)."""
+                 scale_kind: int = SCALE_PER_CHANNEL, sink: bool = True,
+                 cache: str = "int8") -> PagedCase:
+    """Paged INT8 (or float8 e4m3fn) decode: lengths uniform in [len_lo,
+    len_hi]; the physical pool holds exactly sum(ceil(len/bs)) blocks and the
+    block table is a random permutation of them (unused entries -1);
+    sigma = 1/sqrt(D)."""
     rng = make_rng(seed)
+    quant = quantize_fp8 if cache == "fp8" else quantize_int8
     lens = rng.integers(len_lo, len_hi + 1, size=B).astype(np.int32)
     nblk = (lens + bs - 1) // bs
     P = int(nblk.sum())
     q = _normal(rng, (B, Hq, D)).astype(np.float16)
     k = _normal(rng, (P, bs, Hkv, D))
-    kc, ks = quantize_int8(k, scale_kind)
+    kc, ks = quant(k, scale_kind)
     del k
     v = _normal(rng, (P, bs, Hkv, D))
-    vc, vs = quantize_int8(v, scale_kind)
+    vc, vs = quant(v, scale_kind)
     del v
     perm = rng.permutation(P).astype(np.int32)
     bt = np.full((B, max_blocks), -1, dtype=np.int32)
@@ -198,8 +222,8 @@ def deep_context(seed: int = 0, cache: str = "int8", B: int = 16, cap: int = 409
                  live: int = 2600, Hq: int = 16, Hkv: int = 2, D: int = 128, bs: int = 16,
                  sink: bool = False) -> PagedCase:
     """Deep-context split sweep: B sequences with their own contiguous cache of
-    ``cap`` tokens (identity block table), live length ``live``; int8 cache with
-    per-channel scales or a float16 cache; sigma = 1/sqrt(D)."""
+    ``cap`` tokens (identity block table), live length ``live``; int8 or float8
+    e4m3fn cache with per-channel scales, or a float16 cache; sigma = 1/sqrt(D)."""
     rng = make_rng(seed)
     mb = cap // bs
     q = _normal(rng, (B, Hq, D)).astype(np.float16)
@@ -208,6 +232,9 @@ def deep_context(seed: int = 0, cache: str = "int8", B: int = 16, cap: int = 409
     if cache == "int8":
         kc, ks = quantize_int8(k, SCALE_PER_CHANNEL)
         vc, vs = quantize_int8(v, SCALE_PER_CHANNEL)
+    elif cache == "fp8":
+        kc, ks = quantize_fp8(k, SCALE_PER_CHANNEL)
+        vc, vs = quantize_fp8(v, SCALE_PER_CHANNEL)
     elif cache == "fp16":
         kc, vc = k.astype(np.float16), v.astype(np.float16)
         ks = vs = np.ones((Hkv, D), np.float32)
@@ -303,6 +330,9 @@ def random_paged(seed: int, B: int, Hq: int, Hkv: int, D: int, bs: int, max_bloc
     if cache == "int8":
         kc, ks = quantize_int8(k, scale_kind)
         vc, vs = quantize_int8(v, scale_kind)
+    elif cache == "fp8":
+        kc, ks = quantize_fp8(k, scale_kind)
+        vc, vs = quantize_fp8(v, scale_kind)
     else:
         kc, vc = k.astype(np.float16), v.astype(np.float16)
         ks = vs = np.ones((Hkv, D), np.float32)
