@@ -60,7 +60,8 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--extra", default="all",
-                    choices=["all", "paged", "variants", "deep", "prefill", "quantize", "none"],
+                    choices=["all", "paged", "variants", "fp8", "deep", "prefill", "quantize",
+                             "none"],
                     help="which other workloads to measure besides the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
@@ -400,46 +401,56 @@ def extra_configs(torch, K, W, np, dev, stream, peaks, args):
                                              softcap=30.0)
         res["paged_decode_window"] = _paged(torch, K, W, np, t, dev, bench_graph, hbm,
                                             window=1023)
-    if args.extra in ("all", "deep"):
-        for cache in ("int8", "fp16"):
+    if args.extra in ("all", "paged", "fp8"):
+        res["paged_decode_fp8"] = _paged(torch, K, W, np, t, dev, bench_graph, hbm, cache="fp8")
+    if args.extra in ("all", "deep", "fp8"):
+        for cache in (("fp8",) if args.extra == "fp8" else ("int8", "fp8", "fp16")):
             res[f"deep_context_{cache}"] = _deep(torch, K, W, np, t, dev, bench_graph, hbm, cache)
     if args.extra in ("all", "prefill"):
         res["sparse_prefill"] = _prefill(torch, K, W, np, t, bench_graph, peaks)
-    if args.extra in ("all", "quantize"):
+    if args.extra in ("all", "quantize", "fp8"):
         res["quantize_on_write"] = _quantize(torch, K, np, t, dev, bench_graph, hbm)
+        res["quantize_on_write_fp8"] = _quantize(torch, K, np, t, dev, bench_graph, hbm, "fp8")
     return res
 
 
-def _quantize(torch, K, np, t, dev, bench_graph, hbm):
+def _quantize(torch, K, np, t, dev, bench_graph, hbm, cache="int8"):
     """Quantize-on-write of one 8192-token prefill chunk (8 KV heads, D 128)
-    into a paged INT8 cache with per-channel scales, R rotating destinations."""
+    into a paged INT8 or float8 e4m3fn cache with per-channel scales; R
+    rotating sets of new rows, slot maps and destinations (inputs and outputs
+    of a graph together exceed the L2 three times over)."""
     rng = np.random.default_rng(0)
     T, Hkv, Dh, bs = 8192, 8, 128, 16
-    kn = t((rng.standard_normal((T, Hkv, Dh))).astype(np.float16))
-    vn = t((rng.standard_normal((T, Hkv, Dh))).astype(np.float16))
     ks = t(np.exp(rng.uniform(-4, -2, size=(Hkv, Dh))).astype(np.float32))
     vs = t(np.exp(rng.uniform(-4, -2, size=(Hkv, Dh))).astype(np.float32))
     R = 8
     nb = T // bs
-    caches = [dict(k=torch.zeros((nb, bs, Hkv, Dh), dtype=torch.int8, device=dev),
-                   v=torch.zeros((nb, bs, Hkv, Dh), dtype=torch.int8, device=dev),
-                   s=t(rng.permutation(nb * bs).astype(np.int32))) for _ in range(R)]
+    cdt = torch.uint8 if cache == "fp8" else torch.int8
+    sets = [dict(kn=t(rng.standard_normal((T, Hkv, Dh)).astype(np.float16)),
+                 vn=t(rng.standard_normal((T, Hkv, Dh)).astype(np.float16)),
+                 k=torch.zeros((nb, bs, Hkv, Dh), dtype=cdt, device=dev),
+                 v=torch.zeros((nb, bs, Hkv, Dh), dtype=cdt, device=dev),
+                 s=t(rng.permutation(nb * bs).astype(np.int32))) for _ in range(R)]
 
     def fn():
-        for c in caches:
-            K.reshape_and_cache(kn, vn, c["s"], c["k"], c["v"], ks, vs, 2)
+        for c in sets:
+            K.reshape_and_cache(c["kn"], c["vn"], c["s"], c["k"], c["v"], ks, vs, 2)
     sec = bench_graph(fn, R, reps=50)
     byts = 2 * T * Hkv * Dh * 2 + 2 * T * Hkv * Dh + T * 4 + 2 * Hkv * Dh * 4
-    return dict(workload="quantize-on-write: 8192 new tokens x 8 KV heads x head_dim 128 (fp16) "
-                         "into a paged INT8 cache at a permuted slot mapping, per-channel scales",
+    name = "float8 e4m3fn" if cache == "fp8" else "INT8"
+    return dict(workload=f"quantize-on-write: 8192 new tokens x 8 KV heads x head_dim 128 (fp16) "
+                         f"into a paged {name} cache at a permuted slot mapping, per-channel "
+                         f"scales",
                 us_per_call=round(sec * 1e6, 2), gbs=round(byts / sec / 1e9, 1),
-                frac_of_hbm=round(byts / sec / 1e9 / hbm, 4), bytes_per_call=byts)
+                frac_of_hbm=round(byts / sec / 1e9 / hbm, 4), bytes_per_call=byts,
+                rotating_sets=R)
 
 
-def _paged(torch, K, W, np, t, dev, bench_graph, hbm, softcap=0.0, window=-1):
+def _paged(torch, K, W, np, t, dev, bench_graph, hbm, softcap=0.0, window=-1, cache="int8"):
     """Paged decode: 16 sequences, lengths U[512, 8192], 32/8 heads, D 128
-    (optionally with a softcap and a sliding window)."""
-    c = W.paged_decode(seed=0)
+    (optionally with a softcap and a sliding window, or a float8 e4m3fn cache)."""
+    c = W.paged_decode(seed=0, cache=cache)
+    dt = K.CACHE_FP8 if cache == "fp8" else K.CACHE_INT8
     B, Hq, Dh = c.q.shape
     nb, bs, Hkv, _ = c.k_cache.shape
     cap = c.block_table.shape[1] * bs
@@ -447,7 +458,7 @@ def _paged(torch, K, W, np, t, dev, bench_graph, hbm, softcap=0.0, window=-1):
     copies = [dict(k=t(c.k_cache), v=t(c.v_cache)) for _ in range(R)]
     q, ks, vs = t(c.q), t(c.k_scale), t(c.v_scale)
     bt, lens, sink = t(c.block_table), t(c.seq_lens), t(c.sink)
-    ns, chunk, wsb, wave = K.decode_plan(K.PATH_PAGED, K.CACHE_INT8, K.window_span(cap, window),
+    ns, chunk, wsb, wave = K.decode_plan(K.PATH_PAGED, dt, K.window_span(cap, window),
                                          B, Hq, Hkv, Dh, K.GEOM_WAVE)
     ws = torch.empty(max(wsb // 4, 4), dtype=torch.float32, device=dev)
     out = torch.empty_like(q)
@@ -469,9 +480,9 @@ def _paged(torch, K, W, np, t, dev, bench_graph, hbm, softcap=0.0, window=-1):
     if window >= 0:
         opts += f", sliding window {window} (attended sum {tokens})"
     return dict(
-        workload="paged INT8 decode: 16 sequences, lengths U[512,8192] (sum %d), block 16, "
+        workload="paged %s decode: 16 sequences, lengths U[512,8192] (sum %d), block 16, "
                  "permuted block table, 32/8 heads, head_dim 128, per-channel scales, sink%s"
-                 % (int(c.seq_lens.sum()), opts),
+                 % ("float8 e4m3fn" if cache == "fp8" else "INT8", int(c.seq_lens.sum()), opts),
         us_per_call=round(sec * 1e6, 2), gbs=round(byts / sec / 1e9, 1),
         frac_of_hbm=round(byts / sec / 1e9 / hbm, 4), bytes_per_call=byts, num_splits=ns,
         chunk=chunk, wave_ctas=wave, rotating_copies=R)
@@ -482,12 +493,12 @@ def _deep(torch, K, W, np, t, dev, bench_graph, hbm, cache):
     c = W.deep_context(seed=0, cache=cache)
     B, Hq, Dh = c.q.shape
     nb, bs, Hkv, _ = c.k_cache.shape
-    esz = 1 if cache == "int8" else 2
-    R = 20 if cache == "int8" else 10
+    esz = 2 if cache == "fp16" else 1
+    R = 10 if cache == "fp16" else 20
     copies = [dict(k=t(c.k_cache), v=t(c.v_cache)) for _ in range(R)]
     q, ks, vs, bt, lens = t(c.q), t(c.k_scale), t(c.v_scale), t(c.block_table), t(c.seq_lens)
     byts = B * 2600 * Hkv * Dh * 2 * esz + B * Hq * Dh * 4 + B * (2600 // 16 + 1) * 4
-    dt = K.CACHE_INT8 if cache == "int8" else K.CACHE_FP16
+    dt = {"int8": K.CACHE_INT8, "fp8": K.CACHE_FP8, "fp16": K.CACHE_FP16}[cache]
     row = {}
     for label, ovr in (("adaptive", 0), ("chunk128", 128), ("chunk256", 256), ("chunk512", 512)):
         ns, chunk, wsb, wave = K.decode_plan(K.PATH_PAGED, dt, 4096, B, Hq, Hkv, Dh,

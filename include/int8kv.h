@@ -67,6 +67,9 @@ typedef enum {
 
 #define I8KV_CACHE_INT8 1 /* codes in [-128, 127], dequantised with the scales */
 #define I8KV_CACHE_FP16 2 /* paged_decode only: values taken as is, scales ignored */
+#define I8KV_CACHE_FP8 3  /* paged_decode / reshape_and_cache only: float8 e4m3fn codes,
+                             dequantised with the scales (onnxruntime PR 29912, Schema:
+                             cache element type float8e4m3fn) */
 
 #define I8KV_GEOM_WAVE 0       /* onnx-genai PR 1350 rule (num_splits from one wave)        */
 #define I8KV_GEOM_POW2_TILES 1 /* onnxruntime PR 33707 rule (power-of-two tiles per split)  */
@@ -207,8 +210,9 @@ i8kv_status dsa_prefill(const uint16_t* q, const int8_t* k_cache, const int8_t* 
  * (onnxruntime PR 29912, CUDA kernels: "split-KV, block-table-aware decode
  * with native head-sink ... and on-the-fly cache dequantization").
  *   q            [B, Hq, D] fp16              one query row per sequence
- *   k_cache, v_cache [num_blocks, block_size, Hkv, D] int8 or fp16
- *   cache_dtype  I8KV_CACHE_INT8 or I8KV_CACHE_FP16 (scales ignored, may be NULL)
+ *   k_cache, v_cache [num_blocks, block_size, Hkv, D] int8, float8 e4m3fn or fp16
+ *   cache_dtype  I8KV_CACHE_INT8, I8KV_CACHE_FP8 (both dequantised with the
+ *                scales) or I8KV_CACHE_FP16 (scales ignored, may be NULL)
  *   block_table  [B, max_blocks] int32        token t of sequence b is row
  *                block_table[b, t / block_size] * block_size + t % block_size
  *   seq_lens     [B] int32, DEVICE memory     live lengths, clamped to
@@ -281,27 +285,32 @@ i8kv_status split_combine(const float* acc, const float* m, const float* l, int3
 
 /*
  * reshape_and_cache -- quantize-on-write of new key / value rows into a paged
- * INT8 cache (onnxruntime PR 29912, CUDA kernels: "ReshapeAndCache quantizes on
- * write").  For every new token n and KV head g, the cache row
- * (slot_mapping[n], g) receives
- *     code[d] = clamp(round_half_even(x[d] / scale), -127, 127)
- * with scale = k_scale / v_scale per tensor ([1]) or per channel ([Hkv, D]); the
- * quotient is an IEEE fp32 division of the fp16 value widened to fp32; a NaN
- * quotient stores 0.
+ * INT8 or float8 e4m3fn cache (onnxruntime PR 29912, CUDA kernels:
+ * "ReshapeAndCache quantizes on write"; Schema: cache element type int8 or
+ * float8e4m3fn).  For every new token n and KV head g, the cache row
+ * (slot_mapping[n], g) receives, with q = x[d] / scale:
+ *     I8KV_CACHE_INT8: code[d] = clamp(round_half_even(q), -127, 127)
+ *     I8KV_CACHE_FP8:  code[d] = the e4m3fn value nearest q (ties to even),
+ *                      saturated to +-448
+ * with scale = k_scale / v_scale per tensor ([1]) or per channel ([Hkv, D]); q
+ * is the IEEE fp32 quotient of the fp16 value widened to fp32 (exactly: the
+ * kernel's faster product by the reciprocal falls back to the division
+ * wherever the two could round differently); a NaN quotient stores 0.
  *   k_new, v_new   [num_tokens, Hkv, D] fp16, device
  *   slot_mapping   [num_tokens] int32, device: row of the flattened cache
  *                  (block * block_size + offset); < 0: skipped (padding);
  *                  >= num_slots: skipped and I8KV_FLAG_BAD_SLOT raised
- *   k_cache, v_cache [num_slots, Hkv, D] int8 (a paged cache [num_blocks,
+ *   k_cache, v_cache [num_slots, Hkv, D] bytes (a paged cache [num_blocks,
  *                  block_size, Hkv, D] with num_slots = num_blocks * block_size)
+ *   cache_dtype    I8KV_CACHE_INT8 or I8KV_CACHE_FP8 (others: I8KV_EINVAL)
  *   D a multiple of 8; caches, rows and per-channel scales 16-byte aligned.
  * Scales must be finite and positive (not checked on the device).
  */
 i8kv_status reshape_and_cache(const uint16_t* k_new, const uint16_t* v_new,
                               const int32_t* slot_mapping, int32_t num_tokens, int32_t Hkv,
-                              int32_t D, int8_t* k_cache, int8_t* v_cache, int64_t num_slots,
+                              int32_t D, void* k_cache, void* v_cache, int64_t num_slots,
                               const float* k_scale, const float* v_scale, int32_t scale_kind,
-                              uint32_t* flags, void* stream);
+                              int32_t cache_dtype, uint32_t* flags, void* stream);
 
 /*
  * dsa_decode_static_workspace -- dsa_decode without a caller-supplied
@@ -344,6 +353,15 @@ i8kv_status dsa_decode_static_workspace(const uint16_t* q, const int8_t* k_cache
  * of 4, both 16-byte aligned.  For tests of the conversion.
  */
 i8kv_status int8_to_fp16(const int8_t* in, uint16_t* out, int64_t n, void* stream);
+
+/*
+ * fp8_to_fp16 -- the paged decode kernel's float8 e4m3fn -> fp16 conversion
+ * (cvt.rn.f16x2.e4m3x2, exact) over a device buffer of n codes, n a multiple of
+ * 4, both buffers 16-byte aligned; out[i] is the value of in[i] (NaN for the
+ * two NaN patterns).  Exposed so that the conversion can be checked
+ * exhaustively.
+ */
+i8kv_status fp8_to_fp16(const uint8_t* in, uint16_t* out, int64_t n, void* stream);
 
 #ifdef __cplusplus
 }

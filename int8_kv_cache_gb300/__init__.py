@@ -20,7 +20,7 @@ __all__ = [
     "Int8KVError", "load", "library_path", "split_geometry", "split_workspace_bytes",
     "decode_plan", "dsa_decode", "dsa_prefill", "paged_decode", "split_combine", "int8_to_fp16",
     "dsa_decode_static_workspace", "STATIC_WORKSPACE_BYTES", "reshape_and_cache",
-    "FLAG_BAD_SLOT", "paged_decode_ex", "window_span",
+    "FLAG_BAD_SLOT", "paged_decode_ex", "window_span", "CACHE_FP8", "fp8_to_fp16",
     "SCALE_PER_TENSOR", "SCALE_PER_CHANNEL", "CACHE_INT8", "CACHE_FP16", "GEOM_WAVE",
     "GEOM_POW2_TILES", "PATH_DSA", "PATH_PAGED", "MAX_SPLITS", "FLAG_LEN_CLAMPED",
     "FLAG_QUERY_RANGE", "FLAG_BAD_BLOCK",
@@ -30,6 +30,7 @@ SCALE_PER_TENSOR = 1
 SCALE_PER_CHANNEL = 2
 CACHE_INT8 = 1
 CACHE_FP16 = 2
+CACHE_FP8 = 3
 GEOM_WAVE = 0
 GEOM_POW2_TILES = 1
 PATH_DSA = 1
@@ -76,7 +77,8 @@ _SIGNATURES = {
                                _c_vp, _c_vp, _c_vp, _c_vp]),
     "int8_to_fp16": (_c_i32, [_c_vp, _c_vp, _c_i64, _c_vp]),
     "reshape_and_cache": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_i32, _c_i32, _c_i32, _c_vp, _c_vp,
-                                   _c_i64, _c_vp, _c_vp, _c_i32, _c_vp, _c_vp]),
+                                   _c_i64, _c_vp, _c_vp, _c_i32, _c_i32, _c_vp, _c_vp]),
+    "fp8_to_fp16": (_c_i32, [_c_vp, _c_vp, _c_i64, _c_vp]),
     "dsa_decode_static_workspace": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i32, _c_vp,
                                              _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_i32,
                                              _c_f32, _c_vp, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp,
@@ -238,12 +240,7 @@ def paged_decode(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, block_t
     B, Hq, D = q.shape
     nb, bs, Hkv, _ = k_cache.shape
     max_blocks = block_table.shape[1]
-    if k_cache.dtype == torch.int8:
-        cache_dtype = CACHE_INT8
-    elif k_cache.dtype == torch.float16:
-        cache_dtype = CACHE_FP16
-    else:
-        raise TypeError(f"k_cache: int8 or float16 expected, got {k_cache.dtype}")
+    cache_dtype = _cache_dtype(k_cache)
     if out is None and not partials_only:
         out = torch.empty_like(q)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -283,18 +280,42 @@ def split_combine(acc, m, l, Hq: int, Hkv: int, head_sink=None, out=None, lse=No
     return out
 
 
+def _cache_dtype(t, allow_fp16=True):
+    """The C cache-dtype code of a cache tensor: int8 -> INT8, float8_e4m3fn or
+    uint8 (e4m3fn bit patterns) -> FP8, float16 -> FP16."""
+    if t.dtype == torch.int8:
+        return CACHE_INT8
+    if t.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", None)):
+        return CACHE_FP8
+    if allow_fp16 and t.dtype == torch.float16:
+        return CACHE_FP16
+    raise TypeError(f"unsupported cache dtype {t.dtype}")
+
+
 def reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale,
                       scale_kind: int, flags=None, stream=None):
-    """Quantize new rows k_new / v_new [T, Hkv, D] (fp16) into the INT8 caches
-    ([num_slots, Hkv, D] or [num_blocks, block_size, Hkv, D]) at slot_mapping [T]."""
+    """Quantize new rows k_new / v_new [T, Hkv, D] (fp16) into the INT8 or
+    float8 e4m3fn caches (int8, or uint8 / float8_e4m3fn tensors, [num_slots,
+    Hkv, D] or [num_blocks, block_size, Hkv, D]) at slot_mapping [T]."""
     T, Hkv, D = k_new.shape
     num_slots = k_cache.numel() // (Hkv * D)
+    cd = _cache_dtype(k_cache, allow_fp16=False)
     _check("reshape_and_cache", load().reshape_and_cache(
         _t(k_new, torch.float16, "k_new"), _t(v_new, torch.float16, "v_new"),
         _t(slot_mapping, torch.int32, "slot_mapping"), T, Hkv, D,
-        _t(k_cache, torch.int8, "k_cache"), _t(v_cache, torch.int8, "v_cache"), num_slots,
+        _t(k_cache, k_cache.dtype, "k_cache"), _t(v_cache, k_cache.dtype, "v_cache"), num_slots,
         _t(k_scale, torch.float32, "k_scale"), _t(v_scale, torch.float32, "v_scale"), scale_kind,
-        _t(flags, torch.int32, "flags"), _stream(stream)))
+        cd, _t(flags, torch.int32, "flags"), _stream(stream)))
+
+
+def fp8_to_fp16(x, out=None, stream=None):
+    """The paged decode kernel's float8 e4m3fn -> fp16 conversion over a uint8
+    buffer of e4m3fn bit patterns (n % 4 == 0)."""
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float16, device=x.device)
+    _check("fp8_to_fp16", load().fp8_to_fp16(_t(x, x.dtype, "x"), _t(out, torch.float16, "out"),
+                                             x.numel(), _stream(stream)))
+    return out
 
 
 def int8_to_fp16(x, out=None, stream=None):

@@ -55,12 +55,13 @@ i8kv_status check_scales(const float* ks, const float* vs, int32_t kind) {
   return I8KV_OK;
 }
 
-KernelKey make_key(Path path, int32_t D, int32_t G, bool fp16_cache, bool p_lo) {
+KernelKey make_key(Path path, int32_t D, int32_t G, int32_t cache_dtype, bool p_lo) {
   KernelKey k;
   k.path = path;
   k.D = D;
   k.nt = G <= 8 ? 1 : 2;
-  k.fp16_cache = fp16_cache;
+  k.fp16_cache = cache_dtype == I8KV_CACHE_FP16;
+  k.fp8_cache = cache_dtype == I8KV_CACHE_FP8;
   k.p_lo = p_lo;
   return k;
 }
@@ -69,19 +70,22 @@ cudaError_t launch_key(const KernelKey& key, const DecodeParams& p, cudaStream_t
   if (key.path == Path::kDsa) {
     return key.p_lo ? i8kv::launch_dsa_decode(key, p, s, occ) : i8kv::launch_dsa_prefill(key, p, s, occ);
   }
-  return key.fp16_cache ? i8kv::launch_paged_fp16(key, p, s, occ) : i8kv::launch_paged_int8(key, p, s, occ);
+  if (key.fp16_cache) return i8kv::launch_paged_fp16(key, p, s, occ);
+  if (key.fp8_cache) return i8kv::launch_paged_fp8(key, p, s, occ);
+  return i8kv::launch_paged_int8(key, p, s, occ);
 }
 
 // One occupancy wave (SM count x resident CTAs per SM) of a kernel on the
 // current device, cached per (device, kernel).
 i8kv_status wave_of(const KernelKey& key, int32_t* wave) {
   static std::mutex mu;
-  static std::map<std::tuple<int, int, int, int, int, int>, int32_t> cache;
+  static std::map<std::tuple<int, int, int, int, int, int, int>, int32_t> cache;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   const auto k = std::make_tuple(dev, static_cast<int>(key.path), key.D, key.nt,
-                                 static_cast<int>(key.fp16_cache), static_cast<int>(key.p_lo));
+                                 static_cast<int>(key.fp16_cache), static_cast<int>(key.fp8_cache),
+                                 static_cast<int>(key.p_lo));
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(k);
@@ -273,14 +277,16 @@ i8kv_status decode_plan(int32_t path, int32_t cache_dtype, int64_t cap, int32_t 
                         int32_t* wave_ctas) {
   if (num_splits == nullptr || chunk == nullptr || workspace_bytes == nullptr) return I8KV_EINVAL;
   if (path != I8KV_PATH_DSA && path != I8KV_PATH_PAGED) return I8KV_EINVAL;
-  if (cache_dtype != I8KV_CACHE_INT8 && cache_dtype != I8KV_CACHE_FP16) return I8KV_EINVAL;
+  if (cache_dtype != I8KV_CACHE_INT8 && cache_dtype != I8KV_CACHE_FP16 &&
+      cache_dtype != I8KV_CACHE_FP8)
+    return I8KV_EINVAL;
   if (path == I8KV_PATH_DSA && cache_dtype != I8KV_CACHE_INT8) return I8KV_EUNSUPPORTED;
   if (rows < 0 || cap < 0) return I8KV_EINVAL;
   i8kv_status st = check_heads(Hq, Hkv, D);
   if (st != I8KV_OK) return st;
   const int32_t G = Hq / Hkv;
   const KernelKey key = make_key(path == I8KV_PATH_DSA ? Path::kDsa : Path::kPaged, D, G,
-                                 cache_dtype == I8KV_CACHE_FP16, true);
+                                 cache_dtype, true);
   const int32_t units = std::max(1, rows * Hkv);
   if ((st = plan(key, cap, units, mode, override_value, num_splits, chunk, wave_ctas)) != I8KV_OK)
     return st;
@@ -300,7 +306,7 @@ i8kv_status dsa_decode(const uint16_t* q, const int8_t* k_cache, const int8_t* v
                               D, N, max_sel, softmax_scale, head_sink, out, lse, flags, p);
   if (st != I8KV_OK) return st;
   if (num_splits < 0) return I8KV_EINVAL;
-  const KernelKey key = make_key(Path::kDsa, D, p.G, false, true);
+  const KernelKey key = make_key(Path::kDsa, D, p.G, I8KV_CACHE_INT8, true);
   if (num_splits == 0) {
     st = plan(key, max_sel, std::max(1, S * Hkv), I8KV_GEOM_POW2_TILES, 0, &num_splits, &chunk,
               nullptr);
@@ -331,7 +337,8 @@ i8kv_status dsa_prefill(const uint16_t* q, const int8_t* k_cache, const int8_t* 
   if (S == 0) return I8KV_OK;
   p.num_splits = 1;
   p.chunk = static_cast<int32_t>(std::max<int64_t>(16, cdiv(max_sel, 16) * 16));
-  return run(make_key(Path::kDsa, D, p.G, false, false), p, static_cast<cudaStream_t>(stream));
+  return run(make_key(Path::kDsa, D, p.G, I8KV_CACHE_INT8, false), p,
+             static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"
@@ -354,7 +361,9 @@ i8kv_status paged_common(const uint16_t* q, const void* k_cache, const void* v_c
   if (st != I8KV_OK) return st;
   if (block_size % 16 != 0) return I8KV_EUNSUPPORTED;
   if ((st = check_sigma(softmax_scale)) != I8KV_OK) return st;
-  if (cache_dtype != I8KV_CACHE_INT8 && cache_dtype != I8KV_CACHE_FP16) return I8KV_EINVAL;
+  if (cache_dtype != I8KV_CACHE_INT8 && cache_dtype != I8KV_CACHE_FP16 &&
+      cache_dtype != I8KV_CACHE_FP8)
+    return I8KV_EINVAL;
   const bool fp16c = cache_dtype == I8KV_CACHE_FP16;
   if (!fp16c && (st = check_scales(k_scale, v_scale, scale_kind)) != I8KV_OK) return st;
   if (B > 0 && (q == nullptr || k_cache == nullptr || v_cache == nullptr ||
@@ -368,7 +377,7 @@ i8kv_status paged_common(const uint16_t* q, const void* k_cache, const void* v_c
   const int64_t cap = static_cast<int64_t>(max_blocks) * block_size;
   if (cap > INT32_MAX) return I8KV_EUNSUPPORTED;
   const int32_t G = Hq / Hkv;
-  const KernelKey key = make_key(Path::kPaged, D, G, fp16c, true);
+  const KernelKey key = make_key(Path::kPaged, D, G, cache_dtype, true);
   const int64_t span = I8KV_WINDOW_SPAN(cap, window);
   if (num_splits == 0) {
     st = plan(key, span, std::max(1, B * Hkv), I8KV_GEOM_WAVE, 0, &num_splits, &chunk, nullptr);
@@ -464,10 +473,11 @@ i8kv_status split_combine(const float* acc, const float* m, const float* l, int3
 
 i8kv_status reshape_and_cache(const uint16_t* k_new, const uint16_t* v_new,
                               const int32_t* slot_mapping, int32_t num_tokens, int32_t Hkv,
-                              int32_t D, int8_t* k_cache, int8_t* v_cache, int64_t num_slots,
+                              int32_t D, void* k_cache, void* v_cache, int64_t num_slots,
                               const float* k_scale, const float* v_scale, int32_t scale_kind,
-                              uint32_t* flags, void* stream) {
+                              int32_t cache_dtype, uint32_t* flags, void* stream) {
   if (num_tokens < 0 || Hkv < 1 || D < 8 || num_slots < 0) return I8KV_EINVAL;
+  if (cache_dtype != I8KV_CACHE_INT8 && cache_dtype != I8KV_CACHE_FP8) return I8KV_EINVAL;
   if (D % 8 != 0) return I8KV_EUNSUPPORTED;
   i8kv_status st = check_scales(k_scale, v_scale, scale_kind);
   if (st != I8KV_OK) return st;
@@ -480,7 +490,16 @@ i8kv_status reshape_and_cache(const uint16_t* k_new, const uint16_t* v_new,
   if (num_tokens == 0) return I8KV_OK;
   cudaError_t e = i8kv::launch_reshape_and_cache(
       k_new, v_new, slot_mapping, num_tokens, Hkv, D, k_cache, v_cache, num_slots, k_scale, v_scale,
-      scale_kind == I8KV_SCALE_PER_CHANNEL, flags, static_cast<cudaStream_t>(stream));
+      scale_kind == I8KV_SCALE_PER_CHANNEL, cache_dtype == I8KV_CACHE_FP8, flags,
+      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? I8KV_OK : cuda_fail(e);
+}
+
+i8kv_status fp8_to_fp16(const uint8_t* in, uint16_t* out, int64_t n, void* stream) {
+  if (n < 0 || n % 4 != 0) return I8KV_EINVAL;
+  if (n > 0 && (in == nullptr || out == nullptr)) return I8KV_EINVAL;
+  if (!aligned(in, 16) || !aligned(out, 16)) return I8KV_EALIGN;
+  cudaError_t e = i8kv::launch_fp8_to_fp16(in, out, n, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? I8KV_OK : cuda_fail(e);
 }
 

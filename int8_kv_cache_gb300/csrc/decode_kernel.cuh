@@ -110,7 +110,7 @@ __device__ __forceinline__ int swz(int r) {
   }
 }
 
-template <int D, int NT, bool PAGED, bool FP16C, bool PLO>
+template <int D, int NT, bool PAGED, bool FP16C, bool PLO, bool FP8>
 __global__ void __launch_bounds__((Tile<D, NT, FP16C, PAGED>::kThreads),
                                   (Tile<D, NT, FP16C, PAGED>::kMinBlocks))
 decode_kernel(const DecodeParams p) {
@@ -461,18 +461,34 @@ decode_kernel(const DecodeParams p) {
               mma16816(sacc[s][nt], r0, r1, r2, r3, qf[nt][c2][0], qf[nt][c2][1]);
           }
         } else {
-          const uint32_t x0 = flip_i8x4(r0), x1 = flip_i8x4(r1);
-          const uint32_t x2 = flip_i8x4(r2), x3 = flip_i8x4(r3);
+          // K codes -> fp16 pairs (channel 4t, 4t+1) and (4t+2, 4t+3) of each
+          // 4-byte word: the permuted contraction order of the Q' fragments
+          uint32_t k0[4], k1[4];
+          if constexpr (FP8) {
+            e4m3x4_to_h2x2(r0, k0[0], k0[2]);
+            e4m3x4_to_h2x2(r1, k0[1], k0[3]);
+            e4m3x4_to_h2x2(r2, k1[0], k1[2]);
+            e4m3x4_to_h2x2(r3, k1[1], k1[3]);
+          } else {
+            const uint32_t x0 = flip_i8x4(r0), x1 = flip_i8x4(r1);
+            const uint32_t x2 = flip_i8x4(r2), x3 = flip_i8x4(r3);
+            k0[0] = i8x2_to_h2(x0, 0x4140u);
+            k0[1] = i8x2_to_h2(x1, 0x4140u);
+            k0[2] = i8x2_to_h2(x0, 0x4342u);
+            k0[3] = i8x2_to_h2(x1, 0x4342u);
+            k1[0] = i8x2_to_h2(x2, 0x4140u);
+            k1[1] = i8x2_to_h2(x3, 0x4140u);
+            k1[2] = i8x2_to_h2(x2, 0x4342u);
+            k1[3] = i8x2_to_h2(x3, 0x4342u);
+          }
           {
-            const uint32_t a0 = i8x2_to_h2(x0, 0x4140u), a1 = i8x2_to_h2(x1, 0x4140u);
-            const uint32_t a2 = i8x2_to_h2(x0, 0x4342u), a3 = i8x2_to_h2(x1, 0x4342u);
+            const uint32_t a0 = k0[0], a1 = k0[1], a2 = k0[2], a3 = k0[3];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma16816(sacc[s][nt], a0, a1, a2, a3, qf[nt][2 * c2][0], qf[nt][2 * c2][1]);
           }
           {
-            const uint32_t a0 = i8x2_to_h2(x2, 0x4140u), a1 = i8x2_to_h2(x3, 0x4140u);
-            const uint32_t a2 = i8x2_to_h2(x2, 0x4342u), a3 = i8x2_to_h2(x3, 0x4342u);
+            const uint32_t a0 = k1[0], a1 = k1[1], a2 = k1[2], a3 = k1[3];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               if (SUB == 1)
@@ -586,11 +602,28 @@ decode_kernel(const DecodeParams p) {
             if constexpr (PLO) mma16816(acc[c2][nt], r0, r2, r1, r3, pl[s][nt][0], pl[s][nt][1]);
           }
         } else {
-          const uint32_t x0 = flip_i8x4(r0), x1 = flip_i8x4(r1);
-          const uint32_t x2 = flip_i8x4(r2), x3 = flip_i8x4(r3);
+          // V^T codes (from the transposing load) -> fp16 pairs of bytes
+          // (0, 2) and (1, 3) of each word
+          uint32_t v0[4], v1[4];
+          if constexpr (FP8) {
+            e4m3x4_to_h2x2(prmt(r0, 0u, 0x3120u), v0[0], v0[1]);
+            e4m3x4_to_h2x2(prmt(r1, 0u, 0x3120u), v0[2], v0[3]);
+            e4m3x4_to_h2x2(prmt(r2, 0u, 0x3120u), v1[0], v1[1]);
+            e4m3x4_to_h2x2(prmt(r3, 0u, 0x3120u), v1[2], v1[3]);
+          } else {
+            const uint32_t x0 = flip_i8x4(r0), x1 = flip_i8x4(r1);
+            const uint32_t x2 = flip_i8x4(r2), x3 = flip_i8x4(r3);
+            v0[0] = i8x2_to_h2(x0, 0x4240u);
+            v0[1] = i8x2_to_h2(x0, 0x4341u);
+            v0[2] = i8x2_to_h2(x1, 0x4240u);
+            v0[3] = i8x2_to_h2(x1, 0x4341u);
+            v1[0] = i8x2_to_h2(x2, 0x4240u);
+            v1[1] = i8x2_to_h2(x2, 0x4341u);
+            v1[2] = i8x2_to_h2(x3, 0x4240u);
+            v1[3] = i8x2_to_h2(x3, 0x4341u);
+          }
           {
-            const uint32_t a0 = i8x2_to_h2(x0, 0x4240u), a1 = i8x2_to_h2(x0, 0x4341u);
-            const uint32_t a2 = i8x2_to_h2(x1, 0x4240u), a3 = i8x2_to_h2(x1, 0x4341u);
+            const uint32_t a0 = v0[0], a1 = v0[1], a2 = v0[2], a3 = v0[3];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               mma16816(acc[2 * c2][nt], a0, a1, a2, a3, ph[s][nt][0], ph[s][nt][1]);
@@ -599,8 +632,7 @@ decode_kernel(const DecodeParams p) {
             }
           }
           {
-            const uint32_t a0 = i8x2_to_h2(x2, 0x4240u), a1 = i8x2_to_h2(x2, 0x4341u);
-            const uint32_t a2 = i8x2_to_h2(x3, 0x4240u), a3 = i8x2_to_h2(x3, 0x4341u);
+            const uint32_t a0 = v1[0], a1 = v1[1], a2 = v1[2], a3 = v1[3];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               mma16816(acc[2 * c2 + 1][nt], a0, a1, a2, a3, ph[s][nt][0], ph[s][nt][1]);
@@ -767,10 +799,10 @@ decode_kernel(const DecodeParams p) {
 // host-side launch of one instantiation
 // ---------------------------------------------------------------------------
 
-template <int D, int NT, bool PAGED, bool FP16C, bool PLO>
+template <int D, int NT, bool PAGED, bool FP16C, bool PLO, bool FP8>
 cudaError_t run_decode(const DecodeParams& p, cudaStream_t s, int* occupancy) {
   using T = Tile<D, NT, FP16C, PAGED>;
-  auto kern = decode_kernel<D, NT, PAGED, FP16C, PLO>;
+  auto kern = decode_kernel<D, NT, PAGED, FP16C, PLO, FP8>;
   // the opt-in shared-memory size is a per-function attribute: set it once per device
   static std::atomic<unsigned long long> done{0};
   int dev = 0;
@@ -803,16 +835,16 @@ cudaError_t run_decode(const DecodeParams& p, cudaStream_t s, int* occupancy) {
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <bool PAGED, bool FP16C, bool PLO>
+template <bool PAGED, bool FP16C, bool PLO, bool FP8 = false>
 cudaError_t dispatch_decode(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
                             int* occupancy) {
   switch (key.D * 10 + key.nt) {
-    case 641: return run_decode<64, 1, PAGED, FP16C, PLO>(p, s, occupancy);
-    case 642: return run_decode<64, 2, PAGED, FP16C, PLO>(p, s, occupancy);
-    case 1281: return run_decode<128, 1, PAGED, FP16C, PLO>(p, s, occupancy);
-    case 1282: return run_decode<128, 2, PAGED, FP16C, PLO>(p, s, occupancy);
-    case 2561: return run_decode<256, 1, PAGED, FP16C, PLO>(p, s, occupancy);
-    case 2562: return run_decode<256, 2, PAGED, FP16C, PLO>(p, s, occupancy);
+    case 641: return run_decode<64, 1, PAGED, FP16C, PLO, FP8>(p, s, occupancy);
+    case 642: return run_decode<64, 2, PAGED, FP16C, PLO, FP8>(p, s, occupancy);
+    case 1281: return run_decode<128, 1, PAGED, FP16C, PLO, FP8>(p, s, occupancy);
+    case 1282: return run_decode<128, 2, PAGED, FP16C, PLO, FP8>(p, s, occupancy);
+    case 2561: return run_decode<256, 1, PAGED, FP16C, PLO, FP8>(p, s, occupancy);
+    case 2562: return run_decode<256, 2, PAGED, FP16C, PLO, FP8>(p, s, occupancy);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -110,6 +110,16 @@ __device__ __forceinline__ uint32_t i8x2_to_h2(uint32_t xflipped, uint32_t sel) 
 }
 __device__ __forceinline__ uint32_t flip_i8x4(uint32_t w) { return w ^ 0x80808080u; }
 
+// Four float8 e4m3fn values (bytes b0..b3 of w) -> half2 (b0, b1) and half2
+// (b2, b3), with the hardware conversion (exact: every e4m3fn value is an fp16
+// value; the two NaN patterns give NaN).
+__device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, l;\n cvt.rn.f16x2.e4m3x2 %1, h;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

@@ -43,6 +43,7 @@ struct KernelKey {
   int D;
   int nt;          // 8-head tiles: 1 (G <= 8) or 2 (G <= 16)
   bool fp16_cache;
+  bool fp8_cache;  // float8 e4m3fn codes (same tile as int8, other conversion)
   bool p_lo;       // probability tile as fp16 high + low parts
 };
 
@@ -61,15 +62,18 @@ cudaError_t launch_paged_int8(const KernelKey& key, const DecodeParams& p, cudaS
                               int* occupancy);
 cudaError_t launch_paged_fp16(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
                               int* occupancy);
+cudaError_t launch_paged_fp8(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
+                             int* occupancy);
 
 cudaError_t launch_combine(const float* acc, const float* m, const float* l, int units,
                            int num_splits, int Hq, int Hkv, int D, const float* sink, void* out,
                            float* lse, cudaStream_t stream);
 cudaError_t launch_int8_to_fp16(const int8_t* in, uint16_t* out, int64_t n, cudaStream_t stream);
 cudaError_t launch_reshape_and_cache(const void* k_new, const void* v_new, const int32_t* slots,
-                                     int num_tokens, int Hkv, int D, int8_t* k_cache,
-                                     int8_t* v_cache, long long num_slots, const float* ks,
-                                     const float* vs, int per_channel, uint32_t* flags,
+                                     int num_tokens, int Hkv, int D, void* k_cache,
+                                     void* v_cache, long long num_slots, const float* ks,
+                                     const float* vs, int per_channel, bool fp8, uint32_t* flags,
                                      cudaStream_t stream);
+cudaError_t launch_fp8_to_fp16(const uint8_t* in, uint16_t* out, int64_t n, cudaStream_t stream);
 
 }  // namespace i8kv

@@ -71,7 +71,8 @@ def run_paged(c, d=None, num_splits=0, chunk=0, slots=False, flags=None, softcap
     lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device="cuda")
     ns = num_splits
     if ns == 0:
-        dt = K.CACHE_FP16 if c.k_cache.dtype == np.float16 else K.CACHE_INT8
+        dt = {np.dtype(np.float16): K.CACHE_FP16, np.dtype(np.uint8): K.CACHE_FP8}.get(
+            c.k_cache.dtype, K.CACHE_INT8)
         ns, chunk, _, _ = K.decode_plan(K.PATH_PAGED, dt, K.window_span(cap, window), B, Hq, Hkv,
                                         D, K.GEOM_WAVE, 0)
     wsb = K.split_workspace_bytes(B * Hkv, ns, G, D)
@@ -118,11 +119,12 @@ def assert_close_oracle(got, ref, what=""):
                              f"got {got[i]!r} ref {ref[i]!r}")
 
 
-def lse_bound(q, k_scale, scale_kind, Hkv, sigma, fp16_cache=False):
+def lse_bound(q, k_scale, scale_kind, Hkv, sigma, fp16_cache=False, code_max=128.0):
     """Per (row, head) bound on |lse_gpu - lse_ref| from folding k_scale into an
-    fp16 query: eps = sigma * 128 * sum_d |Q'_d - fp16(Q'_d)|, Q' = fp32(Q * k_scale)
-    (the error budget of onnxruntime PR 33707 §1), plus 1e-5 for fp32 / exp2
-    rounding.  Shape [rows, Hq]."""
+    fp16 query: eps = sigma * code_max * sum_d |Q'_d - fp16(Q'_d)|, Q' =
+    fp32(Q * k_scale) (the error budget of onnxruntime PR 33707 §1; code_max
+    bounds |code|: 128 for INT8, 448 for float8 e4m3fn), plus 1e-5 for fp32 /
+    exp2 rounding.  Shape [rows, Hq]."""
     R, Hq, D = q.shape
     G = Hq // Hkv
     if fp16_cache:
@@ -134,7 +136,7 @@ def lse_bound(q, k_scale, scale_kind, Hkv, sigma, fp16_cache=False):
         ks = np.repeat(k_scale.astype(np.float32), G, axis=0)  # [Hq, D]
     qp = (qf * ks[None]).astype(np.float32)
     rnd = np.abs(qp.astype(np.float64) - qp.astype(np.float16).astype(np.float64))
-    return sigma * 128.0 * rnd.sum(axis=-1) + 1e-5
+    return sigma * code_max * rnd.sum(axis=-1) + 1e-5
 
 
 def assert_lse_oracle(got, ref, bound, what=""):
@@ -161,3 +163,10 @@ def assert_split_close(a, b, what=""):
     err = np.abs(a - b)
     assert np.all(err <= SPLIT_TOL * np.maximum(1.0, np.abs(b))), \
         f"{what}: split vs unsplit max err {err.max()}"
+
+
+def paged_bound(c):
+    """lse tolerance of a paged case (int8, float8 e4m3fn or fp16 cache)."""
+    return lse_bound(c.q, c.k_scale, c.scale_kind, c.k_cache.shape[2], c.sigma,
+                     fp16_cache=c.k_cache.dtype == np.float16,
+                     code_max=448.0 if c.k_cache.dtype == np.uint8 else 128.0)

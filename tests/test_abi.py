@@ -125,7 +125,7 @@ def test_paged_decode_validation(lib):
                                 a["stream"])
     assert call(bs=8) == 2
     assert call(bs=24) == 2
-    assert call(dt=3) == 1
+    assert call(dt=4) == 1
     assert call(lens=None) == 1
     assert call(ks=None) == 1
     assert call(dt=2, ks=None, vs=None, ns=2, chunk=64) == 4  # fp16 cache needs no scales
@@ -151,11 +151,11 @@ def test_zero_work_is_a_no_op(lib):
 def test_reshape_and_cache_validation(lib):
     def call(**kw):
         a = dict(k=P, v=P, slots=P, T=4, Hkv=2, D=64, kc=P, vc=P, ns=100, ks=P, vs=P, kind=1,
-                 flags=None, stream=None)
+                 cd=1, flags=None, stream=None)
         a.update(kw)
         return lib.reshape_and_cache(a["k"], a["v"], a["slots"], a["T"], a["Hkv"], a["D"], a["kc"],
-                                     a["vc"], a["ns"], a["ks"], a["vs"], a["kind"], a["flags"],
-                                     a["stream"])
+                                     a["vc"], a["ns"], a["ks"], a["vs"], a["kind"], a["cd"],
+                                     a["flags"], a["stream"])
     assert call(D=60) == 2      # not a multiple of 8
     assert call(D=4) == 1
     assert call(T=-1) == 1
@@ -163,6 +163,9 @@ def test_reshape_and_cache_validation(lib):
     assert call(slots=None) == 1
     assert call(kc=P8) == 3
     assert call(T=0) == 0       # nothing to do, nothing enqueued
+    assert call(T=0, cd=3) == 0  # float8 e4m3fn cache
+    assert call(cd=2) == 1      # an fp16 cache is not a quantised cache
+    assert call(cd=0) == 1
 
 
 def test_paged_decode_ex_validation(lib):
