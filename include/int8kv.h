@@ -81,11 +81,13 @@ typedef enum {
 
 /* bits OR-ed into the optional device `flags` word */
 #define I8KV_FLAG_LEN_CLAMPED 0x1u /* a seq_len was > cap (clamped) or < 0 (taken as 0)       */
-#define I8KV_FLAG_QUERY_RANGE 0x2u /* some Q*k_scale is not finite or beyond +-65504: the FP16
-                                      query of that CTA is not exact to the stated bound      */
+#define I8KV_FLAG_QUERY_RANGE 0x2u /* some Q*k_scale is not finite or beyond +-65504 (that CTA
+                                      took the FP32 path)                                     */
 #define I8KV_FLAG_BAD_BLOCK 0x4u   /* a block-table entry inside the live length is outside
                                       [0, num_blocks): those tokens were skipped              */
 #define I8KV_FLAG_BAD_SLOT 0x8u    /* reshape_and_cache: a slot >= num_slots was skipped      */
+#define I8KV_FLAG_FP32_PATH 0x10u  /* some CTA evaluated its heads on the FP32 path (see the
+                                      numerical eligibility rules below)                     */
 
 /* Human-readable name of a status code (static storage). */
 const char* i8kv_status_string(int status);

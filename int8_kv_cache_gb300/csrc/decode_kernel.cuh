@@ -37,6 +37,7 @@
 #pragma once
 
 #include <cuda_fp16.h>
+#include <type_traits>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -110,6 +111,150 @@ __device__ __forceinline__ int swz(int r) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// FP32 path of one CTA (onnxruntime PR 33707, Summary of Changes §1: a CTA
+// that cannot bound the FP16 rounding evaluates its query heads in FP32 on the
+// CUDA cores, starting from the inputs; review follow-up: value_scale folded
+// into the numerator with a 2^80 shift for scores more than 80 nats below the
+// maximum).  Same outputs as the tensor-core body for the CTA's (unit, split):
+// O and lse with one split, else the partial (m, l, acc).  Two passes over the
+// candidates (the maximum first, so nothing is rescaled), one warp per query
+// head, lane l holding channels l, l + 32, ...  Slow by design: it runs only
+// for CTAs that the eligibility checks send to it.
+// ---------------------------------------------------------------------------
+constexpr float kQueryErrorBudget = 0.125f;  // nats of logit shift from rounding Q' to fp16
+constexpr float kTailDepth = 20.f;           // nats below the running maximum
+constexpr float kMaxValueScale = 65536.f;    // |value_scale| above which the tail matters
+
+template <int D, bool PAGED, bool FP16C, bool FP8, int kThreads>
+__device__ __noinline__ void attend_fp32(const DecodeParams p, float* q32, const float* svs) {
+  constexpr int kWarps = kThreads / 32;
+  constexpr int C = D / 32;  // channels per lane
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int G = p.G;
+  // the CTA's unit and split, and its range of positions [lo, hi) (the same
+  // rules as the tensor-core body: the capacity, the clamped live length, the
+  // window start wlo and the chunks counted from it rounded down to 16)
+  const int unit = blockIdx.x, split = blockIdx.y;
+  const int row = unit / p.Hkv, g = unit - row * p.Hkv;
+  const int cap = PAGED ? p.max_blocks * p.bs : p.max_sel;
+  int len = cap, wlo = 0;
+  if constexpr (PAGED) {
+    len = min(max(p.seq_lens[row], 0), cap);
+    if (p.window >= 0) wlo = max(0, len - 1 - p.window);
+  }
+  const int lo = (wlo & ~15) + split * p.chunk;
+  const int hi = min(min(lo + p.chunk, cap), len);
+  // Q * k_scale in fp32, not rounded to fp16
+  const __half* qrow =
+      reinterpret_cast<const __half*>(p.q) + ((long long)row * p.Hq + g * G) * D;
+  for (int e = threadIdx.x; e < G * D; e += kThreads) {
+    const int d = e % D;
+    float x = __half2float(qrow[e]);
+    if constexpr (!FP16C) x *= p.per_channel ? p.k_scale[g * D + d] : p.k_scale[0];
+    q32[e] = x;
+  }
+  __syncthreads();
+  // cache row of position t, or -1 if t is not attended
+  auto row_of = [&](int t) -> long long {
+    if constexpr (PAGED) {
+      if (t < wlo) return -1;
+      const int blk = p.block_table[(long long)row * p.max_blocks + t / p.bs];
+      if (blk < 0 || (long long)blk >= p.cache_rows) return -1;
+      return (long long)blk * p.bs + t % p.bs;
+    } else {
+      const int key = p.idx[(long long)row * p.max_sel + t];
+      return key >= 0 && (long long)key < p.cache_rows ? key : -1;
+    }
+  };
+  auto value = [&](const void* base, long long r, int d) -> float {
+    const long long i = (r * p.Hkv + g) * D + d;
+    if constexpr (FP16C) {
+      return __half2float(reinterpret_cast<const __half*>(base)[i]);
+    } else if constexpr (FP8) {
+      const uint32_t code = reinterpret_cast<const uint8_t*>(base)[i];
+      uint32_t lo2, hi2;
+      e4m3x4_to_h2x2(code, lo2, hi2);
+      return __half2float(__ushort_as_half(static_cast<unsigned short>(lo2 & 0xFFFFu)));
+    } else {
+      return static_cast<float>(reinterpret_cast<const int8_t*>(base)[i]);
+    }
+  };
+  auto score = [&](const float* qh, long long r) -> float {
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < C; ++c) acc = fmaf(qh[lane + 32 * c], value(p.k, r, lane + 32 * c), acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    float sc = acc * p.sigma;
+    if constexpr (PAGED) {
+      if (p.softcap > 0.f) sc = p.softcap * tanhf(sc / p.softcap);
+    }
+    return sc;
+  };
+  const bool direct = p.num_splits == 1;
+  const long long head0 = (long long)row * p.Hq + g * G;
+  for (int h = warp; h < G; h += kWarps) {
+    const float* qh = q32 + h * D;
+    float m = neg_inf();
+    for (int t = lo; t < hi; ++t) {
+      const long long r = row_of(t);
+      if (r >= 0) m = fmaxf(m, score(qh, r));
+    }
+    // main accumulator (codes x weight) and the one for terms more than 80
+    // nats down, kept 2^80 larger
+    float l = 0.f, a[C], b[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) a[c] = b[c] = 0.f;
+    if (m != neg_inf()) {
+      for (int t = lo; t < hi; ++t) {
+        const long long r = row_of(t);
+        if (r < 0) continue;
+        const float z = score(qh, r) - m;
+        const float w = expf(z);
+        l += w;
+        if (z >= -80.f) {
+#pragma unroll
+          for (int c = 0; c < C; ++c) a[c] = fmaf(w, value(p.v, r, lane + 32 * c), a[c]);
+        } else {
+          const float ws = exp2f(fmaf(z, kLog2e, 80.f));
+#pragma unroll
+          for (int c = 0; c < C; ++c) b[c] = fmaf(ws, value(p.v, r, lane + 32 * c), b[c]);
+        }
+      }
+    }
+    if (direct) {
+      float sc = 0.f;
+      if (l > 0.f) {
+        sc = 1.f / l;
+        if (p.sink != nullptr) sc *= 1.f / (1.f + expf(p.sink[g * G + h] - (m + logf(l))));
+      }
+      __half* o = reinterpret_cast<__half*>(p.out) + (head0 + h) * D;
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
+        const int d = lane + 32 * c;
+        const float vs = FP16C ? 1.f : svs[d];
+        o[d] = __float2half_rn(sc == 0.f ? 0.f : (a[c] * vs + b[c] * (vs * 0x1p-80f)) * sc);
+      }
+      if (lane == 0 && p.lse != nullptr) p.lse[head0 + h] = l > 0.f ? m + logf(l) : neg_inf();
+    } else {
+      const long long base = ((long long)unit * p.num_splits + split) * G + h;
+      if (l > 0.f) {
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+          const int d = lane + 32 * c;
+          const float vs = FP16C ? 1.f : svs[d];
+          p.ws_acc[base * D + d] = a[c] * vs + b[c] * (vs * 0x1p-80f);
+        }
+      }
+      if (lane == 0) {
+        p.ws_m[base] = l > 0.f ? m : neg_inf();
+        p.ws_l[base] = l;
+      }
+    }
+  }
+}
+
 template <int D, int NT, bool PAGED, bool FP16C, bool PLO, bool FP8>
 __global__ void __launch_bounds__((Tile<D, NT, FP16C, PAGED>::kThreads),
                                   (Tile<D, NT, FP16C, PAGED>::kMinBlocks))
@@ -163,9 +308,13 @@ decode_kernel(const DecodeParams p) {
 
   // value scales of this KV head, staged in shared memory for the epilogue
   float* svs = reinterpret_cast<float*>(smem + T::kVsOffset);
+  bool vs_bad = false;  // a value scale is not finite
   if constexpr (!FP16C) {
-    for (int d = threadIdx.x; d < D; d += kThreads)
-      svs[d] = p.per_channel ? p.v_scale[g * D + d] : p.v_scale[0];
+    for (int d = threadIdx.x; d < D; d += kThreads) {
+      const float v = p.per_channel ? p.v_scale[g * D + d] : p.v_scale[0];
+      svs[d] = v;
+      vs_bad |= !(fabsf(v) <= 3.4028235e38f);
+    }
   }
   constexpr int MT_ITERS = (KC + kWarps - 1) / kWarps;
 
@@ -348,13 +497,20 @@ decode_kernel(const DecodeParams p) {
   }
 
   // ---------------- Q' = fp16(Q * k_scale), staged through shared memory ----------------
+  // The CTA takes the FP32 path when an element of Q * k_scale is not finite or
+  // beyond the fp16 range, when for some head eps = sigma * |code|max *
+  // sum_d |Q'_d - fp16(Q'_d)| (a bound on the logit shift from rounding Q')
+  // exceeds the budget, or when a value scale is not finite.
   __half* sq = reinterpret_cast<__half*>(smem + T::kRingBytes + T::kMaskBytes);
+  bool use_fp32 = false;
+  bool vs_big_cta = false;
   {
-    bool bad = false;
+    constexpr float kCodeMax = FP8 ? 448.f : 128.f;
+    bool bad = false, over = false;
 #pragma unroll
     for (int i = 0; i < kQSteps; ++i) {
       const int e = threadIdx.x + i * kThreads;
-      if (e >= NT * D) break;
+      if (e >= NT * D) break;  // uniform per warp (NT * D is a multiple of 32)
       const int h = (e * 8) / D, d0 = (e * 8) % D;
       uint4 packed = q_raw[i];
       if constexpr (!FP16C) {
@@ -362,18 +518,41 @@ decode_kernel(const DecodeParams p) {
         const float ks[8] = {ks_raw[i][0].x, ks_raw[i][0].y, ks_raw[i][0].z, ks_raw[i][0].w,
                              ks_raw[i][1].x, ks_raw[i][1].y, ks_raw[i][1].z, ks_raw[i][1].w};
         uint32_t w[4];
+        float err = 0.f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float2 f = __half22float2(qh[j]);
           const float x0 = f.x * ks[2 * j], x1 = f.y * ks[2 * j + 1];
           bad |= !(fabsf(x0) <= 65504.f) || !(fabsf(x1) <= 65504.f);
           w[j] = pack_h2(x0, x1);
+          const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+          err += fabsf(x0 - r.x) + fabsf(x1 - r.y);
         }
         packed = make_uint4(w[0], w[1], w[2], w[3]);
+        // sum over the D / 8 consecutive lanes holding this head's pieces
+#pragma unroll
+        for (int o = 1; o < D / 8 && o < 32; o <<= 1) err += __shfl_xor_sync(0xffffffffu, err, o);
+        over |= h < G && p.sigma * kCodeMax * err > kQueryErrorBudget;
       }
       *reinterpret_cast<uint4*>(sq + h * T::kQStride + d0) = packed;
     }
-    if (__syncthreads_or(bad) && threadIdx.x == 0) flag_or(p.flags, I8KV_FLAG_QUERY_RANGE);
+    if (bad) flag_or(p.flags, I8KV_FLAG_QUERY_RANGE);
+    use_fp32 = __syncthreads_or(bad || over || vs_bad);
+    // some |value_scale| above 2^16 (the staged scales are visible after the
+    // barrier; each warp reads them all, so no second barrier is needed)
+    if constexpr (!FP16C) {
+      bool big = false;
+#pragma unroll
+      for (int d = lane; d < D; d += 32) big |= fabsf(svs[d]) > kMaxValueScale;
+      vs_big_cta = __any_sync(0xffffffffu, big);
+    }
+  }
+  if (use_fp32) {
+    cp_async_wait_all();
+    __syncthreads();  // every warp's gathers have landed: the ring is free
+    if (threadIdx.x == 0) flag_or(p.flags, I8KV_FLAG_FP32_PATH);
+    attend_fp32<D, PAGED, FP16C, FP8, kThreads>(p, reinterpret_cast<float*>(smem), svs);
+    return;
   }
   // B fragments of Q'^T (k = channel, n = head) in the contraction order of the
   // K fragments: int8 caches take channels 16kc + 4tig + {0,1} / {2,3}, fp16
@@ -410,6 +589,8 @@ decode_kernel(const DecodeParams p) {
     lrun[nt][0] = lrun[nt][1] = 0.f;
   }
 
+  bool deep = false;
+
   // ldmatrix lane address: matrix m = lane/8 covers tokens (lane%8) + 8*(m&1)
   // of the tile and 16-byte chunk 2*c2 + (m>>1)
   const int ld_row = (lane & 7) + 8 * ((lane >> 3) & 1);
@@ -420,6 +601,11 @@ decode_kernel(const DecodeParams p) {
   const float softcap = p.softcap;
   const float cap_k = 2.f * kLog2e / softcap;  // used only when softcap > 0
 
+  // The main loop, instantiated twice: with the tail-depth tracking (a CTA with
+  // some |value_scale| above 2^16) and without it (every other CTA), so that
+  // the common loop carries none of it.
+  auto main_loop = [&](auto track_tag) {
+  constexpr bool kTrackDeep = decltype(track_tag)::value;
   for (int k = 0; k < my_n; ++k) {
     issue(k + T::kStages - 1, q0);
     q0 = q1;
@@ -544,6 +730,12 @@ decode_kernel(const DecodeParams p) {
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
         const float mnew = fmaxf(mrun[nt][j], mx);
         const float base = mnew == neg_inf() ? 0.f : mnew;
+        if constexpr (kTrackDeep) {  // a valid score more than kTailDepth below the running max
+#pragma unroll
+          for (int s = 0; s < SUB; ++s)
+            deep |= (sc[s][j] != neg_inf() && sc[s][j] < mnew - kTailDepth) ||
+                    (sc[s][2 + j] != neg_inf() && sc[s][2 + j] < mnew - kTailDepth);
+        }
         changed |= mnew != mrun[nt][j];
         alpha[nt][j] = fast_exp2((mrun[nt][j] - base) * kLog2e);
         float lsum = 0.f;
@@ -645,7 +837,20 @@ decode_kernel(const DecodeParams p) {
     }
     __syncwarp();
   }
+  };
+  if (vs_big_cta)
+    main_loop(std::true_type{});
+  else
+    main_loop(std::false_type{});
   cp_async_wait_all();
+
+  // a large value scale with a deep candidate: some probability was below the
+  // fp16 tile's range, so the CTA starts over on the FP32 path
+  if (vs_big_cta && __syncthreads_or(deep)) {
+    if (threadIdx.x == 0) flag_or(p.flags, I8KV_FLAG_FP32_PATH);
+    attend_fp32<D, PAGED, FP16C, FP8, kThreads>(p, reinterpret_cast<float*>(smem), svs);
+    return;
+  }
 
   // ---------------- merge the four warps' partials ----------------
   // (m, l) per head of every warp; l is first summed over the 8 lanes that

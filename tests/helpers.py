@@ -34,7 +34,19 @@ def paged_to_device(c):
                 vs=dev(c.v_scale), bt=dev(c.block_table), lens=dev(c.seq_lens), sink=dev(c.sink))
 
 
-def run_dsa(c, d=None, num_splits=0, chunk=0, prefill=False, flags=None):
+def _unpack_partials(ws, units, ns, G, D):
+    """Workspace floats -> (m, l [units, ns, G], acc [units, ns, G, D]) float64."""
+    w = ws.cpu().numpy().astype(np.float64)
+    n = units * ns * G
+    acc = w[:n * D].reshape(units, ns, G, D)
+    m = w[n * D:n * (D + 1)].reshape(units, ns, G)
+    l = w[n * (D + 1):n * (D + 2)].reshape(units, ns, G)
+    return m, l, acc
+
+
+def run_dsa(c, d=None, num_splits=0, chunk=0, prefill=False, flags=None, partials=False):
+    """Sparse decode (or prefill) through the binding: (O, lse) as float64, or
+    with ``partials`` the workspace partials of a partials-only decode call."""
     d = d or sparse_to_device(c)
     S, Hq, D = c.q.shape
     Hkv = c.k_codes.shape[1]
@@ -51,8 +63,12 @@ def run_dsa(c, d=None, num_splits=0, chunk=0, prefill=False, flags=None):
         wsb = K.split_workspace_bytes(S * Hkv, ns, Hq // Hkv, D)
         ws = torch.full((max(wsb // 4, 1),), float("nan"), dtype=torch.float32, device="cuda")
         K.dsa_decode(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"], c.sigma,
-                     d["sink"], num_splits=ns, chunk=chunk, workspace=ws, out=out, lse=lse,
-                     flags=flags)
+                     d["sink"], num_splits=ns, chunk=chunk, workspace=ws,
+                     out=None if partials else out, lse=None if partials else lse, flags=flags,
+                     partials_only=partials)
+        if partials:
+            torch.cuda.synchronize()
+            return _unpack_partials(ws, S * Hkv, ns, Hq // Hkv, D)
     torch.cuda.synchronize()
     return out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
@@ -84,12 +100,7 @@ def run_paged(c, d=None, num_splits=0, chunk=0, slots=False, flags=None, softcap
                    flags=flags, partials_only=partials, softcap=softcap, window=window)
     torch.cuda.synchronize()
     if partials:
-        u = B * Hkv
-        w = ws.cpu().numpy().astype(np.float64)
-        acc = w[:u * ns * G * D].reshape(u, ns, G, D)
-        m = w[u * ns * G * D:u * ns * G * (D + 1)].reshape(u, ns, G)
-        l = w[u * ns * G * (D + 1):u * ns * G * (D + 2)].reshape(u, ns, G)
-        return m, l, acc
+        return _unpack_partials(ws, B * Hkv, ns, G, D)
     res = (out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64))
     if slots:
         res = res + (so.cpu().numpy(),)

@@ -418,3 +418,25 @@ def tiny_probability_case(q0: float, v_code: int, v_scale: float, D: int = 64,
     vB = np.zeros(D, np.int8); vB[0] = v_code
     return two_candidate(q, kA, kB, vA, vB, k_scale=1.0, v_scale=v_scale, sigma=1.0 / 16.0,
                          spread=spread)
+
+
+def query_folding_case(spread: bool = False) -> SparseCase:
+    """Per-channel key scales 32768 and 32766 on query channels +1 and -1: the
+    products Q * k_scale are 32768 and -32766, which fp16 rounds to 32768 and
+    -32768.  Key codes 8 on both channels for candidate A, 0 for B; sigma 1:
+    logits 16 and 0 (0 and 0 after the rounding).  Value code 1 on channel 0
+    for A."""
+    D = 64
+    q = np.zeros(D); q[0], q[1] = 1.0, -1.0
+    kA = np.zeros(D, np.int8); kA[0] = kA[1] = 8
+    kB = np.zeros(D, np.int8)
+    vA = np.zeros(D, np.int8); vA[0] = 1
+    vB = np.zeros(D, np.int8)
+    c = two_candidate(q, kA, kB, vA, vB, k_scale=1.0, v_scale=1.0, sigma=1.0, spread=spread)
+    ks = np.ones((1, D), np.float32)
+    ks[0, 0], ks[0, 1] = 32768.0, 32766.0
+    c.k_scale = ks
+    c.v_scale = np.ones((1, D), np.float32)
+    c.scale_kind = SCALE_PER_CHANNEL
+    c.meta = dict(name="query folding", spread=spread)
+    return c
