@@ -506,14 +506,22 @@ def _deep(torch, K, W, np, t, dev, bench_graph, hbm, cache):
         ws = torch.empty(max(wsb // 4, 4), dtype=torch.float32, device=dev)
         out = torch.empty_like(q)
 
-        def fn():
+        def fn(partials=False):
             for x in copies:
                 K.paged_decode(q, x["k"], x["v"], ks, vs, c.scale_kind, bt, lens, c.sigma,
-                               num_splits=ns, chunk=chunk, workspace=ws, out=out)
+                               num_splits=ns, chunk=chunk, workspace=ws,
+                               out=None if partials else out, partials_only=partials)
         sec = bench_graph(fn, R, reps=100)
         row[label] = dict(us_per_call=round(sec * 1e6, 2), gbs=round(byts / sec / 1e9, 1),
                           frac_of_hbm=round(byts / sec / 1e9 / hbm, 4), num_splits=ns,
                           chunk=chunk)
+        if ns > 1:
+            # the decode kernel alone (partials only, no combine); its bytes
+            # exclude the output
+            kb = byts - B * Hq * Dh * 2
+            ks_ = bench_graph(lambda: fn(True), R, reps=100)
+            row[label].update(kernel_us=round(ks_ * 1e6, 2),
+                              kernel_frac_of_hbm=round(kb / ks_ / 1e9 / hbm, 4))
     return dict(workload=f"deep context: 16 rows, {cache} cache, live 2600 of cap 4096, 16/2 "
                          "heads, head_dim 128", bytes_per_call=byts, rotating_copies=R, **row)
 

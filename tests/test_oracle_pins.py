@@ -389,3 +389,13 @@ def test_fp16_cache_taken_as_is():
     s = c.sigma * (K @ c.q[0, 0].astype(np.float64))
     w = np.exp(s - s.max())
     np.testing.assert_allclose(O[0, 0], (w @ V) / w.sum(), rtol=1e-12)
+
+
+def test_query_folding_case_closed_form():
+    # logits sigma * (32768 * 8 - 32766 * 8) = 16 and 0, values 1 and 0
+    c = W.query_folding_case()
+    O, L = oracle.sparse_attention(c.q, c.k_codes, c.v_codes, c.k_scale, c.v_scale, c.scale_kind,
+                                   c.idx, c.sigma)
+    assert O[0, 0, 0] == pytest.approx(1.0 / (1.0 + math.exp(-16.0)), rel=1e-15)
+    assert L[0, 0] == pytest.approx(16.0 + math.log1p(math.exp(-16.0)), rel=1e-15)
+    assert np.all(O[0, :, 1:] == 0)
