@@ -232,6 +232,23 @@ def capture(torch, fn, stream):
     return g
 
 
+def layer_seed(rank: int, layer: int) -> int:
+    """Seed of one layer's synthetic inputs: every rank decodes layers of its
+    own (replicas; weak scaling)."""
+    return 1000 * rank + layer
+
+
+def max_over_ranks(dist, value: float, device) -> float:
+    """The largest of the ranks' values: the whole job ends with its slowest
+    rank.  No process group: the value itself."""
+    if dist is None:
+        return value
+    import torch
+    tt = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
 def gpu_arm(args, rank, world, local_rank, dist):
     import numpy as np
     import torch
@@ -250,7 +267,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
     # ---- inputs: L layers, each its own cache / rows / lists (seeded) ----
     layers = []
     for li in range(L):
-        c = W.sparse_decode(S_ROWS, seed=1000 * rank + li)
+        c = W.sparse_decode(S_ROWS, seed=layer_seed(rank, li))
         t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
         layers.append(dict(q=t(c.q), k=t(c.k_codes), v=t(c.v_codes), ks=t(c.k_scale),
                            vs=t(c.v_scale), idx=t(c.idx), case=c if li == 0 else None,
@@ -289,10 +306,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
-    if dist is not None:
-        tt = torch.tensor([t], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
+    t = max_over_ranks(dist, t, dev)
 
     b = call_bytes()
     bytes_call = sum(b.values())
@@ -338,11 +352,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
             e2e_step()
         s1.record(stream)
     s1.synchronize()
-    te = s0.elapsed_time(s1) / 1e3
-    if dist is not None:
-        tt = torch.tensor([te], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        te = float(tt.item())
+    te = max_over_ranks(dist, s0.elapsed_time(s1) / 1e3, dev)
     e2e = dict(value=e2e_steps * L * world * bytes_call / te / 1e9, unit="GB/s",
                h2d_bytes_per_step=L * (b["q"] + b["idx"]), d2h_bytes_per_step=L * b["out"],
                us_per_call=te / (e2e_steps * L) * 1e6, steps=e2e_steps,
