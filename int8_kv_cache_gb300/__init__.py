@@ -125,17 +125,21 @@ def _check(fn: str, status: int):
         raise Int8KVError(fn, status, detail)
 
 
-def _t(x: Optional[torch.Tensor], dtype, name: str, device=None) -> Optional[int]:
+def _t(x: Optional[torch.Tensor], dtype, name: str) -> Optional[int]:
     """Device pointer of a contiguous CUDA tensor of the given dtype (None -> NULL)."""
     if x is None:
         return None
-    if not isinstance(x, torch.Tensor):
-        raise TypeError(f"{name} must be a torch.Tensor")
-    if dtype is not None and x.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
-        raise TypeError(f"{name}: expected {dtype}, got {x.dtype}")
-    if not x.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
-    if not x.is_contiguous():
+    try:
+        ok = (dtype is None or x.dtype == dtype or
+              (type(dtype) is tuple and x.dtype in dtype)) and x.is_cuda and x.is_contiguous()
+    except AttributeError:
+        raise TypeError(f"{name} must be a torch.Tensor") from None
+    if not ok:
+        if dtype is not None and x.dtype != dtype and not (type(dtype) is tuple and
+                                                           x.dtype in dtype):
+            raise TypeError(f"{name}: expected {dtype}, got {x.dtype}")
+        if not x.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
         raise ValueError(f"{name} must be contiguous")
     return x.data_ptr()
 
