@@ -65,6 +65,7 @@ def parse():
                     help="which other workloads to measure besides the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--reference-worker", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -90,6 +91,36 @@ def cpu_worker(spec: str):
             break
     dt = time.perf_counter() - t0
     print(json.dumps(dict(calls=calls, seconds=dt)))
+
+
+def reference_worker(spec: str):
+    """The reference arm in one child process with single-threaded BLAS: the
+    FP64 oracle on the headline workload, W warm-up and K timed steps, each step
+    whole query rows (both KV heads of a row: 1/8 of a call), as many as keep
+    the whole run near its time budget."""
+    import oracle
+    import workloads as W
+    a = json.loads(spec)
+    c = W.sparse_decode(S_ROWS, seed=0)
+
+    def rows(r0, n):
+        for i in range(n):
+            r = (r0 + i) % S_ROWS
+            oracle.sparse_attention(c.q[r:r + 1], c.k_codes, c.v_codes, c.k_scale, c.v_scale,
+                                    c.scale_kind, c.idx[r:r + 1], c.sigma)
+    t0 = time.perf_counter()
+    rows(0, 1)
+    t_row = time.perf_counter() - t0
+    n = max(1, int(a["budget"] / max(1, a["steps"] + a["warmup"]) / max(t_row, 1e-6)))
+    r = 0
+    for _ in range(a["warmup"]):
+        rows(r, n)
+        r += n
+    t0 = time.perf_counter()
+    for _ in range(a["steps"]):
+        rows(r, n)
+        r += n
+    print(json.dumps(dict(rows=n * a["steps"], rows_per_step=n, seconds=time.perf_counter() - t0)))
 
 
 def run_cpu_oracle(budget_s: float, max_calls: int = 1000000, seed: int = 0):
@@ -570,28 +601,31 @@ def _prefill(torch, K, W, np, t, bench_graph, peaks):
 
 
 def reference_arm(args, rank, world):
-    """The FP64 oracle on the host cores, each step a bounded sample (whole
-    calls of the headline workload for about args-determined seconds)."""
+    """The FP64 oracle on the host cores (one process, single-threaded BLAS),
+    on the headline workload, metric and unit; each step is a bounded sample of
+    whole query rows, sized so the whole run stays near two minutes.  Under
+    torchrun only rank 0 runs and prints."""
     if rank != 0:
         return None
-    per_step = max(0.5, min(10.0, 60.0 / max(1, args.steps + args.warmup)))
-    for _ in range(args.warmup):
-        run_cpu_oracle(per_step, max_calls=1)
-    tot_s, tot_calls = 0.0, 0
-    for _ in range(args.steps):
-        r = run_cpu_oracle(per_step)
-        tot_s += r["seconds"]
-        tot_calls += r["calls"]
-    b = sum(call_bytes().values())
-    v = tot_calls * b / tot_s / 1e9
-    sample = (f"{tot_calls} whole call(s) of the headline workload over {args.steps} step(s), "
-              "FP64 NumPy oracle, single-threaded BLAS")
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    spec = json.dumps(dict(steps=args.steps, warmup=args.warmup, budget=120.0))
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--reference-worker", spec],
+                       capture_output=True, text=True, env=env, cwd=ROOT)
+    if r.returncode != 0:
+        raise RuntimeError(f"reference worker failed: {r.stderr[-2000:]}")
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    row_bytes = sum(call_bytes().values()) / S_ROWS
+    v = res["rows"] * row_bytes / res["seconds"] / 1e9
+    sample = (f"{res['rows_per_step']} query row(s) per step (both KV heads; a call is "
+              f"{S_ROWS} rows) of the headline workload, {args.steps} timed step(s) after "
+              f"{args.warmup} warm-up, FP64 NumPy oracle, single-threaded BLAS")
     return {"metric": "INT8 split-KV decode us/call and achieved HBM GB/s (% of GB300 peak)",
             "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": tot_s / args.steps * 1e3,
-            "us_per_call": tot_s / tot_calls * 1e6, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD}, "impl": "reference",
+            "warmup": args.warmup, "ms_per_step": res["seconds"] / args.steps * 1e3,
+            "us_per_call": res["seconds"] / res["rows"] * S_ROWS * 1e6,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD}, "impl": "reference",
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -602,6 +636,9 @@ def main():
     args = parse()
     if args.cpu_worker is not None:
         cpu_worker(args.cpu_worker)
+        return
+    if args.reference_worker is not None:
+        reference_worker(args.reference_worker)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
