@@ -219,10 +219,15 @@ def measured_peaks():
 
 
 def kernel_sources_digest():
+    """Digest of the decode kernel's code (comments and blank lines dropped, so
+    that only a change of the code itself retires a committed ncu figure)."""
     h = hashlib.sha256()
     for f in ("decode_kernel.cuh", "device.cuh"):
-        with open(os.path.join(ROOT, "int8_kv_cache_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "int8_kv_cache_gb300", "csrc", f)) as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].strip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -9,13 +9,21 @@
 // partial (m, l, acc * 2^-15 * v_scale) of the split, or, with one split, the
 // normalised output, the log-sum-exp and the head-sink rescale.
 //
-// Design (GB300, sm_103a, 128 threads = 4 warps per CTA):
-//   * Warp-private pipelines.  Warp w owns the 16-token slices w, w+4, w+8, ...
-//     of the split.  It gathers each slice's K and V rows with 16-byte
-//     cp.async copies into its own shared-memory ring (kStages deep), so its
-//     loads stay in flight while it computes earlier slices, and it runs its
-//     own online softmax.  The warps meet once, at the end, to merge their
-//     (m, l, acc) through shared memory.  No warp waits on another in the loop.
+// Design (GB300, sm_103a):
+//   * CTA shape.  The sparse-candidate kernel runs one CTA per SM of 4 to 16
+//     warps (as many 4-warp groups as the registers and shared memory allow);
+//     the paged kernel runs 4-warp CTAs, 2 to 4 per SM, so that the splits of
+//     sequences of very different lengths spread over the SMs.
+//   * Warp-private pipelines.  Warp w owns the steps w, w + kWarps, ... of the
+//     split (a step is 16 tokens, or 32 when two tiles fit the registers).  It
+//     gathers each step's K and V rows with 16-byte cp.async copies into its
+//     own shared-memory ring (2 to 4 stages), so its loads stay in flight while
+//     it computes earlier steps, and it runs its own online softmax.  The warps
+//     meet once, at the end, to merge their (m, l, acc) through shared memory.
+//     No warp waits on another in the loop.
+//   * Numerical eligibility.  A CTA whose FP16 rounding cannot be bounded
+//     (query folding beyond the budget, a non-finite value scale, a large value
+//     scale with a deep tail) evaluates its heads on the FP32 path instead.
 //   * Tensor cores.  QK^T is S^T[token][head] = K[token][d] * Q'[head][d]^T
 //     with tokens as the M=16 dimension and the group's query heads as N (8 per
 //     tile, G <= 8 -> 1 tile, G <= 16 -> 2): mma.sync m16n8k16 f16 x f16 -> f32.
@@ -340,7 +348,7 @@ decode_kernel(const DecodeParams p) {
   const int nhi = min(lo + p.chunk, cap);
 
   // ---------------- per-warp gather pipeline ----------------
-  // Warp w takes the steps w, w+4, w+8, ... of kStep consecutive positions.
+  // Warp w takes the steps w, w + kWarps, ... of kStep consecutive positions.
   int* wmask = reinterpret_cast<int*>(smem + T::kRingBytes) + warp * 4;
   const uint32_t ring_addr = smem_addr(smem + warp * T::kWarpRing);
 

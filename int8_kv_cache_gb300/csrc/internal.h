@@ -47,7 +47,7 @@ struct KernelKey {
   bool p_lo;       // probability tile as fp16 high + low parts
 };
 
-// Launch one decode / prefill kernel: grid (rows * Hkv, num_splits), 128 threads.
+// Launch one decode / prefill kernel: grid (rows * Hkv, num_splits).
 cudaError_t launch_decode(const KernelKey& key, const DecodeParams& p, cudaStream_t stream);
 
 // Resident CTAs per SM of that kernel (occupancy API), or -1 if no such kernel.
