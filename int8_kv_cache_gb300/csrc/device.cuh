@@ -131,13 +131,11 @@ __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
 
 // Programmatic dependent launch: wait until the preceding grid of the stream
 // has completed and its writes are visible (returns at once when the kernel
-// was launched without the programmatic-serialization attribute) ...
+// was launched without the programmatic-serialization attribute).  No kernel
+// here triggers its dependents early: measured, an early trigger made the
+// decode + combine pair slower.
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
-}
-// ... and let the next grid of the stream start launching.
-__device__ __forceinline__ void grid_dependents_launch() {
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
 __device__ __forceinline__ void flag_or(uint32_t* flags, uint32_t bits) {
