@@ -363,6 +363,26 @@ def gpu_arm(args, rank, world, local_rank, dist):
     achieved = kernel_bytes / t_kernel / 1e9
     traffic = ncu_traffic("dsa_decode_S8")
 
+    # ---- context: 7 rounds of the captured step, and uncaptured launches ----
+    rounds = []
+    for _ in range(7):
+        rounds.append(time_graph(torch, g, max(20, min(args.steps, 200)), stream) /
+                      (max(20, min(args.steps, 200)) * L) * 1e6)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        n_eager = max(3, min(args.steps, 50))
+        for _ in range(n_eager):
+            step()
+        e1.record(stream)
+    e1.synchronize()
+    eager_us = e0.elapsed_time(e1) * 1e3 / (n_eager * L)
+    attended = S_ROWS * N_SEL  # candidates per call (every list entry is valid)
+
     # ---- end to end through the public API with host buffers ----
     # Every step copies all layers' query rows and candidate lists from one
     # pinned host buffer (one copy each), calls dsa_decode per layer through
@@ -429,6 +449,12 @@ def gpu_arm(args, rank, world, local_rank, dist):
                      "bytes_per_launch": kernel_bytes, "peak_source": f"{peak_src} hbm_gbs"},
         "clocks": clk,
         "e2e": e2e,
+        "context": {"rounds_us_per_call": [round(r, 3) for r in rounds],
+                    "median_of_7_us_per_call": round(statistics.median(rounds), 3),
+                    "attended_tokens_per_s": round(attended * calls / t),
+                    "uncaptured_us_per_call": round(eager_us, 3),
+                    "note": "rounds: the captured step re-timed 7 times after the timed "
+                            "region; uncaptured: the same calls launched eagerly from Python"},
     }
     if args.extra != "none":
         out["other_configs"] = extra_configs(torch, K, W, np, dev, stream, peaks, args)
