@@ -61,7 +61,7 @@ def parse():
     ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--extra", default="all",
                     choices=["all", "paged", "variants", "fp8", "deep", "prefill", "quantize",
-                             "none"],
+                             "engine", "none"],
                     help="which other workloads to measure besides the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
@@ -493,7 +493,42 @@ def extra_configs(torch, K, W, np, dev, stream, peaks, args):
     if args.extra in ("all", "quantize", "fp8"):
         res["quantize_on_write"] = _quantize(torch, K, np, t, dev, bench_graph, hbm)
         res["quantize_on_write_fp8"] = _quantize(torch, K, np, t, dev, bench_graph, hbm, "fp8")
+    if args.extra in ("all", "engine"):
+        with K.engine(K.ENGINE_TCGEN05):
+            res["engine_tcgen05"] = _engine_tc(torch, K, W, np, t, dev, bench_graph, hbm)
     return res
+
+
+def _engine_tc(torch, K, W, np, t, dev, bench_graph, hbm):
+    """The tcgen05 decode engine on the headline sparse decode (S = 8, 32
+    layers) and on the deep-context int8 sweep's adaptive geometry: the call
+    and the decode kernel alone, for comparison with the default engine."""
+    L = 32
+    layers = []
+    for li in range(L):
+        c = W.sparse_decode(S_ROWS, seed=li)
+        layers.append(dict(q=t(c.q), k=t(c.k_codes), v=t(c.v_codes), ks=t(c.k_scale),
+                           vs=t(c.v_scale), idx=t(c.idx)))
+    ns, chunk, wsb, wave = K.decode_plan(K.PATH_DSA, K.CACHE_INT8, N_SEL, S_ROWS, HQ, HKV, D,
+                                         K.GEOM_POW2_TILES)
+    ws = torch.empty(max(wsb // 4, 4), dtype=torch.float32, device=dev)
+    out = torch.empty((S_ROWS, HQ, D), dtype=torch.float16, device=dev)
+
+    def fn(partials=False):
+        for x in layers:
+            K.dsa_decode(x["q"], x["k"], x["v"], x["ks"], x["vs"], W.SCALE_PER_CHANNEL, x["idx"],
+                         SIGMA, num_splits=ns, chunk=chunk, workspace=ws,
+                         out=None if partials else out, partials_only=partials)
+    b = sum(call_bytes().values())
+    sec = bench_graph(fn, L)
+    ksec = bench_graph(lambda: fn(True), L)
+    kb = b - S_ROWS * HQ * D * 2
+    head = dict(us_per_call=round(sec * 1e6, 2), kernel_us=round(ksec * 1e6, 2),
+                kernel_frac_of_hbm=round(kb / ksec / 1e9 / hbm, 4), num_splits=ns, chunk=chunk,
+                wave_ctas=wave)
+    deep = _deep(torch, K, W, np, t, dev, bench_graph, hbm, "int8")
+    return dict(workload="tcgen05 decode engine: " + WORKLOAD + "; and " + deep["workload"],
+                headline=head, deep_context_int8=deep["adaptive"])
 
 
 def _quantize(torch, K, np, t, dev, bench_graph, hbm, cache="int8"):

@@ -88,6 +88,8 @@ typedef enum {
 #define I8KV_FLAG_BAD_SLOT 0x8u    /* reshape_and_cache: a slot >= num_slots was skipped      */
 #define I8KV_FLAG_FP32_PATH 0x10u  /* some CTA evaluated its heads on the FP32 path (see the
                                       numerical eligibility rules below)                     */
+#define I8KV_FLAG_WAIT_TIMEOUT 0x20u /* a CTA gave up waiting (about a second) for its own
+                                        tensor-core products; its outputs were not written */
 
 /* Human-readable name of a status code (static storage). */
 const char* i8kv_status_string(int status);
@@ -98,6 +100,27 @@ int32_t i8kv_version(void);
 /* The cudaError_t value behind the calling thread's most recent I8KV_ECUDA
  * (0 if there was none). */
 int32_t i8kv_last_cuda_error(void);
+
+/* Decode engines: the kernel family behind dsa_decode, dsa_decode_static_workspace
+ * and paged_decode(_ex). */
+#define I8KV_ENGINE_MMA 0     /* mma.sync m16n8k16 tiles with the exact int8 -> fp16
+                                 conversion in registers (the default)               */
+#define I8KV_ENGINE_TCGEN05 1 /* tcgen05 MMAs with tensor-memory accumulators, one per
+                                 CTA, operands converted into shared memory          */
+
+/*
+ * i8kv_set_decode_engine -- select the decode engine for the whole process.
+ * The tcgen05 engine serves int8 and e4m3fn caches with head_dim 128 or 256;
+ * fp16 caches, other head dims and dsa_prefill always run on the MMA engine.
+ * Both engines compute the same quantities under the same geometry rules, but
+ * decode_plan's wave (and so the automatic geometry) is the selected engine's:
+ * select it before planning, and not while another thread plans or launches.
+ * Errors: I8KV_EINVAL for an unknown engine.
+ */
+i8kv_status i8kv_set_decode_engine(int32_t engine);
+
+/* The selected decode engine (I8KV_ENGINE_*). */
+int32_t i8kv_decode_engine(void);
 
 /*
  * split_geometry -- pure host integer arithmetic, no CUDA call.

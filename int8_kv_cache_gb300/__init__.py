@@ -10,6 +10,7 @@ no fallback.  PyTorch provides device memory and streams.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional
@@ -20,7 +21,9 @@ __all__ = [
     "Int8KVError", "load", "library_path", "split_geometry", "split_workspace_bytes",
     "decode_plan", "dsa_decode", "dsa_prefill", "paged_decode", "split_combine", "int8_to_fp16",
     "dsa_decode_static_workspace", "STATIC_WORKSPACE_BYTES", "reshape_and_cache",
-    "FLAG_BAD_SLOT", "FLAG_FP32_PATH", "paged_decode_ex", "window_span", "CACHE_FP8", "fp8_to_fp16",
+    "FLAG_BAD_SLOT", "FLAG_FP32_PATH", "FLAG_WAIT_TIMEOUT", "ENGINE_MMA", "ENGINE_TCGEN05",
+    "set_decode_engine", "decode_engine", "engine", "paged_decode_ex", "window_span",
+    "CACHE_FP8", "fp8_to_fp16",
     "SCALE_PER_TENSOR", "SCALE_PER_CHANNEL", "CACHE_INT8", "CACHE_FP16", "GEOM_WAVE",
     "GEOM_POW2_TILES", "PATH_DSA", "PATH_PAGED", "MAX_SPLITS", "FLAG_LEN_CLAMPED",
     "FLAG_QUERY_RANGE", "FLAG_BAD_BLOCK",
@@ -41,6 +44,9 @@ FLAG_QUERY_RANGE = 0x2
 FLAG_BAD_BLOCK = 0x4
 FLAG_BAD_SLOT = 0x8
 FLAG_FP32_PATH = 0x10
+FLAG_WAIT_TIMEOUT = 0x20
+ENGINE_MMA = 0
+ENGINE_TCGEN05 = 1
 STATIC_WORKSPACE_BYTES = 4 * 1024 * 1024
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -55,6 +61,8 @@ _SIGNATURES = {
     "i8kv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "i8kv_version": (_c_i32, []),
     "i8kv_last_cuda_error": (_c_i32, []),
+    "i8kv_set_decode_engine": (_c_i32, [_c_i32]),
+    "i8kv_decode_engine": (_c_i32, []),
     "split_geometry": (_c_i32, [_c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                 _P_I32, _P_I32]),
     "split_workspace_bytes": (_c_sz, [_c_i32, _c_i32, _c_i32, _c_i32]),
@@ -168,6 +176,26 @@ def split_geometry(cap: int, units: int, wave_ctas: int, granule: int, min_chunk
 
 def split_workspace_bytes(units: int, num_splits: int, G: int, D: int) -> int:
     return int(load().split_workspace_bytes(units, num_splits, G, D))
+
+
+def set_decode_engine(engine: int) -> None:
+    """Select the process-wide decode engine (ENGINE_MMA or ENGINE_TCGEN05)."""
+    _check("i8kv_set_decode_engine", load().i8kv_set_decode_engine(engine))
+
+
+def decode_engine() -> int:
+    return int(load().i8kv_decode_engine())
+
+
+@contextlib.contextmanager
+def engine(e: int):
+    """Run a block with another decode engine selected, then restore the previous one."""
+    prev = decode_engine()
+    set_decode_engine(e)
+    try:
+        yield
+    finally:
+        set_decode_engine(prev)
 
 
 def decode_plan(path: int, cache_dtype: int, cap: int, rows: int, Hq: int, Hkv: int, D: int,

@@ -47,6 +47,18 @@ def test_version_and_status_strings(lib):
     assert lib.i8kv_status_string(4).startswith(b"workspace")
 
 
+def test_decode_engine_selection(lib):
+    # host-side setting: no CUDA call
+    assert lib.i8kv_decode_engine() == 0
+    assert lib.i8kv_set_decode_engine(1) == 0
+    assert lib.i8kv_decode_engine() == 1
+    assert lib.i8kv_set_decode_engine(2) == 1      # unknown engine: EINVAL, unchanged
+    assert lib.i8kv_set_decode_engine(-1) == 1
+    assert lib.i8kv_decode_engine() == 1
+    assert lib.i8kv_set_decode_engine(0) == 0
+    assert lib.i8kv_decode_engine() == 0
+
+
 def test_geometry_bit_exact_with_oracle(lib):
     import int8_kv_cache_gb300 as K
     caps = [0, 1, 16, 17, 64, 65, 127, 128, 129, 509, 520, 2048, 2112, 2600, 4096, 8192, 32768]
