@@ -406,6 +406,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
                          workspace=ws, out=out_)
         hout_all.copy_(dout_all, non_blocking=True)
 
+    # (1) eager: the binding's calls issued from Python every step
     with torch.cuda.stream(stream):
         for _ in range(3):
             e2e_step()
@@ -417,13 +418,25 @@ def gpu_arm(args, rank, world, local_rank, dist):
             e2e_step()
         s1.record(stream)
     s1.synchronize()
-    te = max_over_ranks(dist, s0.elapsed_time(s1) / 1e3, dev)
+    te_eager = max_over_ranks(dist, s0.elapsed_time(s1) / 1e3, dev)
+    # (2) the same step (copies in, calls, copy out) captured once from the
+    # binding and replayed every step, as a decode engine runs it
+    ge = capture(torch, e2e_step, stream)
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            ge.replay()
+    torch.cuda.synchronize()
+    te = max_over_ranks(dist, time_graph(torch, ge, e2e_steps, stream), dev)
     e2e = dict(value=e2e_steps * L * world * bytes_call / te / 1e9, unit="GB/s",
                h2d_bytes_per_step=L * (b["q"] + b["idx"]), d2h_bytes_per_step=L * b["out"],
                us_per_call=te / (e2e_steps * L) * 1e6, steps=e2e_steps,
+               eager_us_per_call=te_eager / (e2e_steps * L) * 1e6,
+               eager_value=e2e_steps * L * world * bytes_call / te_eager / 1e9,
                note="per step: one pinned-host copy of all layers' query rows and one of their "
                     "lists, the dsa_decode call of the Python binding per layer, one copy of "
-                    "all outputs back")
+                    "all outputs back; the step is captured once as a CUDA graph (copies "
+                    "included) and replayed; eager_* issue the same step from Python every "
+                    "time (host-bound by the binding's per-call overhead)")
 
     out = {
         "metric": "INT8 split-KV decode us/call and achieved HBM GB/s (% of GB300 peak)",
