@@ -9,7 +9,9 @@
 // (one or two; half the threads idle at D = 64) and issues the loads of all its
 // splits at once, so the whole merge costs one L2 round trip.  Each warp reads
 // the (m, l) of all splits (lane k holds split k) and reduces M and L with
-// shuffles.  Splits with m = -inf are skipped without reading their accumulator.
+// shuffles.  The accumulator of a split with m = -inf (an empty split, never
+// written) is loaded with the others but selected away, never multiplied.
+// The head's sink logit is loaded together with the partials.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -33,6 +35,9 @@ combine_kernel(const float* __restrict__ acc, const float* __restrict__ m,
   const long long ml0 = (long long)u * ns * G + j;  // split k at ml0 + k*G
   const int c0 = threadIdx.x * V;                    // first channel of this thread
   const bool has = c0 < D;
+  const int h = (u % Hkv) * G + j;                   // query head within the row
+  // the sink logit travels with the partials' loads (one round trip in all)
+  const float sink_h = sink != nullptr ? sink[h] : 0.f;
 
   // all loads first: (m, l) of every split, and this thread's accumulator
   // channels of every split (up to 32)
@@ -74,12 +79,11 @@ combine_kernel(const float* __restrict__ acc, const float* __restrict__ m,
     }
   }
   if (!has) return;
-  const int h = (u % Hkv) * G + j;
   float lse_v = neg_inf(), scale = 0.f;
   if (L > 0.f) {
     lse_v = M + logf(L);
     scale = 1.f / L;
-    if (sink != nullptr) scale *= 1.f / (1.f + expf(sink[h] - lse_v));
+    if (sink != nullptr) scale *= 1.f / (1.f + expf(sink_h - lse_v));
   }
   __half* dst = out + (long long)wid * D + c0;
   if constexpr (V == 2) {
