@@ -205,6 +205,7 @@ i8kv_status dsa_common(const uint16_t* q, const int8_t* k, const int8_t* v, cons
   p.sigma = sigma;
   p.softcap = 0.f;
   p.window = -1;
+  p.lpt = 0;
   return I8KV_OK;
 }
 
@@ -432,6 +433,9 @@ i8kv_status paged_common(const uint16_t* q, const void* k_cache, const void* v_c
   p.sigma = softmax_scale;
   p.softcap = softcap;
   p.window = window;
+  // longest-first dispatch: ragged batches of long chunks (a property of the
+  // geometry, so eager and captured launches make the same choice)
+  p.lpt = B <= i8kv::kLptMaxRows && chunk >= i8kv::kLptMinChunk;
   return run(key, p, static_cast<cudaStream_t>(stream));
 }
 

@@ -135,15 +135,15 @@ constexpr float kTailDepth = 20.f;           // nats below the running maximum
 constexpr float kMaxValueScale = 65536.f;    // |value_scale| above which the tail matters
 
 template <int D, bool PAGED, bool FP16C, bool FP8, int kThreads>
-__device__ __noinline__ void attend_fp32(const DecodeParams p, float* q32, const float* svs) {
+__device__ __noinline__ void attend_fp32(const DecodeParams p, float* q32, const float* svs,
+                                         int unit, int split) {
   constexpr int kWarps = kThreads / 32;
   constexpr int C = D / 32;  // channels per lane
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int G = p.G;
-  // the CTA's unit and split, and its range of positions [lo, hi) (the same
-  // rules as the tensor-core body: the capacity, the clamped live length, the
-  // window start wlo and the chunks counted from it rounded down to 16)
-  const int unit = blockIdx.x, split = blockIdx.y;
+  // the CTA's range of positions [lo, hi) (the same rules as the tensor-core
+  // body: the capacity, the clamped live length, the window start wlo and the
+  // chunks counted from it rounded down to 16)
   const int row = unit / p.Hkv, g = unit - row * p.Hkv;
   const int cap = PAGED ? p.max_blocks * p.bs : p.max_sel;
   int len = cap, wlo = 0;
@@ -263,6 +263,84 @@ __device__ __noinline__ void attend_fp32(const DecodeParams p, float* q32, const
   }
 }
 
+// ---------------------------------------------------------------------------
+// Longest-first dispatch (paged decode).  CTAs start in the order of their
+// linear index, and a ragged batch otherwise leaves SMs idle at the end while
+// the last long splits finish.  The CTA at dispatch position pos takes the
+// item (unit, split) of rank pos in this order: the full chunks (split-major),
+// then the partial chunks by size in quarters of a chunk (largest quarter
+// first; row order within a quarter), then the empty ones (split-major).  A
+// batch whose rows all have the same live length keeps the natural order,
+// which is then already longest-first.  The geometry (num_splits, chunk) is
+// untouched; only which CTA computes which split changes, so the results are
+// the same bit for bit.
+// Batches of up to 32 rows: lane r of every warp holds row r, and each warp
+// ranks on its own with ballots and shuffles (no shared memory, no barrier).
+// The host enables it (DecodeParams::lpt) for chunks of at least 1024 tokens:
+// a CTA whose item changes loads its prologue twice, which only long CTAs
+// repay (measured: -11 % on ragged 2048-token chunks, +4 to +8 % on 272- and
+// 288-token chunks).
+// ---------------------------------------------------------------------------
+
+// lane of the n-th (from 0) set bit of mask
+__device__ __forceinline__ int nth_set_lane(unsigned mask, int n) {
+  for (int i = 0; i < n; ++i) mask &= mask - 1u;
+  return __ffs(mask) - 1;
+}
+
+static __device__ __noinline__ int2 lpt_item(const DecodeParams p, int pos) {
+  const int lane = threadIdx.x & 31;
+  const int B = p.rows, Hkv = p.Hkv, ns = p.num_splits, chunk = p.chunk;
+  const int cap = p.max_blocks * p.bs;
+  // row `lane`: nf full chunks, then a partial one of rem tokens (0: none)
+  int nf = 0, rem = 0, eff = 0;
+  const bool has = lane < B;
+  if (has) {
+    const int live = min(max(p.seq_lens[lane], 0), cap);
+    const int base = p.window >= 0 ? (max(0, live - 1 - p.window) & ~15) : 0;
+    eff = live - base;
+    nf = min(ns, eff / chunk);
+    rem = nf < ns ? eff - nf * chunk : 0;
+  }
+  // (every lane takes part in every shuffle and vote below: none sits inside a
+  // condition that differs between lanes)
+  const int eff0 = __shfl_sync(0xffffffffu, eff, 0);
+  if (__all_sync(0xffffffffu, !has || eff == eff0))
+    return make_int2(blockIdx.x, blockIdx.y);  // uniform batch: already longest-first
+  const int e = nf + (rem > 0 ? 1 : 0);        // first empty split of the row
+  const int quarter = (4 * rem) / chunk;       // 0..3 for a partial chunk
+  int cum = 0;
+  for (int s = 0; s < ns; ++s) {  // full chunks, split-major
+    const unsigned m = __ballot_sync(0xffffffffu, has && nf > s);
+    const int a = Hkv * __popc(m);
+    if (pos < cum + a) {
+      const int j = pos - cum;
+      return make_int2(nth_set_lane(m, j / Hkv) * Hkv + j % Hkv, s);
+    }
+    cum += a;
+  }
+  for (int qt = 3; qt >= 0; --qt) {  // partial chunks, largest quarter first
+    const unsigned m = __ballot_sync(0xffffffffu, has && rem > 0 && quarter == qt);
+    const int a = Hkv * __popc(m);
+    if (pos < cum + a) {
+      const int j = pos - cum;
+      const int r = nth_set_lane(m, j / Hkv);
+      return make_int2(r * Hkv + j % Hkv, __shfl_sync(0xffffffffu, nf, r));
+    }
+    cum += a;
+  }
+  for (int s = 0; s < ns; ++s) {  // empty chunks, split-major
+    const unsigned m = __ballot_sync(0xffffffffu, has && e <= s);
+    const int c = Hkv * __popc(m);
+    if (pos < cum + c) {
+      const int j = pos - cum;
+      return make_int2(nth_set_lane(m, j / Hkv) * Hkv + j % Hkv, s);
+    }
+    cum += c;
+  }
+  return make_int2(blockIdx.x, blockIdx.y);  // not reached: the ranks cover the grid
+}
+
 template <int D, int NT, bool PAGED, bool FP16C, bool PLO, bool FP8>
 __global__ void __launch_bounds__((Tile<D, NT, FP16C, PAGED>::kThreads),
                                   (Tile<D, NT, FP16C, PAGED>::kMinBlocks))
@@ -278,74 +356,136 @@ decode_kernel(const DecodeParams p) {
   const int warp = threadIdx.x >> 5;
   const int grp = lane >> 2;
   const int tig = lane & 3;
-  const int unit = blockIdx.x;
-  const int split = blockIdx.y;
-  const int row = unit / p.Hkv;
-  const int g = unit - row * p.Hkv;
   const int G = p.G;
+  const int cap = PAGED ? p.max_blocks * p.bs : p.max_sel;
+  // block of a 16-aligned position and the row offset of that position in its
+  // block (block_size is a multiple of 16; a shift when it is a power of two)
+  const int bs_shift = p.bs_log2;
+  auto block_of = [&](int pos) -> int { return bs_shift >= 0 ? pos >> bs_shift : pos / p.bs; };
+  auto offset_in_block = [&](int pos) -> int {
+    return bs_shift >= 0 ? pos & (p.bs - 1) : pos % p.bs;
+  };
   grid_dependency_wait();  // inputs may come from the previous kernel of the stream
 
-  // Query rows of the group and their key scales, 8 channels per thread and
-  // step, loaded first so that their latency overlaps the length and gather-key
-  // loads below.
+  // ---------------- the CTA's item (unit, split) and what depends on it ----------------
+  // Loaded by `setup`: the query rows of the group and their key scales (8
+  // channels per thread and step), the value scales of the KV head, the
+  // length, the candidate range of the split and the first gather keys, all
+  // issued together so that their latencies overlap.  A paged CTA then ranks
+  // the batch for the longest-first dispatch (its loads overlap the ones
+  // above) and loads again only if that gives it another item.
   constexpr int kQSteps = (NT * D + kThreads - 1) / kThreads;
-  uint4 q_raw[kQSteps];
-  float4 ks_raw[kQSteps][2];
-  {
-    const __half* qrow = reinterpret_cast<const __half*>(p.q) + ((long long)row * p.Hq + g * G) * D;
+  constexpr int kVsPer = (D + kThreads - 1) / kThreads;
+  struct Item {
+    int unit, split, row, g, len, wlo, base, lo, nhi;
+    uint4 q_raw[kQSteps];
+    float4 ks_raw[kQSteps][2];
+    float vs_raw[kVsPer];
+    int pf[T::kStages + 1];
+  };
+  // The gather key of step k of this warp in [lo_, end) of row row_ (-1 past
+  // the end): the list entry of position (lane % kStep) of the step (sparse),
+  // or the block id of 16-token tile (lane % SUB) of the step (paged; block_size
+  // is a multiple of 16).  Warp w takes the steps w, w + kWarps, ...
+  auto key_of = [&](int row_, int lo_, int end, int k) -> int {
+    const int n = end > lo_ ? (end - lo_ + T::kStep - 1) / T::kStep : 0;
+    const int nw = n > warp ? (n - warp + kWarps - 1) / kWarps : 0;
+    if (k >= nw) return -1;
+    const int pos0 = lo_ + T::kStep * (warp + kWarps * k);
+    if constexpr (PAGED) {
+      const int pos = pos0 + kSub * (lane % SUB);
+      return pos < end ? __ldg(p.block_table + (long long)row_ * p.max_blocks + block_of(pos)) : -1;
+    } else {
+      const int pos = pos0 + (lane % T::kStep);
+      return pos < end ? __ldg(p.idx + (long long)row_ * p.max_sel + pos) : -1;
+    }
+  };
+  auto setup = [&](int unit_, int split_, Item& it) {
+    it.unit = unit_;
+    it.split = split_;
+    it.row = unit_ / p.Hkv;
+    it.g = unit_ - it.row * p.Hkv;
+    const __half* qrow =
+        reinterpret_cast<const __half*>(p.q) + ((long long)it.row * p.Hq + it.g * G) * D;
 #pragma unroll
     for (int i = 0; i < kQSteps; ++i) {
       const int e = threadIdx.x + i * kThreads;
       const int h = (e * 8) / D, d0 = (e * 8) % D;
-      q_raw[i] = make_uint4(0u, 0u, 0u, 0u);
-      ks_raw[i][0] = ks_raw[i][1] = make_float4(1.f, 1.f, 1.f, 1.f);
+      it.q_raw[i] = make_uint4(0u, 0u, 0u, 0u);
+      it.ks_raw[i][0] = it.ks_raw[i][1] = make_float4(1.f, 1.f, 1.f, 1.f);
       if (e < NT * D && h < G) {
-        q_raw[i] = *reinterpret_cast<const uint4*>(qrow + h * D + d0);
+        it.q_raw[i] = *reinterpret_cast<const uint4*>(qrow + h * D + d0);
         if constexpr (!FP16C) {
           if (p.per_channel) {
-            ks_raw[i][0] = *reinterpret_cast<const float4*>(p.k_scale + g * D + d0);
-            ks_raw[i][1] = *reinterpret_cast<const float4*>(p.k_scale + g * D + d0 + 4);
+            it.ks_raw[i][0] = *reinterpret_cast<const float4*>(p.k_scale + it.g * D + d0);
+            it.ks_raw[i][1] = *reinterpret_cast<const float4*>(p.k_scale + it.g * D + d0 + 4);
           } else {
             const float k0 = p.k_scale[0];
-            ks_raw[i][0] = ks_raw[i][1] = make_float4(k0, k0, k0, k0);
+            it.ks_raw[i][0] = it.ks_raw[i][1] = make_float4(k0, k0, k0, k0);
           }
         }
       }
     }
+#pragma unroll
+    for (int i = 0; i < kVsPer; ++i) {
+      const int d = threadIdx.x + i * kThreads;
+      it.vs_raw[i] = 1.f;
+      if constexpr (!FP16C) {
+        if (d < D) it.vs_raw[i] = p.per_channel ? p.v_scale[it.g * D + d] : p.v_scale[0];
+      }
+    }
+    // candidate range (positions fit 32 bits: the host checks cap + num_splits
+    // * chunk <= INT32_MAX).  Sliding window (paged only): the query at
+    // position len - 1 attends [wlo, len) with wlo = len - 1 - window; the
+    // splits count their chunks from wlo rounded down to the 16-token tile
+    // granule, so this one case waits for the length before the gather keys.
+    it.len = 0;
+    if constexpr (PAGED) it.len = p.seq_lens[it.row];  // in flight while the keys are fetched
+    it.wlo = 0;
+    it.base = 0;
+    if constexpr (PAGED) {
+      if (p.window >= 0) {
+        const int live = min(max(it.len, 0), cap);
+        it.wlo = max(0, live - 1 - p.window);
+        it.base = it.wlo & ~15;
+      }
+    }
+    it.lo = it.base + split_ * p.chunk;
+    it.nhi = min(it.lo + p.chunk, cap);  // nominal end (capacity-bounded)
+    // the first keys, fetched against the nominal end before the live length
+    // of a paged sequence is known
+#pragma unroll
+    for (int k = 0; k <= T::kStages; ++k) it.pf[k] = key_of(it.row, it.lo, it.nhi, k);
+  };
+  Item it;
+  setup(blockIdx.x, blockIdx.y, it);
+  if constexpr (PAGED) {
+    if (p.lpt) {
+      const int2 x = lpt_item(p, blockIdx.y * gridDim.x + blockIdx.x);
+      if (x.x != it.unit || x.y != it.split) setup(x.x, x.y, it);  // uniform over the CTA
+    }
   }
+  const int unit = it.unit, split = it.split, row = it.row, g = it.g;
+  int len = it.len;
+  const int wlo = it.wlo, lo = it.lo, nhi = it.nhi;
+  uint4(&q_raw)[kQSteps] = it.q_raw;
+  float4(&ks_raw)[kQSteps][2] = it.ks_raw;
+  int(&pf)[T::kStages + 1] = it.pf;
 
   // value scales of this KV head, staged in shared memory for the epilogue
   float* svs = reinterpret_cast<float*>(smem + T::kVsOffset);
   bool vs_bad = false;  // a value scale is not finite
   if constexpr (!FP16C) {
-    for (int d = threadIdx.x; d < D; d += kThreads) {
-      const float v = p.per_channel ? p.v_scale[g * D + d] : p.v_scale[0];
-      svs[d] = v;
-      vs_bad |= !(fabsf(v) <= 3.4028235e38f);
+#pragma unroll
+    for (int i = 0; i < kVsPer; ++i) {
+      const int d = threadIdx.x + i * kThreads;
+      if (d < D) {
+        svs[d] = it.vs_raw[i];
+        vs_bad |= !(fabsf(it.vs_raw[i]) <= 3.4028235e38f);
+      }
     }
   }
   constexpr int MT_ITERS = (KC + kWarps - 1) / kWarps;
-
-  // ---------------- candidate range of this split ----------------
-  // (positions fit 32 bits: the host checks cap + num_splits * chunk <= INT32_MAX)
-  const int cap = PAGED ? p.max_blocks * p.bs : p.max_sel;
-  int len = 0;
-  if constexpr (PAGED) len = p.seq_lens[row];  // in flight while the keys are fetched
-  // Sliding window (paged only): the query at position len - 1 attends
-  // [wlo, len) with wlo = len - 1 - window; the splits then count their chunks
-  // from wlo rounded down to the 16-token tile granule, so this one case waits
-  // for the length before the first gather keys.
-  int wlo = 0, base = 0;
-  if constexpr (PAGED) {
-    if (p.window >= 0) {
-      const int live = min(max(len, 0), cap);
-      wlo = max(0, live - 1 - p.window);
-      base = wlo & ~15;
-    }
-  }
-  const int lo = base + split * p.chunk;
-  // nominal end of the split (capacity-bounded); the live end follows below
-  const int nhi = min(lo + p.chunk, cap);
 
   // ---------------- per-warp gather pipeline ----------------
   // Warp w takes the steps w, w + kWarps, ... of kStep consecutive positions.
@@ -360,40 +500,17 @@ decode_kernel(const DecodeParams p) {
   const long long lane_off = (long long)g * T::kRowBytes + chunk_id * 16;
 
   auto step_pos = [&](int k) -> int { return lo + T::kStep * (warp + kWarps * k); };
-  // block of a 16-aligned position and the row offset of that position in its
-  // block (block_size is a multiple of 16; a shift when it is a power of two)
-  const int bs_shift = p.bs_log2;
-  auto block_of = [&](int pos) -> int { return bs_shift >= 0 ? pos >> bs_shift : pos / p.bs; };
-  auto offset_in_block = [&](int pos) -> int {
-    return bs_shift >= 0 ? pos & (p.bs - 1) : pos % p.bs;
-  };
   auto steps_below = [&](int end) -> int {
     const int n = end > lo ? (end - lo + T::kStep - 1) / T::kStep : 0;
     return n > warp ? (n - warp + kWarps - 1) / kWarps : 0;
   };
-
-  // The per-step gather key, loaded ahead of the copies: the list entry of
-  // position (lane % kStep) of the step (sparse), or the block id of 16-token
-  // tile (lane % SUB) of the step (paged; block_size is a multiple of 16).
-  // The first keys are fetched against the nominal end, before the live length
-  // of a paged sequence is known.
+  // later keys: against the live end once it is known
   int fetch_hi = nhi;
   int fetch_n = steps_below(nhi);
   auto fetch = [&](int k) -> int {
     if (k >= fetch_n) return -1;
-    const int pos0 = step_pos(k);
-    if constexpr (PAGED) {
-      const int pos = pos0 + kSub * (lane % SUB);
-      return pos < fetch_hi ? __ldg(p.block_table + (long long)row * p.max_blocks + block_of(pos))
-                            : -1;
-    } else {
-      const int pos = pos0 + (lane % T::kStep);
-      return pos < fetch_hi ? __ldg(p.idx + (long long)row * p.max_sel + pos) : -1;
-    }
+    return key_of(row, lo, fetch_hi, k);
   };
-  int pf[T::kStages + 1];
-#pragma unroll
-  for (int k = 0; k <= T::kStages; ++k) pf[k] = fetch(k);
 
   // live end of the split
   int hi = nhi;
@@ -559,7 +676,8 @@ decode_kernel(const DecodeParams p) {
     cp_async_wait_all();
     __syncthreads();  // every warp's gathers have landed: the ring is free
     if (threadIdx.x == 0) flag_or(p.flags, I8KV_FLAG_FP32_PATH);
-    attend_fp32<D, PAGED, FP16C, FP8, kThreads>(p, reinterpret_cast<float*>(smem), svs);
+    attend_fp32<D, PAGED, FP16C, FP8, kThreads>(p, reinterpret_cast<float*>(smem), svs, unit,
+                                                split);
     return;
   }
   // B fragments of Q'^T (k = channel, n = head) in the contraction order of the
@@ -856,7 +974,8 @@ decode_kernel(const DecodeParams p) {
   // fp16 tile's range, so the CTA starts over on the FP32 path
   if (vs_big_cta && __syncthreads_or(deep)) {
     if (threadIdx.x == 0) flag_or(p.flags, I8KV_FLAG_FP32_PATH);
-    attend_fp32<D, PAGED, FP16C, FP8, kThreads>(p, reinterpret_cast<float*>(smem), svs);
+    attend_fp32<D, PAGED, FP16C, FP8, kThreads>(p, reinterpret_cast<float*>(smem), svs, unit,
+                                                split);
     return;
   }
 

@@ -129,7 +129,8 @@ __global__ void __launch_bounds__(256, 1) decode_tc_kernel(const DecodeParams p)
   using T = TcTile<D>;
   constexpr int BT = T::BT;
   constexpr int kThreads = T::kThreads;
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t tc_smem[];
+  uint8_t* const smem = tc_smem;
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -337,7 +338,8 @@ __global__ void __launch_bounds__(256, 1) decode_tc_kernel(const DecodeParams p)
     cp_async_wait_all();
     __syncthreads();
     if (tid == 0) flag_or(p.flags, I8KV_FLAG_FP32_PATH);
-    attend_fp32<D, PAGED, false, FP8, kThreads>(p, reinterpret_cast<float*>(smem), svs);
+    attend_fp32<D, PAGED, false, FP8, kThreads>(p, reinterpret_cast<float*>(smem), svs,
+                                                blockIdx.x, blockIdx.y);
     return;
   }
 
@@ -545,7 +547,8 @@ __global__ void __launch_bounds__(256, 1) decode_tc_kernel(const DecodeParams p)
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tbase, T::kCols);
     if (tid == 0) flag_or(p.flags, I8KV_FLAG_FP32_PATH);
-    attend_fp32<D, PAGED, false, FP8, kThreads>(p, reinterpret_cast<float*>(smem), svs);
+    attend_fp32<D, PAGED, false, FP8, kThreads>(p, reinterpret_cast<float*>(smem), svs,
+                                                blockIdx.x, blockIdx.y);
     return;
   }
 

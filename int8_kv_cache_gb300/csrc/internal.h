@@ -36,7 +36,13 @@ struct DecodeParams {
   float sigma;
   float softcap;             // paged: > 0 caps scores to softcap * tanh(s / softcap); 0 off
   int32_t window;            // paged: >= 0 attends [len - 1 - window, len); -1 off
+  int32_t lpt;               // paged: longest-first dispatch of the (unit, split) items
 };
+
+// Longest-first dispatch of the paged decode (decode_kernel.cuh, lpt_item):
+// batches of at most kLptMaxRows rows, chunks of at least kLptMinChunk tokens.
+constexpr int kLptMaxRows = 32;
+constexpr int kLptMinChunk = 1024;
 
 struct KernelKey {
   Path path;
