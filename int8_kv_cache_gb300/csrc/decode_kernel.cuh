@@ -14,6 +14,9 @@
 //     warps (as many 4-warp groups as the registers and shared memory allow);
 //     the paged kernel runs 4-warp CTAs, 2 to 4 per SM, so that the splits of
 //     sequences of very different lengths spread over the SMs.
+//   * Dispatch order (paged, long chunks).  A CTA may take another (unit,
+//     split) item than its grid position names, so that the longest chunks of
+//     a ragged batch start first (lpt_item below); the geometry is unchanged.
 //   * Warp-private pipelines.  Warp w owns the steps w, w + kWarps, ... of the
 //     split (a step is 16 tokens, or 32 when two tiles fit the registers).  It
 //     gathers each step's K and V rows with 16-byte cp.async copies into its
