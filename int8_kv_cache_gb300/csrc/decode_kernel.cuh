@@ -277,8 +277,9 @@ __device__ __noinline__ void attend_fp32(const DecodeParams p, float* q32, const
 // which is then already longest-first.  The geometry (num_splits, chunk) is
 // untouched; only which CTA computes which split changes, so the results are
 // the same bit for bit.
-// Batches of up to 32 rows: lane r of every warp holds row r, and each warp
-// ranks on its own with ballots and shuffles (no shared memory, no barrier).
+// Batches of up to 128 rows: lane l of every warp holds rows l, l + 32, ...,
+// and each warp ranks on its own with ballots and shuffles (no shared memory,
+// no barrier).
 // The host enables it (DecodeParams::lpt) for chunks of at least 1024 tokens:
 // a CTA whose item changes loads its prologue twice, which only long CTAs
 // repay (measured: -11 % on ragged 2048-token chunks, +4 to +8 % on 272- and
@@ -292,54 +293,97 @@ __device__ __forceinline__ int nth_set_lane(unsigned mask, int n) {
 }
 
 static __device__ __noinline__ int2 lpt_item(const DecodeParams p, int pos) {
+  constexpr int J = kLptMaxRows / 32;  // rows per lane: lane, lane + 32, ...
   const int lane = threadIdx.x & 31;
   const int B = p.rows, Hkv = p.Hkv, ns = p.num_splits, chunk = p.chunk;
   const int cap = p.max_blocks * p.bs;
-  // row `lane`: nf full chunks, then a partial one of rem tokens (0: none)
-  int nf = 0, rem = 0, eff = 0;
-  const bool has = lane < B;
-  if (has) {
-    const int live = min(max(p.seq_lens[lane], 0), cap);
-    const int base = p.window >= 0 ? (max(0, live - 1 - p.window) & ~15) : 0;
-    eff = live - base;
-    nf = min(ns, eff / chunk);
-    rem = nf < ns ? eff - nf * chunk : 0;
+  const int jn = (B + 31) / 32;  // row groups in use (uniform)
+  // row lane + 32 j: nf full chunks, then a partial one of rem tokens (0: none)
+  int nf[J], rem[J], eff[J];
+  bool has[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int r = lane + 32 * j;
+    has[j] = r < B;
+    nf[j] = rem[j] = eff[j] = 0;
+    if (has[j]) {
+      const int live = min(max(p.seq_lens[r], 0), cap);
+      const int base = p.window >= 0 ? (max(0, live - 1 - p.window) & ~15) : 0;
+      eff[j] = live - base;
+      nf[j] = min(ns, eff[j] / chunk);
+      rem[j] = nf[j] < ns ? eff[j] - nf[j] * chunk : 0;
+    }
   }
   // (every lane takes part in every shuffle and vote below: none sits inside a
   // condition that differs between lanes)
-  const int eff0 = __shfl_sync(0xffffffffu, eff, 0);
-  if (__all_sync(0xffffffffu, !has || eff == eff0))
+  const int eff0 = __shfl_sync(0xffffffffu, eff[0], 0);
+  bool same = true;
+#pragma unroll
+  for (int j = 0; j < J; ++j) same &= !has[j] || eff[j] == eff0;
+  if (__all_sync(0xffffffffu, same))
     return make_int2(blockIdx.x, blockIdx.y);  // uniform batch: already longest-first
-  const int e = nf + (rem > 0 ? 1 : 0);        // first empty split of the row
-  const int quarter = (4 * rem) / chunk;       // 0..3 for a partial chunk
+  // the rank-th row (ascending) among those whose bit is set in m[j]
+  auto nth_row = [&](const unsigned (&m)[J], int rank) -> int {
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int c = __popc(m[j]);
+      if (rank < c) return 32 * j + nth_set_lane(m[j], rank);
+      rank -= c;
+    }
+    return -1;  // not reached
+  };
   int cum = 0;
   for (int s = 0; s < ns; ++s) {  // full chunks, split-major
-    const unsigned m = __ballot_sync(0xffffffffu, has && nf > s);
-    const int a = Hkv * __popc(m);
-    if (pos < cum + a) {
-      const int j = pos - cum;
-      return make_int2(nth_set_lane(m, j / Hkv) * Hkv + j % Hkv, s);
+    unsigned m[J];
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      m[j] = j < jn ? __ballot_sync(0xffffffffu, has[j] && nf[j] > s) : 0u;
+      c += __popc(m[j]);
     }
-    cum += a;
+    if (pos < cum + Hkv * c) {
+      const int q = pos - cum;
+      return make_int2(nth_row(m, q / Hkv) * Hkv + q % Hkv, s);
+    }
+    cum += Hkv * c;
   }
   for (int qt = 3; qt >= 0; --qt) {  // partial chunks, largest quarter first
-    const unsigned m = __ballot_sync(0xffffffffu, has && rem > 0 && quarter == qt);
-    const int a = Hkv * __popc(m);
-    if (pos < cum + a) {
-      const int j = pos - cum;
-      const int r = nth_set_lane(m, j / Hkv);
-      return make_int2(r * Hkv + j % Hkv, __shfl_sync(0xffffffffu, nf, r));
+    unsigned m[J];
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      m[j] = j < jn ? __ballot_sync(0xffffffffu, has[j] && rem[j] > 0 &&
+                                                     (4 * rem[j]) / chunk == qt)
+                    : 0u;
+      c += __popc(m[j]);
     }
-    cum += a;
+    if (pos < cum + Hkv * c) {
+      const int q = pos - cum;
+      const int r = nth_row(m, q / Hkv);
+      int nfr = 0;  // nf of row r, from the lane that holds it
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const int v = __shfl_sync(0xffffffffu, nf[j], r & 31);
+        if (j == r / 32) nfr = v;
+      }
+      return make_int2(r * Hkv + q % Hkv, nfr);
+    }
+    cum += Hkv * c;
   }
   for (int s = 0; s < ns; ++s) {  // empty chunks, split-major
-    const unsigned m = __ballot_sync(0xffffffffu, has && e <= s);
-    const int c = Hkv * __popc(m);
-    if (pos < cum + c) {
-      const int j = pos - cum;
-      return make_int2(nth_set_lane(m, j / Hkv) * Hkv + j % Hkv, s);
+    unsigned m[J];
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int e = nf[j] + (rem[j] > 0 ? 1 : 0);  // first empty split of the row
+      m[j] = j < jn ? __ballot_sync(0xffffffffu, has[j] && e <= s) : 0u;
+      c += __popc(m[j]);
     }
-    cum += c;
+    if (pos < cum + Hkv * c) {
+      const int q = pos - cum;
+      return make_int2(nth_row(m, q / Hkv) * Hkv + q % Hkv, s);
+    }
+    cum += Hkv * c;
   }
   return make_int2(blockIdx.x, blockIdx.y);  // not reached: the ranks cover the grid
 }

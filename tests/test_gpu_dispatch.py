@@ -1,6 +1,6 @@
 """Longest-first dispatch of the paged decode, against the FP64 oracle.
 
-Paged calls whose chunks hold at least 1024 tokens (batches of up to 32 rows)
+Paged calls whose chunks hold at least 1024 tokens (batches of up to 128 rows)
 hand the (unit, split) items to the CTAs longest chunk first instead of in
 split-major order.  Only which CTA computes which split changes, so every
 output, lse and split partial must still be the oracle's.  The lengths put
@@ -93,9 +93,10 @@ def test_window_with_long_chunks():
     _check_partials(c, 2, window=1500)
 
 
-@pytest.mark.parametrize("B", [32, 33])
-def test_batch_of_32_rows_and_one_more(B):
-    # 32 rows: the dispatch ranks the batch; 33 rows: split-major order
+@pytest.mark.parametrize("B", [32, 33, 100, 128, 129])
+def test_batches_up_to_128_rows_and_one_more(B):
+    # up to 128 rows (one to four rows per lane): the dispatch ranks the
+    # batch; 129 rows: split-major order
     lens = W.make_rng(33).integers(0, 4600, size=B)
     c = _case(lens, seed=34, Hq=8, Hkv=1)
     o, lse = run_paged(c, num_splits=4, chunk=CHUNK)
