@@ -94,14 +94,18 @@ struct Tile {
   static constexpr int kMaskBytes = kWarps * 4 * 4;
   static constexpr int kRingBytes = kWarps * kWarpRing;
   static constexpr int kLoopBytes = kRingBytes + kMaskBytes + kQBytes;
-  // end-of-CTA merge: every thread's accumulator fragment (E floats, padded by
-  // 4 for conflict-free 16-byte access) plus m, l of the warps x 16 heads
+  // end-of-CTA merge: each warp leaves its lanes' accumulator fragments (E
+  // floats each, padded by 4 for conflict-free 16-byte access) in its own ring,
+  // which is free once the warp's copies have landed
   static constexpr int kE = (D / 16) * NT * 4;
-  static constexpr int kMergeBytes = (kThreads * (kE + 4) + 3 * kWarps * 16 + 32) * 4;
+  static constexpr int kFragBytes = 32 * (kE + 4) * 4;
   // value scales of the group's KV head, staged with the query and read by the
-  // epilogue (after both the ring and the merge area)
-  static constexpr int kVsOffset = kLoopBytes > kMergeBytes ? kLoopBytes : kMergeBytes;
-  static constexpr int kSmem = kVsOffset + D * 4;
+  // epilogue, then the merge scalars: m, l and weights of the warps x 16 heads,
+  // and M, L of the 16 heads
+  static constexpr int kVsOffset = kLoopBytes;
+  static constexpr int kScalOffset = kVsOffset + D * 4;
+  static constexpr int kSmem = kScalOffset + (3 * kWarps * 16 + 32) * 4;
+  static_assert(kFragBytes <= kWarpRing, "a warp's fragments fit its ring");
   static_assert(kChunks <= 32 && 32 % kChunks == 0, "row layout");
   static_assert(kCopies >= 1, "copy layout");
   static_assert(kGroups >= 1 && kThreads <= 1024, "CTA shape");
@@ -1026,11 +1030,12 @@ decode_kernel(const DecodeParams p) {
     return;
   }
 
-  // ---------------- merge the four warps' partials ----------------
-  // (m, l) per head of every warp; l is first summed over the 8 lanes that
-  // share a head pair.
-  float* mw = reinterpret_cast<float*>(smem + kThreads * (T::kE + 4) * 4);  // [warps][16]
-  float* lw = mw + kWarps * 16;                                           // [warps][16]
+  // ---------------- merge the warps' partials ----------------
+  // Each warp publishes its (m, l) per head (l first summed over the 8 lanes
+  // that share a head pair) and its fragments as soon as its loop is done,
+  // without waiting for the others; one barrier then makes them all visible.
+  float* mw = reinterpret_cast<float*>(smem + T::kScalOffset);  // [warps][16]
+  float* lw = mw + kWarps * 16;                                 // [warps][16]
   float lsum[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -1042,7 +1047,6 @@ decode_kernel(const DecodeParams p) {
       l += __shfl_xor_sync(0xffffffffu, l, 16);
       lsum[nt][j] = l;
     }
-  __syncthreads();  // every warp is done with its ring: reuse the memory
   if (grp == 0) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -1052,10 +1056,12 @@ decode_kernel(const DecodeParams p) {
         lw[warp * 16 + nt * 8 + 2 * tig + j] = lsum[nt][j];
       }
   }
-  // each thread's fragment, thread-major: [thread][E (+4 pad)]
-  float* frag = reinterpret_cast<float*>(smem);
+  // each lane's fragment in its warp's ring: [lane][E (+4 pad)]
+  auto frag_of = [&](int w) -> float* {
+    return reinterpret_cast<float*>(smem + w * T::kWarpRing);
+  };
   {
-    float4* mine = reinterpret_cast<float4*>(frag + threadIdx.x * (T::kE + 4));
+    float4* mine = reinterpret_cast<float4*>(frag_of(warp) + lane * (T::kE + 4));
 #pragma unroll
     for (int mt = 0; mt < KC; ++mt)
 #pragma unroll
@@ -1111,7 +1117,7 @@ decode_kernel(const DecodeParams p) {
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
         const float4 v = reinterpret_cast<const float4*>(
-            frag + (w * 32 + lane) * (T::kE + 4))[mt * NT + nt];
+            frag_of(w) + lane * (T::kE + 4))[mt * NT + nt];
         const float f0 = fws[w * 16 + nt * 8 + 2 * tig], f1 = fws[w * 16 + nt * 8 + 2 * tig + 1];
         a.x += f0 * v.x;  // (head 2tig,   channel da)
         a.y += f1 * v.y;  // (head 2tig+1, channel da)
