@@ -100,11 +100,10 @@ struct Tile {
   static constexpr int kE = (D / 16) * NT * 4;
   static constexpr int kFragBytes = 32 * (kE + 4) * 4;
   // value scales of the group's KV head, staged with the query and read by the
-  // epilogue, then the merge scalars: m, l and weights of the warps x 16 heads,
-  // and M, L of the 16 heads
+  // epilogue, then the merge scalars: m and l of the warps x 16 heads
   static constexpr int kVsOffset = kLoopBytes;
   static constexpr int kScalOffset = kVsOffset + D * 4;
-  static constexpr int kSmem = kScalOffset + (3 * kWarps * 16 + 32) * 4;
+  static constexpr int kSmem = kScalOffset + 2 * kWarps * 16 * 4;
   static_assert(kFragBytes <= kWarpRing, "a warp's fragments fit its ring");
   static_assert(kChunks <= 32 && 32 % kChunks == 0, "row layout");
   static_assert(kCopies >= 1, "copy layout");
@@ -1072,25 +1071,28 @@ decode_kernel(const DecodeParams p) {
   __syncthreads();
 
   // Warp w finishes m-tiles w, w + kWarps, ... of the fragment of its lane
-  // index: weights f_w' = exp(m_w' - M) per head, then sum over the warps.
-  // per-head merge weights f[w][h] = exp(m_w - M), M and L, computed once
-  float* fws = lw + kWarps * 16;  // [warps][16]
-  float* Ms = fws + kWarps * 16;  // [16]
-  float* Ls = Ms + 16;            // [16]
-  if (threadIdx.x < 16) {
-    const int h = threadIdx.x;
-    float M = neg_inf();
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * 16 + h]);
-    float L = 0.f;
-    for (int w = 0; w < kWarps; ++w) {
-      const float f = M == neg_inf() ? 0.f : fast_exp2((mw[w * 16 + h] - M) * kLog2e);
-      fws[w * 16 + h] = f;
-      L += f * lw[w * 16 + h];
+  // index.  Each thread forms the merge weights f_w = exp(m_w - M) of its own
+  // heads (2 tig, 2 tig + 1 of each n-tile), with M and L, from the published
+  // scalars: no second barrier.
+  float fw[NT][2][kWarps], Mh[NT][2], Lh[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int h = nt * 8 + 2 * tig + j;
+      float M = neg_inf();
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * 16 + h]);
+      float L = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float f = M == neg_inf() ? 0.f : fast_exp2((mw[w * 16 + h] - M) * kLog2e);
+        fw[nt][j][w] = f;
+        L += f * lw[w * 16 + h];
+      }
+      Mh[nt][j] = M;
+      Lh[nt][j] = L;
     }
-    Ms[h] = M;
-    Ls[h] = L;
-  }
-  __syncthreads();
 
   const bool direct = p.num_splits == 1;
   const long long head0 = (long long)row * p.Hq + g * G;
@@ -1118,7 +1120,7 @@ decode_kernel(const DecodeParams p) {
       for (int w = 0; w < kWarps; ++w) {
         const float4 v = reinterpret_cast<const float4*>(
             frag_of(w) + lane * (T::kE + 4))[mt * NT + nt];
-        const float f0 = fws[w * 16 + nt * 8 + 2 * tig], f1 = fws[w * 16 + nt * 8 + 2 * tig + 1];
+        const float f0 = fw[nt][0][w], f1 = fw[nt][1][w];
         a.x += f0 * v.x;  // (head 2tig,   channel da)
         a.y += f1 * v.y;  // (head 2tig+1, channel da)
         a.z += f0 * v.z;  // (head 2tig,   channel db)
@@ -1130,7 +1132,7 @@ decode_kernel(const DecodeParams p) {
         if (h >= G) continue;
         const float va = j == 0 ? a.x : a.y;
         const float vb = j == 0 ? a.z : a.w;
-        const float M = Ms[h], L = Ls[h];
+        const float M = Mh[nt][j], L = Lh[nt][j];
         if (direct) {
           float oa = 0.f, ob = 0.f;
           if (L > 0.f) {
@@ -1168,7 +1170,7 @@ decode_kernel(const DecodeParams p) {
       for (int j = 0; j < 2; ++j) {
         const int h = nt * 8 + 2 * tig + j;
         if (h >= G) continue;
-        const float M = Ms[h], L = Ls[h];
+        const float M = Mh[nt][j], L = Lh[nt][j];
         if (direct) {
           if (p.lse != nullptr) p.lse[head0 + h] = L > 0.f ? M + logf(L) : neg_inf();
         } else {
