@@ -76,7 +76,7 @@ def _check_partials(c, ns, window=-1):
                         "normalised partial")
 
 
-@pytest.mark.parametrize("cache", ["int8", "fp8"])
+@pytest.mark.parametrize("cache", ["int8", "fp8", "fp16"])
 def test_ragged_rows_every_item_class(cache):
     c = _case(LENS, cache=cache)
     o, lse = run_paged(c, num_splits=4, chunk=CHUNK)
