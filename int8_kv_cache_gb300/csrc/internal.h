@@ -54,13 +54,9 @@ struct KernelKey {
   bool tc;         // served by the tcgen05 (tensor-memory) decode kernel
 };
 
-// Launch one decode / prefill kernel: grid (rows * Hkv, num_splits).
-cudaError_t launch_decode(const KernelKey& key, const DecodeParams& p, cudaStream_t stream);
-
-// Resident CTAs per SM of that kernel (occupancy API), or -1 if no such kernel.
-int decode_occupancy(const KernelKey& key);
-
-// Per-path launchers (one per translation unit).
+// Per-path launchers (one per translation unit): grid (rows * Hkv, num_splits);
+// with occupancy != NULL nothing is launched and the resident CTAs per SM of
+// the selected kernel are returned there instead.
 cudaError_t launch_dsa_decode(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
                               int* occupancy);
 cudaError_t launch_dsa_prefill(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
