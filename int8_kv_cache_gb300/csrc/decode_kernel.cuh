@@ -508,11 +508,21 @@ decode_kernel(const DecodeParams p) {
     for (int k = 0; k <= T::kStages; ++k) it.pf[k] = key_of(it.row, it.lo, it.nhi, k);
   };
   Item it;
-  setup(blockIdx.x, blockIdx.y, it);
-  if constexpr (PAGED) {
-    if (p.lpt) {
-      const int2 x = lpt_item(p, blockIdx.y * gridDim.x + blockIdx.x);
-      if (x.x != it.unit || x.y != it.split) setup(x.x, x.y, it);  // uniform over the CTA
+  {
+    // one call site: the natural item, then (paged, rarely) the dispatched one
+    int u = blockIdx.x, sp = blockIdx.y;
+#pragma unroll 1
+    for (int pass = 0;; ++pass) {
+      setup(u, sp, it);
+      if constexpr (!PAGED) {
+        break;
+      } else {
+        if (!p.lpt || pass > 0) break;
+        const int2 x = lpt_item(p, blockIdx.y * gridDim.x + blockIdx.x);
+        if (x.x == u && x.y == sp) break;  // uniform over the CTA
+        u = x.x;
+        sp = x.y;
+      }
     }
   }
   const int unit = it.unit, split = it.split, row = it.row, g = it.g;
