@@ -283,10 +283,11 @@ __device__ __noinline__ void attend_fp32(const DecodeParams p, float* q32, const
 // Batches of up to 128 rows: lane l of every warp holds rows l, l + 32, ...,
 // and each warp ranks on its own with ballots and shuffles (no shared memory,
 // no barrier).
-// The host enables it (DecodeParams::lpt) for chunks of at least 1024 tokens:
+// The host enables it (DecodeParams::lpt) for chunks of at least 1280 tokens:
 // a CTA whose item changes loads its prologue twice, which only long CTAs
-// repay (measured: -11 % on ragged 2048-token chunks, +4 to +8 % on 272- and
-// 288-token chunks).
+// repay (measured on a ragged batch, kernel time against split-major order:
+// -10 % with 2048-token chunks, -1 to -1.5 % with 1376 and 1648, +3 % with
+// 1024, +4 to +8 % with 272 and 288).
 // ---------------------------------------------------------------------------
 
 // lane of the n-th (from 0) set bit of mask

@@ -42,7 +42,7 @@ struct DecodeParams {
 // Longest-first dispatch of the paged decode (decode_kernel.cuh, lpt_item):
 // batches of at most kLptMaxRows rows, chunks of at least kLptMinChunk tokens.
 constexpr int kLptMaxRows = 128;
-constexpr int kLptMinChunk = 1024;
+constexpr int kLptMinChunk = 1280;
 
 struct KernelKey {
   Path path;

@@ -1,6 +1,6 @@
 """Longest-first dispatch of the paged decode, against the FP64 oracle.
 
-Paged calls whose chunks hold at least 1024 tokens (batches of up to 128 rows)
+Paged calls whose chunks hold at least 2048 tokens (batches of up to 128 rows)
 hand the (unit, split) items to the CTAs longest chunk first instead of in
 split-major order.  Only which CTA computes which split changes, so every
 output, lse and split partial must still be the oracle's.  The lengths put
@@ -21,11 +21,11 @@ from helpers import (assert_close_oracle, assert_lse_oracle, lse_bound, oracle_p
 
 pytestmark = pytest.mark.gpu
 
-CHUNK = 1024
-# cap 4096 = 4 chunks: rows with 0..4 full chunks and partial chunks of
-# 1, 22, 552, 1022, 1023 tokens (quarters 0, 0, 2, 3, 3), one empty row and
+CHUNK = 2048
+# cap 8192 = 4 chunks: rows with 0..4 full chunks and partial chunks of
+# 1, 44, 1104, 2044, 2047 tokens (quarters 0, 0, 2, 3, 3), one empty row and
 # one row beyond the cap
-LENS = [0, 1, 1023, 1024, 1025, 2047, 2048, 2070, 2600, 3070, 4096, 5000]
+LENS = [0, 1, 2047, 2048, 2049, 4095, 4096, 4140, 5200, 6140, 8192, 9000]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -43,7 +43,7 @@ def _bound(c):
 
 
 def _case(lens, cache="int8", seed=31, Hq=16, Hkv=2):
-    return W.random_paged(seed=seed, B=len(lens), Hq=Hq, Hkv=Hkv, D=128, bs=16, max_blocks=256,
+    return W.random_paged(seed=seed, B=len(lens), Hq=Hq, Hkv=Hkv, D=128, bs=16, max_blocks=512,
                           lens=lens, sink=True, cache=cache)
 
 
@@ -85,19 +85,19 @@ def test_ragged_rows_every_item_class(cache):
 
 
 def test_window_with_long_chunks():
-    # window 1500: span min(4096, 1516) = 1516 -> 2 chunks of 1024 counted from
+    # window 3500: span min(8192, 3516) = 3516 -> 2 chunks of 2048 counted from
     # the window start
     c = _case(LENS, seed=32)
-    o, lse = run_paged(c, num_splits=2, chunk=CHUNK, window=1500)
-    _check_outputs(c, o, lse, window=1500)
-    _check_partials(c, 2, window=1500)
+    o, lse = run_paged(c, num_splits=2, chunk=CHUNK, window=3500)
+    _check_outputs(c, o, lse, window=3500)
+    _check_partials(c, 2, window=3500)
 
 
 @pytest.mark.parametrize("B", [32, 33, 100, 128, 129])
 def test_batches_up_to_128_rows_and_one_more(B):
     # up to 128 rows (one to four rows per lane): the dispatch ranks the
     # batch; 129 rows: split-major order
-    lens = W.make_rng(33).integers(0, 4600, size=B)
+    lens = W.make_rng(33).integers(0, 9200, size=B)
     c = _case(lens, seed=34, Hq=8, Hkv=1)
     o, lse = run_paged(c, num_splits=4, chunk=CHUNK)
     _check_outputs(c, o, lse)
@@ -105,8 +105,8 @@ def test_batches_up_to_128_rows_and_one_more(B):
 
 def test_single_split_rows_ordered_by_length():
     # one split of the whole capacity: the items are the units, longest first
-    c = _case([10, 4000, 0, 2500, 700, 4096], seed=35)
-    o, lse = run_paged(c, num_splits=1, chunk=4096)
+    c = _case([10, 8000, 0, 5000, 1400, 8192], seed=35)
+    o, lse = run_paged(c, num_splits=1, chunk=8192)
     _check_outputs(c, o, lse)
 
 
@@ -114,8 +114,8 @@ def test_captured_graph_replays_with_other_lengths():
     """The order is decided on the device from the live lengths: one captured
     launch serves two different batches."""
     import int8_kv_cache_gb300 as K
-    lens_a = [2048, 10, 3000, 0, 4096, 1500]
-    lens_b = [1, 4096, 1024, 2600, 30, 3333]
+    lens_a = [4096, 10, 6000, 0, 8192, 3000]
+    lens_b = [1, 8192, 2048, 5200, 60, 6666]
     c = _case(np.maximum(lens_a, lens_b), seed=36)
     d = paged_to_device(c)
     B, Hq, D = c.q.shape
