@@ -88,8 +88,6 @@ typedef enum {
 #define I8KV_FLAG_BAD_SLOT 0x8u    /* reshape_and_cache: a slot >= num_slots was skipped      */
 #define I8KV_FLAG_FP32_PATH 0x10u  /* some CTA evaluated its heads on the FP32 path (see the
                                       numerical eligibility rules below)                     */
-#define I8KV_FLAG_WAIT_TIMEOUT 0x20u /* a CTA gave up waiting (about a second) for its own
-                                        tensor-core products; its outputs were not written */
 
 /* Human-readable name of a status code (static storage). */
 const char* i8kv_status_string(int status);
@@ -100,27 +98,6 @@ int32_t i8kv_version(void);
 /* The cudaError_t value behind the calling thread's most recent I8KV_ECUDA
  * (0 if there was none). */
 int32_t i8kv_last_cuda_error(void);
-
-/* Decode engines: the kernel family behind dsa_decode, dsa_decode_static_workspace
- * and paged_decode(_ex). */
-#define I8KV_ENGINE_MMA 0     /* mma.sync m16n8k16 tiles with the exact int8 -> fp16
-                                 conversion in registers (the default)               */
-#define I8KV_ENGINE_TCGEN05 1 /* tcgen05 MMAs with tensor-memory accumulators, one per
-                                 CTA, operands converted into shared memory          */
-
-/*
- * i8kv_set_decode_engine -- select the decode engine for the whole process.
- * The tcgen05 engine serves int8 and e4m3fn caches with head_dim 128 or 256;
- * fp16 caches, other head dims and dsa_prefill always run on the MMA engine.
- * Both engines compute the same quantities under the same geometry rules, but
- * decode_plan's wave (and so the automatic geometry) is the selected engine's:
- * select it before planning, and not while another thread plans or launches.
- * Errors: I8KV_EINVAL for an unknown engine.
- */
-i8kv_status i8kv_set_decode_engine(int32_t engine);
-
-/* The selected decode engine (I8KV_ENGINE_*). */
-int32_t i8kv_decode_engine(void);
 
 /*
  * split_geometry -- pure host integer arithmetic, no CUDA call.
@@ -281,6 +258,11 @@ i8kv_status paged_decode(const uint16_t* q, const void* k_cache, const void* v_c
   ((window) < 0 || (int64_t)(cap) <= (int64_t)(window) + 16 ? (int64_t)(cap)      \
                                                             : (int64_t)(window) + 16)
 
+/* paged_window_span -- I8KV_WINDOW_SPAN(cap, window) as a function, for
+ * bindings that cannot expand the macro: the positions a windowed paged decode's
+ * splits cover (cap when window < 0).  Pure host arithmetic, no CUDA call. */
+int64_t paged_window_span(int64_t cap, int32_t window);
+
 i8kv_status paged_decode_ex(const uint16_t* q, const void* k_cache, const void* v_cache,
                             int32_t cache_dtype, const float* k_scale, const float* v_scale,
                             int32_t scale_kind, const int32_t* block_table,
@@ -344,7 +326,9 @@ i8kv_status reshape_and_cache(const uint16_t* k_new, const uint16_t* v_new,
  * application's allocator, loops that must never enter the allocator).  The
  * pages have no counterpart; this is a convenience of this library.
  *   Arguments and results as for dsa_decode, without workspace and
- *   workspace_bytes.  The split partials go to a device array inside the
+ *   workspace_bytes, except that out must not be NULL when S > 0 (I8KV_EINVAL:
+ *   partials left in the library's private array could not be read by the
+ *   caller).  The split partials go to a device array inside the
  *   library of I8KV_STATIC_WORKSPACE_BYTES bytes, allocated when CUDA loads the
  *   library's device code on a device and held on every such device until the
  *   process exits.  Nothing is allocated or freed by the call itself.
@@ -353,12 +337,17 @@ i8kv_status reshape_and_cache(const uint16_t* k_new, const uint16_t* v_new,
  *     I8KV_EWORKSPACE before anything is enqueued.
  *   - The first call on a device looks the array's device address up
  *     (cudaGetSymbolAddress, with that device current) and caches it; make that
- *     first call before any stream capture.
+ *     first call before any stream capture.  The cached address belongs to the
+ *     device's current CUDA context: do not call this entry point again after
+ *     cudaDeviceReset (or any other teardown of the primary context) in the
+ *     same process.
  *   - All calls on a device share the one array.  Calls whose kernels can run
  *     at the same time on the GPU (different streams without ordering between
  *     them) race on it and give wrong results; calls ordered on one stream are
- *     fine.  Nothing in it needs clearing between calls: each call writes every
- *     entry it reads back.
+ *     fine.  Nothing in it needs clearing between calls: each call's decode
+ *     kernel writes the (m, l) entry of every (unit, split, head) that its
+ *     combine reads, and the combine reads a split's partial vector only when
+ *     that split wrote it.
  */
 #define I8KV_STATIC_WORKSPACE_BYTES (4u * 1024u * 1024u)
 i8kv_status dsa_decode_static_workspace(const uint16_t* q, const int8_t* k_cache,

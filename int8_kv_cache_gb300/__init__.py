@@ -10,7 +10,6 @@ no fallback.  PyTorch provides device memory and streams.
 """
 from __future__ import annotations
 
-import contextlib
 import ctypes
 import os
 from typing import Optional
@@ -21,8 +20,7 @@ __all__ = [
     "Int8KVError", "load", "library_path", "split_geometry", "split_workspace_bytes",
     "decode_plan", "dsa_decode", "dsa_prefill", "paged_decode", "split_combine", "int8_to_fp16",
     "dsa_decode_static_workspace", "STATIC_WORKSPACE_BYTES", "reshape_and_cache",
-    "FLAG_BAD_SLOT", "FLAG_FP32_PATH", "FLAG_WAIT_TIMEOUT", "ENGINE_MMA", "ENGINE_TCGEN05",
-    "set_decode_engine", "decode_engine", "engine", "paged_decode_ex", "window_span",
+    "FLAG_BAD_SLOT", "FLAG_FP32_PATH", "paged_decode_ex", "window_span",
     "CACHE_FP8", "fp8_to_fp16",
     "SCALE_PER_TENSOR", "SCALE_PER_CHANNEL", "CACHE_INT8", "CACHE_FP16", "GEOM_WAVE",
     "GEOM_POW2_TILES", "PATH_DSA", "PATH_PAGED", "MAX_SPLITS", "FLAG_LEN_CLAMPED",
@@ -44,9 +42,6 @@ FLAG_QUERY_RANGE = 0x2
 FLAG_BAD_BLOCK = 0x4
 FLAG_BAD_SLOT = 0x8
 FLAG_FP32_PATH = 0x10
-FLAG_WAIT_TIMEOUT = 0x20
-ENGINE_MMA = 0
-ENGINE_TCGEN05 = 1
 STATIC_WORKSPACE_BYTES = 4 * 1024 * 1024
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -61,8 +56,7 @@ _SIGNATURES = {
     "i8kv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "i8kv_version": (_c_i32, []),
     "i8kv_last_cuda_error": (_c_i32, []),
-    "i8kv_set_decode_engine": (_c_i32, [_c_i32]),
-    "i8kv_decode_engine": (_c_i32, []),
+    "paged_window_span": (_c_i64, [_c_i64, _c_i32]),
     "split_geometry": (_c_i32, [_c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                 _P_I32, _P_I32]),
     "split_workspace_bytes": (_c_sz, [_c_i32, _c_i32, _c_i32, _c_i32]),
@@ -152,6 +146,16 @@ def _t(x: Optional[torch.Tensor], dtype, name: str) -> Optional[int]:
     return x.data_ptr()
 
 
+def _on_current_device(x: torch.Tensor, name: str) -> None:
+    """The library works on the current CUDA device (its kernels, its cached
+    launch attributes and its static workspace are per device): refuse tensors
+    that live on another one."""
+    if x.is_cuda and x.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {x.device}, but the current device is "
+                         f"cuda:{torch.cuda.current_device()}; call under "
+                         f"torch.cuda.device({x.device})")
+
+
 def _stream(stream) -> Optional[int]:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -178,26 +182,6 @@ def split_workspace_bytes(units: int, num_splits: int, G: int, D: int) -> int:
     return int(load().split_workspace_bytes(units, num_splits, G, D))
 
 
-def set_decode_engine(engine: int) -> None:
-    """Select the process-wide decode engine (ENGINE_MMA or ENGINE_TCGEN05)."""
-    _check("i8kv_set_decode_engine", load().i8kv_set_decode_engine(engine))
-
-
-def decode_engine() -> int:
-    return int(load().i8kv_decode_engine())
-
-
-@contextlib.contextmanager
-def engine(e: int):
-    """Run a block with another decode engine selected, then restore the previous one."""
-    prev = decode_engine()
-    set_decode_engine(e)
-    try:
-        yield
-    finally:
-        set_decode_engine(prev)
-
-
 def decode_plan(path: int, cache_dtype: int, cap: int, rows: int, Hq: int, Hkv: int, D: int,
                 mode: int, override_value: int = 0):
     """(num_splits, chunk, workspace_bytes, wave_ctas) on the current device."""
@@ -221,6 +205,7 @@ def dsa_decode(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, idx,
     idx [S, max_sel] int32.  Returns ``out`` ([S, Hq, D] fp16).  With
     ``partials_only`` (and num_splits > 1) only the workspace partials are
     written (out is NULL at the C ABI) and None is returned."""
+    _on_current_device(q, "q")
     S, Hq, D = q.shape
     N, Hkv, _ = k_cache.shape
     max_sel = idx.shape[1]
@@ -241,6 +226,7 @@ def dsa_prefill(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, idx,
                 softmax_scale: float, head_sink=None, out=None, lse=None, flags=None,
                 stream=None):
     """Sparse-candidate prefill (tensor-core path, no splits)."""
+    _on_current_device(q, "q")
     S, Hq, D = q.shape
     N, Hkv, _ = k_cache.shape
     max_sel = idx.shape[1]
@@ -257,8 +243,9 @@ def dsa_prefill(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, idx,
 
 
 def window_span(cap: int, window: int) -> int:
-    """Positions the splits of a windowed paged decode cover (I8KV_WINDOW_SPAN)."""
-    return cap if window < 0 or cap <= window + 16 else window + 16
+    """Positions the splits of a windowed paged decode cover (the library's
+    paged_window_span, i.e. I8KV_WINDOW_SPAN)."""
+    return int(load().paged_window_span(cap, window))
 
 
 def paged_decode(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, block_table, seq_lens,
@@ -270,6 +257,7 @@ def paged_decode(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, block_t
     With ``partials_only`` (and num_splits > 1) only the workspace partials are
     written and None is returned.  ``softcap`` > 0 or ``window`` >= 0 go through
     the C entry point paged_decode_ex, the defaults through paged_decode."""
+    _on_current_device(q, "q")
     B, Hq, D = q.shape
     nb, bs, Hkv, _ = k_cache.shape
     max_blocks = block_table.shape[1]
@@ -303,6 +291,7 @@ def paged_decode_ex(*args, softcap: float = 0.0, window: int = -1, **kw):
 def split_combine(acc, m, l, Hq: int, Hkv: int, head_sink=None, out=None, lse=None,
                   stream=None):
     """Combine partials acc [units, splits, G, D], m, l [units, splits, G] (fp32)."""
+    _on_current_device(acc, "acc")
     units, ns, G, D = acc.shape
     if out is None:
         out = torch.empty((units * G, D), dtype=torch.float16, device=acc.device)
@@ -330,6 +319,7 @@ def reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_s
     """Quantize new rows k_new / v_new [T, Hkv, D] (fp16) into the INT8 or
     float8 e4m3fn caches (int8, or uint8 / float8_e4m3fn tensors, [num_slots,
     Hkv, D] or [num_blocks, block_size, Hkv, D]) at slot_mapping [T]."""
+    _on_current_device(k_new, "k_new")
     T, Hkv, D = k_new.shape
     num_slots = k_cache.numel() // (Hkv * D)
     cd = _cache_dtype(k_cache, allow_fp16=False)
@@ -368,6 +358,7 @@ def dsa_decode_static_workspace(q, k_cache, v_cache, k_scale, v_scale, scale_kin
     array (STATIC_WORKSPACE_BYTES), for callers that cannot allocate scratch
     memory when they call; calls that may run concurrently on the GPU must not
     use it (they share the array)."""
+    _on_current_device(q, "q")
     S, Hq, D = q.shape
     N, Hkv, _ = k_cache.shape
     max_sel = idx.shape[1]

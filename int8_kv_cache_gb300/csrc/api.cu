@@ -4,7 +4,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <map>
@@ -56,8 +55,6 @@ i8kv_status check_scales(const float* ks, const float* vs, int32_t kind) {
   return I8KV_OK;
 }
 
-std::atomic<int32_t> g_engine{I8KV_ENGINE_MMA};
-
 KernelKey make_key(Path path, int32_t D, int32_t G, int32_t cache_dtype, bool p_lo) {
   KernelKey k;
   k.path = path;
@@ -66,9 +63,6 @@ KernelKey make_key(Path path, int32_t D, int32_t G, int32_t cache_dtype, bool p_
   k.fp16_cache = cache_dtype == I8KV_CACHE_FP16;
   k.fp8_cache = cache_dtype == I8KV_CACHE_FP8;
   k.p_lo = p_lo;
-  // the tensor-memory kernel: decode (not prefill) over int8 / e4m3fn codes,
-  // head_dim 128 or 256, when that engine is selected
-  k.tc = g_engine.load() == I8KV_ENGINE_TCGEN05 && p_lo && !k.fp16_cache && (D == 128 || D == 256);
   return k;
 }
 
@@ -85,13 +79,13 @@ cudaError_t launch_key(const KernelKey& key, const DecodeParams& p, cudaStream_t
 // current device, cached per (device, kernel).
 i8kv_status wave_of(const KernelKey& key, int32_t* wave) {
   static std::mutex mu;
-  static std::map<std::tuple<int, int, int, int, int, int, int, int>, int32_t> cache;
+  static std::map<std::tuple<int, int, int, int, int, int, int>, int32_t> cache;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   const auto k = std::make_tuple(dev, static_cast<int>(key.path), key.D, key.nt,
                                  static_cast<int>(key.fp16_cache), static_cast<int>(key.fp8_cache),
-                                 static_cast<int>(key.p_lo), static_cast<int>(key.tc));
+                                 static_cast<int>(key.p_lo));
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(k);
@@ -225,18 +219,12 @@ const char* i8kv_status_string(int status) {
   }
 }
 
-int32_t i8kv_version(void) { return 100; }
+int32_t i8kv_version(void) { return 200; }
 
 // The CUDA error code behind the calling thread's last I8KV_ECUDA (0 if none).
 int32_t i8kv_last_cuda_error(void) { return g_last_cuda_error; }
 
-i8kv_status i8kv_set_decode_engine(int32_t engine) {
-  if (engine != I8KV_ENGINE_MMA && engine != I8KV_ENGINE_TCGEN05) return I8KV_EINVAL;
-  g_engine.store(engine);
-  return I8KV_OK;
-}
-
-int32_t i8kv_decode_engine(void) { return g_engine.load(); }
+int64_t paged_window_span(int64_t cap, int32_t window) { return I8KV_WINDOW_SPAN(cap, window); }
 
 i8kv_status split_geometry(int64_t cap, int32_t units, int32_t wave_ctas, int32_t granule,
                            int32_t min_chunk, int32_t max_splits, int32_t mode,

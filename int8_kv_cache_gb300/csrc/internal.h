@@ -51,7 +51,6 @@ struct KernelKey {
   bool fp16_cache;
   bool fp8_cache;  // float8 e4m3fn codes (same tile as int8, other conversion)
   bool p_lo;       // probability tile as fp16 high + low parts
-  bool tc;         // served by the tcgen05 (tensor-memory) decode kernel
 };
 
 // Per-path launchers (one per translation unit): grid (rows * Hkv, num_splits);

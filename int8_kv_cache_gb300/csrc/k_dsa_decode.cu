@@ -1,10 +1,9 @@
-// Instantiations of the decode kernels: DSA sparse-candidate decode (the mma.sync kernel, or the tensor-memory kernel when that engine is selected).
-#include "decode_tc.cuh"
+// Instantiations of the decode kernel: DSA sparse-candidate decode.
+#include "decode_kernel.cuh"
 
 namespace i8kv {
 cudaError_t launch_dsa_decode(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
-                           int* occupancy) {
-  return key.tc ? dispatch_decode_tc<false, false>(key, p, s, occupancy)
-                : dispatch_decode<false, false, true>(key, p, s, occupancy);
+                              int* occupancy) {
+  return dispatch_decode<false, false, true>(key, p, s, occupancy);
 }
 }  // namespace i8kv

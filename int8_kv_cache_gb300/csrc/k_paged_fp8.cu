@@ -1,10 +1,9 @@
-// Instantiations of the decode kernels: paged decode over a float8 e4m3fn cache (the mma.sync kernel, or the tensor-memory kernel when that engine is selected).
-#include "decode_tc.cuh"
+// Instantiations of the decode kernel: paged decode over a float8 e4m3fn cache.
+#include "decode_kernel.cuh"
 
 namespace i8kv {
 cudaError_t launch_paged_fp8(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
                              int* occupancy) {
-  return key.tc ? dispatch_decode_tc<true, true>(key, p, s, occupancy)
-                : dispatch_decode<true, false, true, true>(key, p, s, occupancy);
+  return dispatch_decode<true, false, true, true>(key, p, s, occupancy);
 }
 }  // namespace i8kv

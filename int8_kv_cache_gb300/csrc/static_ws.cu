@@ -31,6 +31,8 @@ void* g_ptr[kMaxDevices] = {};
 // Device address of the scratch on the current device.  The symbol's name in
 // host code is not a device address, so it is resolved with
 // cudaGetSymbolAddress once per device, with that device current, and cached.
+// The cache assumes the device's primary context lives as long as the process
+// (no cudaDeviceReset in between): a reset unloads the array with the module.
 i8kv_status static_workspace(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -60,6 +62,9 @@ extern "C" i8kv_status dsa_decode_static_workspace(
   // combine reads a split's accumulator only when that split wrote it.  So no
   // clearing is needed between calls, and the previous call's contents are
   // never read.
+  // With out == NULL dsa_decode would leave the partials in the array below,
+  // where the caller cannot read them: refuse it.
+  if (out == nullptr && S > 0) return I8KV_EINVAL;
   void* ws = nullptr;
   i8kv_status st = static_workspace(&ws);
   if (st != I8KV_OK) return st;

@@ -47,16 +47,11 @@ def test_version_and_status_strings(lib):
     assert lib.i8kv_status_string(4).startswith(b"workspace")
 
 
-def test_decode_engine_selection(lib):
-    # host-side setting: no CUDA call
-    assert lib.i8kv_decode_engine() == 0
-    assert lib.i8kv_set_decode_engine(1) == 0
-    assert lib.i8kv_decode_engine() == 1
-    assert lib.i8kv_set_decode_engine(2) == 1      # unknown engine: EINVAL, unchanged
-    assert lib.i8kv_set_decode_engine(-1) == 1
-    assert lib.i8kv_decode_engine() == 1
-    assert lib.i8kv_set_decode_engine(0) == 0
-    assert lib.i8kv_decode_engine() == 0
+def test_window_span_matches_the_oracle(lib):
+    # host-only arithmetic: the span a windowed paged decode's splits cover
+    for cap in (0, 16, 96, 512, 4096, 8192):
+        for window in (-1, 0, 1, 15, 16, 80, 95, 496, 1023, 5000):
+            assert lib.paged_window_span(cap, window) == oracle.window_span(cap, window)
 
 
 def test_geometry_bit_exact_with_oracle(lib):
