@@ -33,6 +33,7 @@ import statistics
 import subprocess
 import sys
 import time
+from typing import Optional
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -60,12 +61,11 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--extra", default="all",
-                    choices=["all", "paged", "variants", "fp8", "deep", "prefill", "quantize",
-                             "engine", "none"],
+                    choices=["all", "sparse", "paged", "variants", "fp8", "deep", "prefill",
+                             "quantize", "none"],
                     help="which other workloads to measure besides the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
-    ap.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
-    ap.add_argument("--reference-worker", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--clock-sampler", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -73,97 +73,164 @@ def parse():
 # the oracle on the host cores (CPU baseline and the reference arm)
 # --------------------------------------------------------------------------
 
-def cpu_worker(spec: str):
-    """Runs in a child process with single-threaded BLAS: time the FP64 oracle
-    on whole calls of the headline workload until `budget` seconds passed."""
-    import numpy as np  # noqa: F401
+def _oracle_worker(wid: int, nworkers: int, cmd_q, res_q):
+    """One host core of the oracle pool: build the headline workload (seeded,
+    the same in every worker), then on each command compute the requested
+    number of query rows (both KV heads of a row) with the FP64 oracle.
+    Worker w takes the rows w, w + nworkers, ... of the 8-row call, cycling."""
     import oracle
     import workloads as W
-    a = json.loads(spec)
-    c = W.sparse_decode(S_ROWS, seed=a["seed"])
-    t0 = time.perf_counter()
-    calls = 0
-    while True:
-        oracle.sparse_attention(c.q, c.k_codes, c.v_codes, c.k_scale, c.v_scale, c.scale_kind,
-                                c.idx, c.sigma)
-        calls += 1
-        if time.perf_counter() - t0 >= a["budget"] or calls >= a["max_calls"]:
-            break
-    dt = time.perf_counter() - t0
-    print(json.dumps(dict(calls=calls, seconds=dt)))
-
-
-def reference_worker(spec: str):
-    """The reference arm in one child process with single-threaded BLAS: the
-    FP64 oracle on the headline workload, W warm-up and K timed steps, each step
-    whole query rows (both KV heads of a row: 1/8 of a call), as many as keep
-    the whole run near its time budget."""
-    import oracle
-    import workloads as W
-    a = json.loads(spec)
     c = W.sparse_decode(S_ROWS, seed=0)
-
-    def rows(r0, n):
-        for i in range(n):
-            r = (r0 + i) % S_ROWS
-            oracle.sparse_attention(c.q[r:r + 1], c.k_codes, c.v_codes, c.k_scale, c.v_scale,
-                                    c.scale_kind, c.idx[r:r + 1], c.sigma)
-    t0 = time.perf_counter()
-    rows(0, 1)
-    t_row = time.perf_counter() - t0
-    n = max(1, int(a["budget"] / max(1, a["steps"] + a["warmup"]) / max(t_row, 1e-6)))
-    r = 0
-    for _ in range(a["warmup"]):
-        rows(r, n)
-        r += n
-    t0 = time.perf_counter()
-    for _ in range(a["steps"]):
-        rows(r, n)
-        r += n
-    print(json.dumps(dict(rows=n * a["steps"], rows_per_step=n, seconds=time.perf_counter() - t0)))
+    res_q.put(("ready", wid, 0))
+    r = wid
+    while True:
+        n = cmd_q.get()
+        if n is None:
+            break
+        for _ in range(n):
+            k = r % S_ROWS
+            oracle.sparse_attention(c.q[k:k + 1], c.k_codes, c.v_codes, c.k_scale, c.v_scale,
+                                    c.scale_kind, c.idx[k:k + 1], c.sigma)
+            r += nworkers
+        res_q.put(("done", wid, n))
 
 
-def run_cpu_oracle(budget_s: float, max_calls: int = 1000000, seed: int = 0):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    spec = json.dumps(dict(budget=budget_s, max_calls=max_calls, seed=seed))
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", spec],
-                       capture_output=True, text=True, env=env, cwd=ROOT)
-    if r.returncode != 0:
-        raise RuntimeError(f"cpu oracle worker failed: {r.stderr[-2000:]}")
-    res = json.loads(r.stdout.strip().splitlines()[-1])
-    b = sum(call_bytes().values())
-    gbs = res["calls"] * b / res["seconds"] / 1e9
-    return dict(value=gbs, unit="GB/s", cores=1, kind="oracle", calls=res["calls"],
-                seconds=res["seconds"], seconds_per_call=res["seconds"] / res["calls"],
-                sample=f"{res['calls']} whole call(s) of the headline workload (one layer, S=8 "
-                       f"rows x 24 heads x 2048 candidates), FP64 NumPy oracle, single-threaded "
-                       f"BLAS, {res['seconds']:.1f} s")
+class OraclePool:
+    """The FP64 oracle on every host core this process may use: one spawned
+    worker per core, each with single-threaded BLAS, computing whole query rows
+    of the headline workload.  A step sends every worker the same row count and
+    ends when the last one is done (wall clock)."""
+
+    def __init__(self, cores: int):
+        import multiprocessing as mp
+        self.cores = cores
+        ctx = mp.get_context("spawn")  # never fork after CUDA has been touched
+        saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS",
+                                                 "MKL_NUM_THREADS", "CUDA_VISIBLE_DEVICES")}
+        os.environ.update(OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+                          CUDA_VISIBLE_DEVICES="")
+        try:
+            self.cmd = [ctx.Queue() for _ in range(cores)]
+            self.res = ctx.Queue()
+            self.procs = [ctx.Process(target=_oracle_worker, args=(w, cores, self.cmd[w], self.res),
+                                      daemon=True) for w in range(cores)]
+            for p in self.procs:
+                p.start()
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        for _ in range(cores):
+            self._get()
+
+    def _get(self):
+        msg = self.res.get(timeout=600)
+        return msg
+
+    def step(self, rows_per_worker: int) -> float:
+        """Wall seconds for every worker to compute rows_per_worker rows."""
+        t0 = time.perf_counter()
+        for q in self.cmd:
+            q.put(rows_per_worker)
+        for _ in range(self.cores):
+            self._get()
+        return time.perf_counter() - t0
+
+    def close(self):
+        for q in self.cmd:
+            q.put(None)
+        for p in self.procs:
+            p.join(timeout=30)
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_cpu_oracle(budget_s: float):
+    """cpu_baseline: the oracle on all host cores for about budget_s seconds."""
+    cores = host_cores()
+    pool = OraclePool(cores)
+    try:
+        pool.step(1)  # warm-up: one row per worker
+        t_row = pool.step(1)
+        n = max(1, int(budget_s / max(t_row, 1e-6)))
+        sec = pool.step(n)
+    finally:
+        pool.close()
+    rows = n * cores
+    row_bytes = sum(call_bytes().values()) / S_ROWS
+    return dict(value=rows * row_bytes / sec / 1e9, unit="GB/s", cores=cores, kind="oracle",
+                seconds=sec, rows=rows, seconds_per_call=sec / rows * S_ROWS,
+                sample=f"{rows} query rows of the headline workload ({n} per core; a call is "
+                       f"{S_ROWS} rows x 24 heads x 2048 candidates), FP64 NumPy oracle, one "
+                       f"spawned process per host core ({cores}) with single-threaded BLAS, "
+                       f"{sec:.1f} s wall")
 
 
 # --------------------------------------------------------------------------
 # clocks during the timed region
 # --------------------------------------------------------------------------
 
-class ClockSampler:
-    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+_NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
+
+def clock_sampler(spec: str):
+    """Child process: read the GPU's SM clock, its maximum and the clock event
+    reasons through NVML (read only) every 2 ms and print one line per sample
+    (wall time, MHz, max MHz, reason bits) until killed."""
+    import ctypes
+    a = json.loads(spec)
+    nv = ctypes.CDLL("libnvidia-ml.so.1")
+    if nv.nvmlInit_v2() != 0:
+        raise SystemExit(2)
+    h = ctypes.c_void_p()
+    rc = -1
+    if a.get("uuid"):  # the CUDA device's own UUID: right whatever CUDA_VISIBLE_DEVICES says
+        rc = nv.nvmlDeviceGetHandleByUUID(a["uuid"].encode(), ctypes.byref(h))
+    if rc != 0:
+        rc = nv.nvmlDeviceGetHandleByIndex_v2(a["index"], ctypes.byref(h))
+    if rc != 0:
+        raise SystemExit(3)
+    reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+        nv.nvmlDeviceGetCurrentClocksThrottleReasons
+    mhz, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+    nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+    print("ready", flush=True)
+    while True:
+        nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz))
+        reasons_fn(h, ctypes.byref(rs))
+        print(f"{time.time():.6f} {mhz.value} {mx.value} {rs.value}", flush=True)
+        time.sleep(0.002)
+
+
+class ClockSampler:
+    """SM clocks and clock event reasons sampled every 2 ms (NVML, in a child
+    process) around the timed region; the samples inside it are kept."""
+
+    def __init__(self, device_index: int, uuid: Optional[str]):
+        self.spec = json.dumps(dict(index=device_index, uuid=uuid))
         self.proc = None
-        self.idx = gpu_index
         self.t_start = self.t_stop = None
 
     def start(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except (OSError, ValueError):
+            self.proc = subprocess.Popen([sys.executable, os.path.abspath(__file__),
+                                          "--clock-sampler", self.spec],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            line = self.proc.stdout.readline()
+            if not line.startswith("ready"):
+                self.proc.kill()
+                self.proc = None
+        except OSError:
             self.proc = None
-        time.sleep(0.3)
 
     def mark(self, start: bool):
         if start:
@@ -174,35 +241,29 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.2)
+        time.sleep(0.01)
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        rows = [ln.split(",") for ln in out.strip().splitlines() if ln.count(",") >= 8]
+        rows = []
+        for ln in out.strip().splitlines():
+            f = ln.split()
+            if len(f) == 4:
+                rows.append((float(f[0]), float(f[1]), float(f[2]), int(f[3])))
+        inside = [r for r in rows if self.t_start is not None and
+                  self.t_start <= r[0] <= (self.t_stop or 1e30)]
+        window = "timed region" if inside else "around the timed region"
+        rows = inside or rows[-20:]
         if not rows:
             return None
-
-        def when(r):
-            try:
-                import datetime
-                return datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
-            except ValueError:
-                return None
-        inside = [r for r in rows if when(r) is not None and self.t_start is not None
-                  and self.t_start <= when(r) <= (self.t_stop or 1e30)]
-        window = "timed region" if inside else "around the timed region"
-        rows = inside or rows
-        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4)
-                          if r[5 + i].strip().lower() == "active"})
-        return dict(sm_mhz=statistics.median(sm) if sm else None,
-                    sm_max_mhz=max(mx) if mx else None, reasons=reasons, samples=len(rows),
-                    window=window)
+        reasons = sorted({name for r in rows for bit, name in _NVML_REASONS.items()
+                          if r[3] & bit})
+        return dict(sm_mhz=statistics.median(r[1] for r in rows),
+                    sm_max_mhz=max(r[2] for r in rows), reasons=reasons, samples=len(rows),
+                    window=window, source="NVML every 2 ms")
 
 
 # --------------------------------------------------------------------------
@@ -330,7 +391,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
             g.replay()
     torch.cuda.synchronize()
 
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(local_rank, getattr(props, "uuid", None) and
+                          "GPU-" + str(props.uuid).replace("GPU-", ""))
     clocks.start()
     if dist is not None:
         dist.barrier()
@@ -471,7 +533,67 @@ def gpu_arm(args, rank, world, local_rank, dist):
     }
     if args.extra != "none":
         out["other_configs"] = extra_configs(torch, K, W, np, dev, stream, peaks, args)
+        if args.extra in ("all", "sparse"):
+            out["other_configs"]["sparse_decode_rows"] = _sparse_rows(
+                torch, K, W, layers, stream, peaks["hbm_gbs"], kernel_us_s8=t_kernel * 1e6,
+                call_us_s8=us_per_call)
+        deep = out["other_configs"].get("deep_context_int8")
+        if deep is not None:
+            a = deep["adaptive"]
+            kb = deep["bytes_per_call"] - 16 * 16 * 128 * 2  # the kernel writes partials, not O
+            out["roofline_deep"] = {
+                "bound": "hbm", "achieved": round(kb / (a["kernel_us"] * 1e-6) / 1e9, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(kb / (a["kernel_us"] * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                "traffic": ncu_traffic("deep_context_int8"),
+                "kernel": "decode_kernel<128,1,paged,int8,hi+lo>", "us_per_launch": a["kernel_us"],
+                "bytes_per_launch": kb, "us_per_call": a["us_per_call"],
+                "workload": deep["workload"] + ", adaptive geometry (wave rule)",
+                "peak_source": f"{peak_src} hbm_gbs"}
     return out
+
+
+def _sparse_rows(torch, K, W, layers, stream, hbm, kernel_us_s8, call_us_s8):
+    """The headline workload at S = 1, 2 and 4 query rows (the first S rows of
+    each layer's S = 8 rows and lists, the same 32 caches): the call and the
+    decode kernel alone, each as a graph of 32 calls."""
+    res = {}
+    for S in (1, 2, 4):
+        ns, chunk, wsb, wave = K.decode_plan(K.PATH_DSA, K.CACHE_INT8, N_SEL, S, HQ, HKV, D,
+                                             K.GEOM_POW2_TILES)
+        ws = torch.empty(max(wsb // 4, 4), dtype=torch.float32, device=layers[0]["q"].device)
+        views = [(x["q"][:S].contiguous(), x["k"], x["v"], x["ks"], x["vs"],
+                  x["idx"][:S].contiguous(), torch.empty_like(x["q"][:S])) for x in layers]
+
+        def fn(partials=False):
+            for q_, k_, v_, ks_, vs_, idx_, out_ in views:
+                K.dsa_decode(q_, k_, v_, ks_, vs_, W.SCALE_PER_CHANNEL, idx_, SIGMA,
+                             num_splits=ns, chunk=chunk, workspace=ws,
+                             out=None if partials else out_, partials_only=partials)
+        b = call_bytes(S=S)
+        sec = _graph_seconds(torch, fn, stream, len(views))
+        row = dict(us_per_call=round(sec * 1e6, 3), gbs=round(sum(b.values()) / sec / 1e9, 1),
+                   frac_of_hbm=round(sum(b.values()) / sec / 1e9 / hbm, 4), num_splits=ns,
+                   chunk=chunk, wave_ctas=wave)
+        if ns > 1:
+            ksec = _graph_seconds(torch, lambda: fn(True), stream, len(views))
+            kb = sum(b.values()) - b["out"]
+            row.update(kernel_us=round(ksec * 1e6, 3),
+                       kernel_frac_of_hbm=round(kb / ksec / 1e9 / hbm, 4))
+        res[f"S{S}"] = row
+    res["S8"] = dict(us_per_call=round(call_us_s8, 3), kernel_us=round(kernel_us_s8, 3),
+                     note="the headline line above")
+    return dict(workload=WORKLOAD.replace("S=8 rows", "S=1/2/4 rows") +
+                "; 32 layers per graph (the headline's caches, its first S rows and lists)",
+                **res)
+
+
+def _graph_seconds(torch, fn, stream, calls, reps=50):
+    g = capture(torch, fn, stream)
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            g.replay()
+    return time_graph(torch, g, reps, stream) / (reps * calls)
 
 
 def extra_configs(torch, K, W, np, dev, stream, peaks, args):
@@ -506,42 +628,7 @@ def extra_configs(torch, K, W, np, dev, stream, peaks, args):
     if args.extra in ("all", "quantize", "fp8"):
         res["quantize_on_write"] = _quantize(torch, K, np, t, dev, bench_graph, hbm)
         res["quantize_on_write_fp8"] = _quantize(torch, K, np, t, dev, bench_graph, hbm, "fp8")
-    if args.extra in ("all", "engine"):
-        with K.engine(K.ENGINE_TCGEN05):
-            res["engine_tcgen05"] = _engine_tc(torch, K, W, np, t, dev, bench_graph, hbm)
     return res
-
-
-def _engine_tc(torch, K, W, np, t, dev, bench_graph, hbm):
-    """The tcgen05 decode engine on the headline sparse decode (S = 8, 32
-    layers) and on the deep-context int8 sweep's adaptive geometry: the call
-    and the decode kernel alone, for comparison with the default engine."""
-    L = 32
-    layers = []
-    for li in range(L):
-        c = W.sparse_decode(S_ROWS, seed=li)
-        layers.append(dict(q=t(c.q), k=t(c.k_codes), v=t(c.v_codes), ks=t(c.k_scale),
-                           vs=t(c.v_scale), idx=t(c.idx)))
-    ns, chunk, wsb, wave = K.decode_plan(K.PATH_DSA, K.CACHE_INT8, N_SEL, S_ROWS, HQ, HKV, D,
-                                         K.GEOM_POW2_TILES)
-    ws = torch.empty(max(wsb // 4, 4), dtype=torch.float32, device=dev)
-    out = torch.empty((S_ROWS, HQ, D), dtype=torch.float16, device=dev)
-
-    def fn(partials=False):
-        for x in layers:
-            K.dsa_decode(x["q"], x["k"], x["v"], x["ks"], x["vs"], W.SCALE_PER_CHANNEL, x["idx"],
-                         SIGMA, num_splits=ns, chunk=chunk, workspace=ws,
-                         out=None if partials else out, partials_only=partials)
-    b = sum(call_bytes().values())
-    sec = bench_graph(fn, L)
-    ksec = bench_graph(lambda: fn(True), L)
-    kb = b - S_ROWS * HQ * D * 2
-    head = dict(us_per_call=round(sec * 1e6, 2), kernel_us=round(ksec * 1e6, 2),
-                kernel_frac_of_hbm=round(kb / ksec / 1e9 / hbm, 4), num_splits=ns, chunk=chunk,
-                wave_ctas=wave)
-    deep = _deep(torch, K, W, np, t, dev, bench_graph, hbm, "int8")
-    return dict(workload="tcgen05 decode engine: " + WORKLOAD + "; and " + deep["workload"],
-                headline=head, deep_context_int8=deep["adaptive"])
 
 
 def _quantize(torch, K, np, t, dev, bench_graph, hbm, cache="int8"):
@@ -680,32 +767,37 @@ def _prefill(torch, K, W, np, t, bench_graph, peaks):
 
 
 def reference_arm(args, rank, world):
-    """The FP64 oracle on the host cores (one process, single-threaded BLAS),
-    on the headline workload, metric and unit; each step is a bounded sample of
-    whole query rows, sized so the whole run stays near two minutes.  Under
-    torchrun only rank 0 runs and prints."""
+    """The FP64 oracle on the host cores (one spawned process per core,
+    single-threaded BLAS each), on the headline workload, metric and unit.
+    Each step is a bounded sample: every core computes the same number of whole
+    query rows, sized so the whole run stays near two minutes.  Under torchrun
+    only rank 0 runs and prints."""
     if rank != 0:
         return None
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    spec = json.dumps(dict(steps=args.steps, warmup=args.warmup, budget=120.0))
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--reference-worker", spec],
-                       capture_output=True, text=True, env=env, cwd=ROOT)
-    if r.returncode != 0:
-        raise RuntimeError(f"reference worker failed: {r.stderr[-2000:]}")
-    res = json.loads(r.stdout.strip().splitlines()[-1])
+    cores = host_cores()
+    pool = OraclePool(cores)
+    try:
+        t_row = pool.step(1)
+        n = max(1, int(120.0 / max(1, args.steps + args.warmup) / max(t_row, 1e-6)))
+        for _ in range(args.warmup):
+            pool.step(n)
+        sec = sum(pool.step(n) for _ in range(args.steps))
+    finally:
+        pool.close()
+    rows = n * cores * args.steps
     row_bytes = sum(call_bytes().values()) / S_ROWS
-    v = res["rows"] * row_bytes / res["seconds"] / 1e9
-    sample = (f"{res['rows_per_step']} query row(s) per step (both KV heads; a call is "
+    v = rows * row_bytes / sec / 1e9
+    sample = (f"{n * cores} query row(s) per step ({n} per core, both KV heads; a call is "
               f"{S_ROWS} rows) of the headline workload, {args.steps} timed step(s) after "
-              f"{args.warmup} warm-up, FP64 NumPy oracle, single-threaded BLAS")
+              f"{args.warmup} warm-up, FP64 NumPy oracle, one spawned process per host core "
+              f"with single-threaded BLAS")
     return {"metric": "INT8 split-KV decode us/call and achieved HBM GB/s (% of GB300 peak)",
             "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": res["seconds"] / args.steps * 1e3,
-            "us_per_call": res["seconds"] / res["rows"] * S_ROWS * 1e6,
+            "warmup": args.warmup, "ms_per_step": sec / args.steps * 1e3,
+            "us_per_call": sec / rows * S_ROWS * 1e6,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": WORKLOAD}, "impl": "reference",
-            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -713,11 +805,8 @@ def reference_arm(args, rank, world):
 
 def main():
     args = parse()
-    if args.cpu_worker is not None:
-        cpu_worker(args.cpu_worker)
-        return
-    if args.reference_worker is not None:
-        reference_worker(args.reference_worker)
+    if args.clock_sampler is not None:
+        clock_sampler(args.clock_sampler)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -131,11 +131,20 @@ __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
 
 // Programmatic dependent launch: wait until the preceding grid of the stream
 // has completed and its writes are visible (returns at once when the kernel
-// was launched without the programmatic-serialization attribute).  No kernel
-// here triggers its dependents early: measured, an early trigger made the
-// decode + combine pair slower.
+// was launched without the programmatic-serialization attribute).
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+
+// Let the next grid of the stream start launching before this one ends (its
+// CTAs still block in grid_dependency_wait until this grid has completed and
+// its writes are visible, so this only hides launch latency).  Used by the
+// combine kernel only: measured on the sparse decode (S = 8, graphs of 32
+// calls), a trigger at combine entry took a call from 11.55 to 11.26 us, while
+// one at decode entry made the call slower (12.68 us) and the decode kernel
+// alone slower too (8.78 -> 8.89 us).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
 __device__ __forceinline__ void flag_or(uint32_t* flags, uint32_t bits) {
