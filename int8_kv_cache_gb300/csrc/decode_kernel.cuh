@@ -73,7 +73,10 @@ struct Tile {
   static constexpr int kCopies = kStep / kRowsPerCopy;
   static constexpr int kTileBytes = kStep * kRowBytes;   // K (or V) of one step, dense
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kQStride = D + 8;             // Q' staging row (halves), padded
+  // Q' staging row (halves), padded so that the B-fragment loads of a warp
+  // fall in distinct banks: 4-byte loads (fp16 cache) want a row offset of 4
+  // banks, 8-byte loads (int8 / e4m3fn: 4 channels per thread) 8 banks
+  static constexpr int kQStride = FP16C ? D + 8 : D + 16;
   static constexpr int kQBytes = 16 * kQStride * 2;
   // 4-warp groups per SM the registers allow (16, 12 or 8 warps per SM) ...
   static constexpr int kRegGroups = D * NT >= 512 ? 2 : (D * NT >= 256 ? 3 : 4);
@@ -1071,13 +1074,16 @@ decode_kernel(const DecodeParams p) {
     return reinterpret_cast<float*>(smem + w * T::kWarpRing);
   };
   {
+    // a lane's fragment of n-tile nt holds heads nt*8 + 2tig (+1): lanes whose
+    // heads are all padding (G not a multiple of 8) neither write nor read it
     float4* mine = reinterpret_cast<float4*>(frag_of(warp) + lane * (T::kE + 4));
 #pragma unroll
     for (int mt = 0; mt < KC; ++mt)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
-        mine[mt * NT + nt] = make_float4(acc[mt][nt][0], acc[mt][nt][1], acc[mt][nt][2],
-                                         acc[mt][nt][3]);
+        if (nt * 8 + 2 * tig < G)
+          mine[mt * NT + nt] = make_float4(acc[mt][nt][0], acc[mt][nt][1], acc[mt][nt][2],
+                                           acc[mt][nt][3]);
   }
   __syncthreads();
 
@@ -1126,6 +1132,7 @@ decode_kernel(const DecodeParams p) {
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
+      if (nt * 8 + 2 * tig >= G) continue;  // padding heads only
       float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
