@@ -88,6 +88,9 @@ typedef enum {
 #define I8KV_FLAG_BAD_SLOT 0x8u    /* reshape_and_cache: a slot >= num_slots was skipped      */
 #define I8KV_FLAG_FP32_PATH 0x10u  /* some CTA evaluated its heads on the FP32 path (see the
                                       numerical eligibility rules below)                     */
+#define I8KV_FLAG_WAIT_TIMEOUT 0x20u /* dsa_prefill's tensor-core kernel: a CTA gave up waiting
+                                        (about a second) for its own asynchronous copies or
+                                        tensor-core products; its outputs are NaN          */
 
 /* Human-readable name of a status code (static storage). */
 const char* i8kv_status_string(int status);

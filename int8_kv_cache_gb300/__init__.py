@@ -20,7 +20,7 @@ __all__ = [
     "Int8KVError", "load", "library_path", "split_geometry", "split_workspace_bytes",
     "decode_plan", "dsa_decode", "dsa_prefill", "paged_decode", "split_combine", "int8_to_fp16",
     "dsa_decode_static_workspace", "STATIC_WORKSPACE_BYTES", "reshape_and_cache",
-    "FLAG_BAD_SLOT", "FLAG_FP32_PATH", "paged_decode_ex", "window_span",
+    "FLAG_BAD_SLOT", "FLAG_FP32_PATH", "FLAG_WAIT_TIMEOUT", "paged_decode_ex", "window_span",
     "CACHE_FP8", "fp8_to_fp16",
     "SCALE_PER_TENSOR", "SCALE_PER_CHANNEL", "CACHE_INT8", "CACHE_FP16", "GEOM_WAVE",
     "GEOM_POW2_TILES", "PATH_DSA", "PATH_PAGED", "MAX_SPLITS", "FLAG_LEN_CLAMPED",
@@ -42,6 +42,7 @@ FLAG_QUERY_RANGE = 0x2
 FLAG_BAD_BLOCK = 0x4
 FLAG_BAD_SLOT = 0x8
 FLAG_FP32_PATH = 0x10
+FLAG_WAIT_TIMEOUT = 0x20
 STATIC_WORKSPACE_BYTES = 4 * 1024 * 1024
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

@@ -340,6 +340,15 @@ i8kv_status dsa_prefill(const uint16_t* q, const int8_t* k_cache, const int8_t* 
   if (S == 0) return I8KV_OK;
   p.num_splits = 1;
   p.chunk = static_cast<int32_t>(std::max<int64_t>(16, cdiv(max_sel, 16) * 16));
+  // dense tensor-core kernel where the rows' lists cover the cache densely
+  // enough (a shape rule, so eager and captured calls choose alike), else the
+  // gathering mma.sync kernel
+  int smem = 0, mask_rows = 0;
+  if (i8kv::prefill_tc_plan(D, p.G, S, N, max_sel, &smem, &mask_rows)) {
+    cudaError_t e = i8kv::launch_dsa_prefill_tc(p, D, smem, mask_rows,
+                                                static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? I8KV_OK : cuda_fail(e);
+  }
   return run(make_key(Path::kDsa, D, p.G, I8KV_CACHE_INT8, false), p,
              static_cast<cudaStream_t>(stream));
 }

@@ -67,6 +67,13 @@ cudaError_t launch_paged_fp16(const KernelKey& key, const DecodeParams& p, cudaS
 cudaError_t launch_paged_fp8(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
                              int* occupancy);
 
+// The dense tensor-core prefill (prefill_tc.cu): whether it serves a shape
+// (and with how much shared memory / how many mask rows), and its launch.
+bool prefill_tc_plan(int D, int G, int rows, long long N, int max_sel, int* smem_bytes,
+                     int* mask_rows);
+cudaError_t launch_dsa_prefill_tc(const DecodeParams& p, int D, int smem, int mask_rows,
+                                  cudaStream_t s);
+
 cudaError_t launch_combine(const float* acc, const float* m, const float* l, int units,
                            int num_splits, int Hq, int Hkv, int D, const float* sink, void* out,
                            float* lse, cudaStream_t stream);

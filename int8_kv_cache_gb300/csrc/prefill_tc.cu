@@ -1,0 +1,725 @@
+// Tensor-core (tcgen05) sparse-candidate prefill over an INT8 cache.
+//
+// What it computes (onnxruntime PR 33707 "INT8-KV DynamicSparseAttention",
+// Summary of Changes §1: the multi-row prefill over gathered candidates, no
+// splits, the probability tile as a single FP16 tile): for every query row r
+// and query head h (KV head g = h / G),
+//   O[r, h] = sum_t e^(s_t - m) v_scale * V[t, g] / sum_t e^(s_t - m),
+//   s_t = sigma * dot(fp16(Q[r, h] * k_scale), K codes[t, g]),
+// over the valid entries t of the row's candidate list, then lse and the sink.
+//
+// Design (GB300): a prefill's rows select large overlapping subsets of one
+// cache (2048 of the first 6-8k tokens per row in the pages' workload), so the
+// kernel does not gather per row.  A CTA takes a tile of 128 query vectors of
+// one KV head (the (row, head) pairs r*G + j, consecutive, so a tile spans
+// about 128 / G rows), builds a bitmask of each of its rows' candidates in
+// shared memory, and streams the cache positions those rows select in blocks
+// of 64 contiguous tokens:
+//   S[128 x 64] = Q'[128 x D] K_block^T      tcgen05 kind::f16, M=128, N=64
+//   softmax over the block with the row's mask (a position not in the row's
+//   list gets probability 0), the probability tile p * 2^15 as fp16
+//   O[128 x D] += P[128 x 64] V_block          tcgen05 kind::f16, M=128, N=D
+// so each cache block is converted int8 -> fp16 once per tile instead of once
+// per row that selects it, and both products are real dense contractions with
+// the accumulators in tensor memory.  The cost is the masked positions'
+// products (at the pages' density of one in four, 3-4x the selected flops),
+// which the tensor cores absorb.
+//
+// Warp roles (288 threads, one CTA per SM):
+//   warps 0-3  softmax and epilogue; thread i owns query vector i of the tile
+//              (tensor-memory lane i): scores in, probabilities out, running
+//              max / sum, the O rescale when its max moves, the output row.
+//   warps 4-7  converters: load the raw int8 K and V rows of a block into
+//              registers (one block ahead), convert them exactly to fp16 core
+//              matrices in one of two buffers per operand (K as the K-major B
+//              operand of QK^T, V as the MN-major B operand of PV), signal the
+//              MMA thread.
+//   warp 8     lane 0 issues the MMAs; the warp owns the tensor memory.
+// Hand-offs are mbarriers: every wait is bounded (about a second, or at once
+// after another thread gave up); a CTA that gives up writes NaN for its
+// outputs and raises I8KV_FLAG_WAIT_TIMEOUT instead of hanging.
+//
+// The numerical rules of the other kernels hold: a query vector whose Q' is
+// out of the fp16 range or whose folding error exceeds the budget, a row whose
+// list repeats an entry (the bitmask cannot count it), a non-finite value
+// scale, or a value scale above 2^16 with a score more than 20 nats below the
+// running maximum send the vector to an FP32 CUDA-core evaluation over its
+// list (two passes, the 2^80-shifted accumulator for terms more than 80 nats
+// down), whose result replaces the tensor-core one.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <climits>
+
+#include "../../include/int8kv.h"
+#include "device.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace i8kv {
+namespace pf {
+
+constexpr int BM = 128;  // query vectors per tile (tensor-memory lanes)
+constexpr int BN = 64;   // cache positions per block
+constexpr int kSoftWarps = 4;
+constexpr int kCvtWarps = 4;
+constexpr int kMmaWarp = 8;
+constexpr int kThreads = 32 * (kSoftWarps + kCvtWarps + 1);
+constexpr int kCvtThreads = 32 * kCvtWarps;
+constexpr float kQueryBudget = 0.125f;  // nats (the decode kernels' query-folding budget)
+constexpr float kTail = 20.f;           // nats below the running maximum
+constexpr float kBigVs = 65536.f;       // |value_scale| above which the tail matters
+
+// barrier slots (8 bytes each) in the misc area
+// (buffer b of a double-buffered pair: slot + b)
+enum Bar { kKFull0, kKFull1, kVFull0, kVFull1, kKFree0, kKFree1, kVFree0, kVFree1, kSFull0,
+           kSFull1, kSFree0, kSFree1, kPFull, kPVDone, kDone, kNumBars };
+// int slots after the barriers
+enum Slot { kTmem, kAbort, kPMin, kPMax, kNumFp32, kVsBig, kVsBad, kNumSlots };
+
+template <int D>
+struct Layout {
+  static constexpr int kQBytes = BM * D * 2;        // Q' (A of QK^T), fp16 core matrices
+  static constexpr int kKVBytes = BN * D * 2;       // one fp16 K or V block
+  static constexpr int kPBytes = BM * BN * 2;       // P (A of PV)
+  static constexpr int kQ = 0;
+  static constexpr int kK16 = kQ + kQBytes;         // two K buffers
+  static constexpr int kV16 = kK16 + 2 * kKVBytes;  // two V buffers
+  static constexpr int kP = kV16 + 2 * kKVBytes;
+  static constexpr int kVs = kP + kPBytes;
+  static constexpr int kMisc = kVs + D * 4;         // barriers, ints, the FP32 vector list
+  static constexpr int kBarBytes = 128;
+  static constexpr int kSlotOff = kMisc + kBarBytes;
+  static constexpr int kListOff = kSlotOff + 64;    // BM uint16 vector indices
+  static constexpr int kMask = kListOff + 2 * BM;   // row bitmasks, block flags, row flags
+  // byte stride between 8-row groups of core matrices (8 rows x 16 bytes each)
+  static constexpr int kGroupD = (D / 8) * 128;     // rows of D fp16 values (Q', K, V)
+  static constexpr int kGroupP = (BN / 8) * 128;    // rows of BN fp16 values (P)
+  static constexpr int kOCol = 2 * BN;              // tensor-memory column of O (after S0, S1)
+  static constexpr int kTmemCols = (kOCol + D) <= 256 ? 256 : 512;
+  static_assert(kNumBars * 8 <= kBarBytes, "barriers");
+  static_assert(kNumSlots * 4 <= 64, "slots");
+};
+
+struct Args {
+  DecodeParams p;
+  int tiles_per_head;  // ceil(rows * G / 128)
+  int mask_rows;       // rows a tile can span
+  int mask_words;      // ceil(N / 32)
+  int nblocks;         // ceil(N / BN)
+};
+
+// Exact int8 -> fp16 of 16 codes (one 16-byte chunk) in channel order.
+__device__ __forceinline__ void cvt16(const uint4 raw, uint4& lo, uint4& hi) {
+  const uint32_t x0 = flip_i8x4(raw.x), x1 = flip_i8x4(raw.y);
+  const uint32_t x2 = flip_i8x4(raw.z), x3 = flip_i8x4(raw.w);
+  lo = make_uint4(i8x2_to_h2(x0, 0x4140u), i8x2_to_h2(x0, 0x4342u), i8x2_to_h2(x1, 0x4140u),
+                  i8x2_to_h2(x1, 0x4342u));
+  hi = make_uint4(i8x2_to_h2(x2, 0x4140u), i8x2_to_h2(x2, 0x4342u), i8x2_to_h2(x3, 0x4140u),
+                  i8x2_to_h2(x3, 0x4342u));
+}
+
+// The FP32 CUDA-core evaluation of one query vector over its row's list (one
+// warp; lane l holds channels l, l + 32, ...).  Two passes: the maximum, then
+// the weights; terms more than 80 nats down accumulate 2^80 larger.
+template <int D>
+__device__ __noinline__ void fp32_vector(const DecodeParams& p, int row, int h, int g,
+                                         const float* svs) {
+  constexpr int C = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long N = p.cache_rows;
+  const __half* qv = reinterpret_cast<const __half*>(p.q) + ((long long)row * p.Hq + h) * D;
+  float q32[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) {
+    const int d = lane + 32 * c;
+    q32[c] = __half2float(qv[d]) * (p.per_channel ? p.k_scale[g * D + d] : p.k_scale[0]);
+  }
+  const int32_t* list = p.idx + (long long)row * p.max_sel;
+  const int8_t* kc = reinterpret_cast<const int8_t*>(p.k);
+  const int8_t* vc = reinterpret_cast<const int8_t*>(p.v);
+  auto score = [&](long long t) -> float {
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < C; ++c)
+      acc = fmaf(q32[c], static_cast<float>(kc[(t * p.Hkv + g) * D + lane + 32 * c]), acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    return acc * p.sigma;
+  };
+  float m = neg_inf();
+  for (int j = 0; j < p.max_sel; ++j) {
+    const int t = list[j];
+    if (t >= 0 && t < N) m = fmaxf(m, score(t));
+  }
+  float l = 0.f, a[C], b[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) a[c] = b[c] = 0.f;
+  if (m != neg_inf()) {
+    for (int j = 0; j < p.max_sel; ++j) {
+      const int t = list[j];
+      if (t < 0 || t >= N) continue;
+      const float z = score(t) - m;
+      const float w = expf(z);
+      l += w;
+      if (z >= -80.f) {
+#pragma unroll
+        for (int c = 0; c < C; ++c)
+          a[c] = fmaf(w, static_cast<float>(vc[((long long)t * p.Hkv + g) * D + lane + 32 * c]),
+                      a[c]);
+      } else {
+        const float ws = exp2f(fmaf(z, kLog2e, 80.f));
+#pragma unroll
+        for (int c = 0; c < C; ++c)
+          b[c] = fmaf(ws, static_cast<float>(vc[((long long)t * p.Hkv + g) * D + lane + 32 * c]),
+                      b[c]);
+      }
+    }
+  }
+  float sc = 0.f;
+  if (l > 0.f) {
+    sc = 1.f / l;
+    if (p.sink != nullptr) sc *= 1.f / (1.f + expf(p.sink[h] - (m + logf(l))));
+  }
+  __half* o = reinterpret_cast<__half*>(p.out) + ((long long)row * p.Hq + h) * D;
+#pragma unroll
+  for (int c = 0; c < C; ++c) {
+    const int d = lane + 32 * c;
+    const float vs = svs[d];
+    o[d] = __float2half_rn(sc == 0.f ? 0.f : (a[c] * vs + b[c] * (vs * 0x1p-80f)) * sc);
+  }
+  if (lane == 0 && p.lse != nullptr)
+    p.lse[(long long)row * p.Hq + h] = l > 0.f ? m + logf(l) : neg_inf();
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
+  using L = Layout<D>;
+  const DecodeParams& p = a.p;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t sbase = smem_addr(smem);
+  auto bar = [&](int k) -> uint32_t { return sbase + L::kMisc + 8 * k; };
+  volatile int* slot = reinterpret_cast<volatile int*>(smem + L::kSlotOff);
+  int* slot_rw = reinterpret_cast<int*>(smem + L::kSlotOff);
+  uint16_t* fplist = reinterpret_cast<uint16_t*>(smem + L::kListOff);
+  float* svs = reinterpret_cast<float*>(smem + L::kVs);
+  uint32_t* mask = reinterpret_cast<uint32_t*>(smem + L::kMask);
+  uint8_t* blk_any = reinterpret_cast<uint8_t*>(mask + a.mask_rows * a.mask_words);
+  uint8_t* row_dup = blk_any + a.nblocks;
+
+  // ---------------- the tile ----------------
+  const int G = p.G, Hkv = p.Hkv;
+  const long long N = p.cache_rows;
+  const int tile = gridDim.x - 1 - blockIdx.x;  // later rows (longer causal lists) first
+  const int g = tile / a.tiles_per_head;
+  const long long nvec = (long long)p.rows * G;
+  const long long v0 = (long long)(tile - g * a.tiles_per_head) * BM;
+  const int r_lo = (int)(v0 / G);
+  const int r_hi = (int)((v0 + BM - 1 < nvec ? v0 + BM - 1 : nvec - 1) / G);
+  const int nrows = r_hi - r_lo + 1;
+
+  grid_dependency_wait();  // inputs may come from the previous kernel of the stream
+
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(sbase + L::kSlotOff + 4 * kTmem, L::kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(bar(kKFull0 + b), kCvtThreads);
+      tc::mbar_init(bar(kVFull0 + b), kCvtThreads);
+      tc::mbar_init(bar(kKFree0 + b), 1);
+      tc::mbar_init(bar(kVFree0 + b), 1);
+      tc::mbar_init(bar(kSFull0 + b), 1);
+      tc::mbar_init(bar(kSFree0 + b), 32 * kSoftWarps);
+    }
+    tc::mbar_init(bar(kPFull), 32 * kSoftWarps);
+    tc::mbar_init(bar(kPVDone), 1);
+    tc::mbar_init(bar(kDone), 1);
+    tc::fence_mbar_init();
+    slot[kAbort] = 0;
+    slot[kPMin] = INT_MAX;
+    slot[kPMax] = -1;
+    slot[kNumFp32] = 0;
+    slot[kVsBig] = 0;
+    slot[kVsBad] = 0;
+  }
+  for (int i = tid; i < nrows * a.mask_words; i += kThreads) mask[i] = 0u;
+  for (int i = tid; i < a.nblocks; i += kThreads) blk_any[i] = 0;
+  for (int i = tid; i < nrows; i += kThreads) row_dup[i] = 0;
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = static_cast<uint32_t>(slot[kTmem]);
+
+  // ---------------- the rows' candidate bitmasks ----------------
+  {
+    int lo = INT_MAX, hi = -1;
+    for (int rr = 0; rr < nrows; ++rr) {
+      const int32_t* list = p.idx + (long long)(r_lo + rr) * p.max_sel;
+      uint32_t* mrow = mask + rr * a.mask_words;
+      for (int j = tid; j < p.max_sel; j += kThreads) {
+        const int t = __ldg(list + j);
+        if (t < 0 || t >= N) continue;
+        const uint32_t bit = 1u << (t & 31);
+        if (atomicOr(mrow + (t >> 5), bit) & bit) row_dup[rr] = 1;  // a repeated entry
+        blk_any[t / BN] = 1;
+        lo = min(lo, t);
+        hi = max(hi, t);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lane == 0 && hi >= 0) {
+      atomicMin(slot_rw + kPMin, lo);
+      atomicMax(slot_rw + kPMax, hi);
+    }
+  }
+  // value scales of the KV head
+  for (int d = tid; d < D; d += kThreads) {
+    const float vs = p.per_channel ? p.v_scale[g * D + d] : p.v_scale[0];
+    svs[d] = vs;
+    if (!(fabsf(vs) <= 3.4028235e38f)) slot[kVsBad] = 1;
+    if (fabsf(vs) > kBigVs) slot[kVsBig] = 1;
+  }
+  __syncthreads();
+  const int pmax = slot[kPMax];
+  const int blo = pmax >= 0 ? slot[kPMin] / BN : 0;
+  const int bhi = pmax >= 0 ? pmax / BN : -1;
+  const bool vs_bad = slot[kVsBad] != 0;
+  const bool vs_big = slot[kVsBig] != 0;
+  // the blocks some row of the tile selects, in order: blo, next(blo), ...
+  auto next_blk = [&](int b) -> int {
+    ++b;
+    while (b <= bhi && !blk_any[b]) ++b;
+    return b;
+  };
+  const int first = (bhi >= 0 && blk_any[blo]) ? blo : next_blk(blo);
+
+  // ---------------- Q' = fp16(Q * k_scale) (softmax warps) ----------------
+  // Thread r stages its query vector as row r of the A operand: core matrix
+  // (r / 8, d / 8) holds rows r..r+7 x channels 8k..8k+7 (16 bytes per row).
+  const int r = tid;  // softmax warps: the vector of this thread
+  const long long vidx = v0 + r;
+  const bool vec_live = warp < kSoftWarps && vidx < nvec;
+  const int vrow = vec_live ? (int)(vidx / G) : r_lo;
+  const int vh = vec_live ? g * G + (int)(vidx - (long long)vrow * G) : 0;
+  bool need_fp32 = false;
+  if (warp < kSoftWarps) {
+    const __half* qrow = reinterpret_cast<const __half*>(p.q) + ((long long)vrow * p.Hq + vh) * D;
+    uint8_t* qdst = smem + L::kQ + (r >> 3) * L::kGroupD + (r & 7) * 16;
+    bool bad = false;
+    float err = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < D / 8; ++c) {
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (vec_live) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(qrow + 8 * c);
+        const __half2* qh = reinterpret_cast<const __half2*>(&raw);
+        float ks[8];
+        if (p.per_channel) {
+          const float4 k0 = *reinterpret_cast<const float4*>(p.k_scale + g * D + 8 * c);
+          const float4 k1 = *reinterpret_cast<const float4*>(p.k_scale + g * D + 8 * c + 4);
+          ks[0] = k0.x; ks[1] = k0.y; ks[2] = k0.z; ks[3] = k0.w;
+          ks[4] = k1.x; ks[5] = k1.y; ks[6] = k1.z; ks[7] = k1.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ks[e] = p.k_scale[0];
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(qh[e]);
+          const float x0 = f.x * ks[2 * e], x1 = f.y * ks[2 * e + 1];
+          bad |= !(fabsf(x0) <= 65504.f) || !(fabsf(x1) <= 65504.f);
+          o[e] = pack_h2(x0, x1);
+          const float2 rr2 = __half22float2(*reinterpret_cast<const __half2*>(&o[e]));
+          err += fabsf(x0 - rr2.x) + fabsf(x1 - rr2.y);
+        }
+        w = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      *reinterpret_cast<uint4*>(qdst + c * 128) = w;
+    }
+    if (vec_live) {
+      if (bad) flag_or(p.flags, I8KV_FLAG_QUERY_RANGE);
+      need_fp32 = bad || p.sigma * 128.f * err > kQueryBudget || vs_bad || row_dup[vrow - r_lo];
+    }
+    tc::fence_smem_to_async();  // Q' is read by the tensor core
+  }
+  // a tile with nothing for the tensor cores (no selected block, or every
+  // value scale unusable) skips the pipeline
+  const bool run_tc = first <= bhi && !vs_bad;
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+
+  // ---------------- the pipeline ----------------
+  if (run_tc) {
+    if (warp >= kSoftWarps && warp < kSoftWarps + kCvtWarps) {
+      // ---- converters ----
+      // Thread ct owns 32-byte pieces (row pr, channels 32cp .. 32cp + 31) of
+      // every block's K and V: q = ct + 128k -> pr = q % BN, cp = q / BN, so
+      // the lanes of a warp take consecutive rows (conflict-free core-matrix
+      // stores).  Its pieces of the next block are loaded into registers while
+      // the tensor cores work on the current ones.
+      const int ct = tid - 32 * kSoftWarps;
+      constexpr int kPairs = BN * D / 32 / kCvtThreads;
+      const int8_t* kc = reinterpret_cast<const int8_t*>(p.k);
+      const int8_t* vc = reinterpret_cast<const int8_t*>(p.v);
+      uint4 kr[kPairs][2], vr[kPairs][2];
+      auto load = [&](const int8_t* base, int blk, uint4 (&dst)[kPairs][2]) {
+#pragma unroll
+        for (int k = 0; k < kPairs; ++k) {
+          const int q = ct + kCvtThreads * k;
+          const long long pos = (long long)blk * BN + q % BN;
+          if (pos < N) {
+            const uint4* src =
+                reinterpret_cast<const uint4*>(base + (pos * Hkv + g) * D + 32 * (q / BN));
+            dst[k][0] = __ldg(src);
+            dst[k][1] = __ldg(src + 1);
+          } else {
+            dst[k][0] = dst[k][1] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      };
+      auto convert = [&](const uint4 (&src)[kPairs][2], uint32_t dst16) {
+#pragma unroll
+        for (int k = 0; k < kPairs; ++k) {
+          const int q = ct + kCvtThreads * k;
+          const int pr = q % BN, cp = q / BN;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint4 lo, hi;
+            cvt16(src[k][hh], lo, hi);
+            // channels 32cp + 16hh .. +15 -> core matrices (pr / 8, 4cp + 2hh [+1])
+            const uint32_t a = dst16 + (pr >> 3) * L::kGroupD + (pr & 7) * 16 +
+                               (4 * cp + 2 * hh) * 128;
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(a), "r"(lo.x),
+                         "r"(lo.y), "r"(lo.z), "r"(lo.w)
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(a + 128), "r"(hi.x),
+                         "r"(hi.y), "r"(hi.z), "r"(hi.w)
+                         : "memory");
+          }
+        }
+      };
+      load(kc, first, kr);
+      load(vc, first, vr);
+      int i = 0;
+      for (int blk = first; blk <= bhi; ++i) {
+        const int nxt = next_blk(blk);
+        const int b = i & 1;
+        // buffer b is free once the products of block i - 2 have read it
+        if (!tc::mbar_wait(bar(kKFree0 + b), ((i >> 1) & 1) ^ 1, slot)) {
+          slot[kAbort] = 1;
+          break;
+        }
+        convert(kr, sbase + L::kK16 + b * L::kKVBytes);
+        tc::fence_smem_to_async();
+        tc::mbar_arrive(bar(kKFull0 + b));
+        if (nxt <= bhi) load(kc, nxt, kr);
+        if (!tc::mbar_wait(bar(kVFree0 + b), ((i >> 1) & 1) ^ 1, slot)) {
+          slot[kAbort] = 1;
+          break;
+        }
+        convert(vr, sbase + L::kV16 + b * L::kKVBytes);
+        tc::fence_smem_to_async();
+        tc::mbar_arrive(bar(kVFull0 + b));
+        if (nxt <= bhi) load(vc, nxt, vr);
+        blk = nxt;
+      }
+    } else if (warp == kMmaWarp) {
+      // ---- MMA issue (one thread) ----
+      // order: QK(0), QK(1), PV(0), QK(2), PV(1), ...: the scores of block
+      // i + 1 are computed while the softmax works on block i
+      if (lane == 0) {
+        constexpr uint32_t kIdQK = tc::idesc_f16(BM, BN, false, false);
+        constexpr uint32_t kIdPV = tc::idesc_f16(BM, D, false, true);
+        const uint32_t q_s = sbase + L::kQ, p_s = sbase + L::kP;
+        auto pv = [&](int j) -> bool {
+          const int b = j & 1;
+          if (!tc::mbar_wait(bar(kPFull), j & 1, slot)) return false;
+          if (!tc::mbar_wait(bar(kVFull0 + b), (j >> 1) & 1, slot)) return false;
+          tc::fence_after_sync();
+          const uint32_t v_s = sbase + L::kV16 + b * L::kKVBytes;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            // A = P (K-major: M = vectors, K = positions), B = V (MN-major:
+            // K = positions, N = channels)
+            const uint64_t ad = tc::smem_desc(p_s + kk * 256, 128, L::kGroupP);
+            const uint64_t bd = tc::smem_desc(v_s + kk * 2 * L::kGroupD, L::kGroupD, 128);
+            tc::mma_f16(tbase + L::kOCol, ad, bd, kIdPV, j > 0 || kk > 0);
+          }
+          tc::mma_commit(bar(kVFree0 + b));
+          tc::mma_commit(bar(kPVDone));
+          return true;
+        };
+        int i = 0;
+        bool ok = true;
+        for (int blk = first; blk <= bhi; blk = next_blk(blk), ++i) {
+          const int b = i & 1;
+          ok = tc::mbar_wait(bar(kKFull0 + b), (i >> 1) & 1, slot) &&
+               tc::mbar_wait(bar(kSFree0 + b), ((i >> 1) & 1) ^ 1, slot);
+          if (!ok) break;
+          tc::fence_after_sync();
+          const uint32_t k_s = sbase + L::kK16 + b * L::kKVBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            // A = Q' (K-major: M = vectors, K = channels), B = K (K-major:
+            // N = positions, K = channels)
+            const uint64_t ad = tc::smem_desc(q_s + kk * 256, 128, L::kGroupD);
+            const uint64_t bd = tc::smem_desc(k_s + kk * 256, 128, L::kGroupD);
+            tc::mma_f16(tbase + b * BN, ad, bd, kIdQK, kk > 0);
+          }
+          tc::mma_commit(bar(kSFull0 + b));
+          tc::mma_commit(bar(kKFree0 + b));
+          if (i > 0 && !(ok = pv(i - 1))) break;
+        }
+        if (ok && i > 0) ok = pv(i - 1);
+        if (!ok) slot[kAbort] = 1;
+        // everything issued has completed before the tensor memory is released
+        tc::mma_commit(bar(kDone));
+        if (!tc::mbar_wait(bar(kDone), 0)) slot[kAbort] = 1;
+      }
+      __syncwarp();
+    } else {
+      // ---- softmax (one query vector per thread) ----
+      const uint32_t t_lane = (uint32_t)(32 * warp) << 16;
+      const uint32_t* mrow = mask + (vrow - r_lo) * a.mask_words;
+      const float sigma = p.sigma;
+      float m_run = neg_inf(), l_run = 0.f;
+      bool deep = false, loop_ok = true;
+      // the warp's lanes take every decision together (tcgen05.ld / st are
+      // warp-collective)
+      auto wait_all = [&](int b, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, tc::mbar_wait(bar(b), parity, slot));
+      };
+      int i = 0;
+      for (int blk = first; blk <= bhi; blk = next_blk(blk), ++i) {
+        if (!wait_all(kSFull0 + (i & 1), (i >> 1) & 1)) {
+          loop_ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        float s[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 16; ++c) {
+          float v16[16];
+          tc::tmem_ld16(tbase + t_lane + (i & 1) * BN + 16 * c, v16);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) s[16 * c + e] = v16[e];
+        }
+        tc::tmem_wait_ld();
+        tc::fence_before_sync();
+        tc::mbar_arrive(bar(kSFree0 + (i & 1)));
+        // the row's selection of positions blk*64 .. blk*64+63
+        const uint32_t w0 = vec_live ? mrow[2 * blk] : 0u;
+        const uint32_t w1 = vec_live && 2 * blk + 1 < a.mask_words ? mrow[2 * blk + 1] : 0u;
+        float mx = neg_inf();
+#pragma unroll
+        for (int j = 0; j < BN; ++j) {
+          const bool sel = ((j < 32 ? w0 >> j : w1 >> (j - 32)) & 1u) != 0u;
+          s[j] = sel ? s[j] * sigma : neg_inf();
+          mx = fmaxf(mx, s[j]);
+        }
+        const float m_new = fmaxf(m_run, mx);
+        const float base = m_new == neg_inf() ? 0.f : m_new;
+        if (vs_big) {
+#pragma unroll
+          for (int j = 0; j < BN; ++j) deep |= s[j] != neg_inf() && s[j] < m_new - kTail;
+        }
+        const float alpha = fast_exp2((m_run - base) * kLog2e);
+        float ps = 0.f;
+        uint32_t ph[BN / 2];
+#pragma unroll
+        for (int j = 0; j < BN / 2; ++j) {
+          const float p0 = fast_exp2((s[2 * j] - base) * kLog2e);
+          const float p1 = fast_exp2((s[2 * j + 1] - base) * kLog2e);
+          ps += p0 + p1;
+          ph[j] = pack_h2(p0 * kProbScale, p1 * kProbScale);
+        }
+        l_run = l_run * alpha + ps;
+        const bool rescale = i > 0 && m_new != m_run;
+        m_run = m_new;
+        // P's buffer and O are free once the previous block's PV has completed
+        if (i > 0 && !wait_all(kPVDone, (i - 1) & 1)) {
+          loop_ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float f = rescale ? alpha : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tc::tmem_ld32(tbase + t_lane + L::kOCol + 32 * c, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= f;
+            tc::tmem_st32(tbase + t_lane + L::kOCol + 32 * c, o);
+          }
+          tc::tmem_wait_st();
+        }
+        // row r of P: core matrix (r / 8, k) holds positions 8k..8k+7
+        uint8_t* pdst = smem + L::kP + (r >> 3) * L::kGroupP + (r & 7) * 16;
+#pragma unroll
+        for (int k = 0; k < BN / 8; ++k)
+          *reinterpret_cast<uint4*>(pdst + k * 128) =
+              make_uint4(ph[4 * k], ph[4 * k + 1], ph[4 * k + 2], ph[4 * k + 3]);
+        tc::fence_smem_to_async();
+        tc::fence_before_sync();
+        tc::mbar_arrive(bar(kPFull));
+      }
+      // ---- epilogue: O / l, the sink, lse ----
+      const bool ok = __all_sync(0xffffffffu, loop_ok && !slot[kAbort]) &&
+                      (i == 0 || wait_all(kPVDone, (i - 1) & 1));
+      tc::fence_after_sync();
+      need_fp32 |= vec_live && vs_big && deep;
+      const bool write = vec_live && !need_fp32;
+      float sc = 0.f;
+      const float lse_v = l_run > 0.f ? m_run + logf(l_run) : neg_inf();
+      if (l_run > 0.f) {
+        sc = kInvProbScale / l_run;
+        if (p.sink != nullptr) sc *= 1.f / (1.f + expf(p.sink[vh] - lse_v));
+      }
+      __half* orow = reinterpret_cast<__half*>(p.out) + ((long long)vrow * p.Hq + vh) * D;
+      if (ok && i > 0) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tc::tmem_ld32(tbase + t_lane + L::kOCol + 32 * c, o);
+          tc::tmem_wait_ld();
+          if (write) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint32_t h[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int d = 32 * c + 8 * u + 2 * e;
+                h[e] = pack_h2(o[8 * u + 2 * e] * sc * svs[d], o[8 * u + 2 * e + 1] * sc * svs[d + 1]);
+              }
+              *reinterpret_cast<uint4*>(orow + 32 * c + 8 * u) = make_uint4(h[0], h[1], h[2], h[3]);
+            }
+          }
+        }
+      } else if (ok && write) {  // no selected block: O = 0
+        for (int c = 0; c < D / 8; ++c)
+          *reinterpret_cast<uint4*>(orow + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (ok && write && p.lse != nullptr) p.lse[(long long)vrow * p.Hq + vh] = lse_v;
+      if (!ok) slot[kAbort] = 1;
+      tc::fence_before_sync();
+    }
+  } else if (warp < kSoftWarps && vec_live && !need_fp32) {
+    // no tensor-core work: every position of the tile is unselected
+    __half* orow = reinterpret_cast<__half*>(p.out) + ((long long)vrow * p.Hq + vh) * D;
+    for (int c = 0; c < D / 8; ++c)
+      *reinterpret_cast<uint4*>(orow + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
+    if (p.lse != nullptr) p.lse[(long long)vrow * p.Hq + vh] = neg_inf();
+  }
+  if (need_fp32) {
+    const int k = atomicAdd(slot_rw + kNumFp32, 1);
+    fplist[k] = (uint16_t)r;
+  }
+  __syncthreads();
+
+  const bool aborted = slot[kAbort] != 0;
+  if (aborted) {
+    // the CTA gave up waiting: its outputs are marked invalid
+    if (tid == 0) flag_or(p.flags, I8KV_FLAG_WAIT_TIMEOUT);
+    if (warp < kSoftWarps && vec_live) {
+      __half* orow = reinterpret_cast<__half*>(p.out) + ((long long)vrow * p.Hq + vh) * D;
+      for (int d = 0; d < D; ++d) orow[d] = __ushort_as_half(0x7E00);
+      if (p.lse != nullptr) p.lse[(long long)vrow * p.Hq + vh] = __int_as_float(0x7FC00000);
+    }
+  } else {
+    // ---------------- the FP32 vectors (every warp takes its share) ----------------
+    const int nfp = slot[kNumFp32];
+    if (nfp > 0 && tid == 0) flag_or(p.flags, I8KV_FLAG_FP32_PATH);
+    for (int k = warp; k < nfp; k += kThreads / 32) {
+      const long long v = v0 + fplist[k];
+      const int row = (int)(v / G);
+      fp32_vector<D>(p, row, g * G + (int)(v - (long long)row * G), g, svs);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tbase, L::kTmemCols);
+  }
+}
+
+}  // namespace pf
+
+// Whether the dense tensor-core prefill serves a shape, and its shared memory.
+// It does when head_dim is 128 or 256, the lists are long enough against the
+// cache for the dense blocks to pay (4 * max_sel >= N: the masked products
+// are at most three times the selected ones), and a tile's row bitmasks fit
+// in shared memory.
+bool prefill_tc_plan(int D, int G, int rows, long long N, int max_sel, int* smem_bytes,
+                     int* mask_rows) {
+  if (D != 128 && D != 256) return false;
+  if (rows < 1 || N < 1 || max_sel < 1 || N > INT32_MAX / 2) return false;
+  if (4LL * max_sel < N) return false;
+  const long long mr = std::min<long long>(127 / G + 2, rows);
+  const long long words = (N + 31) / 32;
+  const long long nblocks = (N + pf::BN - 1) / pf::BN;
+  const long long mask = ((mr * words * 4 + nblocks + mr) + 15) / 16 * 16;
+  const long long base = D == 256 ? pf::Layout<256>::kMask : pf::Layout<128>::kMask;
+  const long long total = base + mask;
+  if (total > 227 * 1024) return false;
+  *smem_bytes = (int)total;
+  *mask_rows = (int)mr;
+  return true;
+}
+
+template <int D>
+static cudaError_t run_prefill_tc(const pf::Args& a, int smem, int tiles, cudaStream_t s) {
+  auto kern = pf::prefill_tc_kernel<D>;
+  static std::atomic<unsigned long long> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(done.load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    done.fetch_or(bit);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)tiles);
+  cfg.blockDim = dim3(pf::kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+cudaError_t launch_dsa_prefill_tc(const DecodeParams& p, int D, int smem, int mask_rows,
+                                  cudaStream_t s) {
+  pf::Args a;
+  a.p = p;
+  const long long nvec = (long long)p.rows * p.G;
+  a.tiles_per_head = (int)((nvec + pf::BM - 1) / pf::BM);
+  a.mask_rows = mask_rows;
+  a.mask_words = (int)((p.cache_rows + 31) / 32);
+  a.nblocks = (int)((p.cache_rows + pf::BN - 1) / pf::BN);
+  const long long tiles = (long long)a.tiles_per_head * p.Hkv;
+  if (tiles > INT32_MAX) return cudaErrorInvalidValue;
+  return D == 256 ? run_prefill_tc<256>(a, smem, (int)tiles, s)
+                  : run_prefill_tc<128>(a, smem, (int)tiles, s);
+}
+
+}  // namespace i8kv

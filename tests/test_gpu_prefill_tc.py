@@ -1,0 +1,93 @@
+"""The dense tensor-core prefill (dsa_prefill for head_dim 128 / 256 when the
+rows' lists cover the cache densely enough) against the FP64 oracle, on the
+cases its design has to get right: unsorted lists with invalid entries, lists
+that repeat an entry (those rows go to the FP32 path), empty rows, a last tile
+only partly filled with query vectors, one query head per KV head (tiles that
+span 128 rows), per-tensor scales, the head sink, and a large value scale with
+a deep candidate.  The full-size workload is covered by test_gpu_full_size."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from helpers import (assert_close_oracle, assert_lse_close, assert_lse_oracle, lse_bound,
+                     oracle_dsa, run_dsa)
+
+pytestmark = pytest.mark.gpu
+
+FP32_PATH = 0x10
+WAIT_TIMEOUT = 0x20
+
+
+def bound_of(c):
+    """lse tolerance against the oracle: the query-rounding bound per head."""
+    return lse_bound(c.q, c.k_scale, c.scale_kind, c.k_codes.shape[1], c.sigma)
+
+
+def _flags():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def _run(c):
+    f = _flags()
+    o, l = run_dsa(c, prefill=True, flags=f)
+    return o, l, int(f.item())
+
+
+@pytest.mark.parametrize("S,Hq,Hkv,D,N,max_sel,kind", [
+    (37, 24, 2, 256, 700, 400, W.SCALE_PER_CHANNEL),   # 444 vectors per KV head: partial tile
+    (20, 8, 2, 128, 1000, 300, W.SCALE_PER_TENSOR),
+    (3, 2, 2, 256, 500, 200, W.SCALE_PER_CHANNEL),     # G = 1: a tile spans 128 rows
+    (130, 1, 1, 128, 256, 64, W.SCALE_PER_CHANNEL),    # G = 1, two tiles
+])
+def test_unsorted_lists_with_invalid_entries(S, Hq, Hkv, D, N, max_sel, kind):
+    c = W.random_sparse(seed=S * 7 + D, S=S, Hq=Hq, Hkv=Hkv, D=D, N=N, max_sel=max_sel,
+                        invalid_frac=0.15, scale_kind=kind, sink=True, sigma=1.0 / 16)
+    ref_o, ref_l = oracle_dsa(c)
+    o, l, f = _run(c)
+    assert not f & WAIT_TIMEOUT
+    assert_close_oracle(o, ref_o, "dense prefill")
+    assert_lse_oracle(l, ref_l, bound_of(c))
+
+
+def test_repeated_entries_and_empty_rows():
+    c = W.random_sparse(seed=11, S=24, Hq=24, Hkv=2, D=256, N=600, max_sel=256, sink=True,
+                        sigma=1.0 / 16)
+    c.idx[3, 10:20] = c.idx[3, 0:10]        # row 3 lists ten candidates twice
+    c.idx[7, 100] = c.idx[7, 5]             # row 7 one candidate twice
+    c.idx[12, :] = -1                       # row 12 attends nothing
+    c.idx[13, :] = 600 + np.arange(256)     # row 13: every entry out of range
+    ref_o, ref_l = oracle_dsa(c)
+    o, l, f = _run(c)
+    assert f & FP32_PATH                     # the repeating rows took the FP32 path
+    assert not f & WAIT_TIMEOUT
+    assert_close_oracle(o, ref_o, "repeated entries")
+    assert np.all(o[12] == 0) and np.all(np.isneginf(l[12]))
+    assert np.all(o[13] == 0) and np.all(np.isneginf(l[13]))
+    assert_lse_close(l, ref_l, 1e-4)
+
+
+def test_matches_the_decode_kernel_on_the_same_rows():
+    # the prefill's dense kernel and the decode kernel (one split) compute the
+    # same quantity with different tensor-core paths
+    c = W.random_sparse(seed=12, S=40, Hq=24, Hkv=2, D=256, N=1024, max_sel=512,
+                        sorted_lists=True, sigma=1.0 / 16)
+    o, l, _ = _run(c)
+    od, ld = run_dsa(c, num_splits=1, chunk=512)
+    assert np.all(np.abs(o - od) <= 2e-3 + 1e-2 * np.abs(od))
+    assert_lse_close(l, ld, 1e-4)
+
+
+@pytest.mark.parametrize("q0,vs,fp32", [(336.0, 2.0 ** 28, True), (320.0, 2.0 ** 28, False)])
+def test_tail_depth_rule(q0, vs, fp32):
+    """A candidate 21 nats below the maximum under a value scale of 2^28 goes to
+    the FP32 path; exactly 20 nats down stays on the tensor cores."""
+    c = W.tiny_probability_case(q0, 1, vs, D=128)
+    c.q = np.concatenate([c.q] * 2, axis=1)  # 8 query heads over 2 KV heads
+    c.k_codes = np.concatenate([c.k_codes] * 2, axis=1)
+    c.v_codes = np.concatenate([c.v_codes] * 2, axis=1)
+    ref_o, ref_l = oracle_dsa(c)
+    o, l, f = _run(c)
+    assert bool(f & FP32_PATH) == fp32
+    assert np.all(np.abs(o - ref_o) <= 2e-3 + 1e-2 * np.abs(ref_o))
+    assert_lse_close(l, ref_l, 1e-5)
