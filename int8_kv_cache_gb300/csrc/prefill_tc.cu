@@ -81,7 +81,7 @@ enum Slot { kTmem, kAbort, kPMin, kPMax, kNumFp32, kVsBig, kVsBad, kNumSlots };
 
 template <int D>
 struct Layout {
-  static constexpr int kQBytes = BM * D * 2;        // Q' (A of QK^T), fp16 core matrices
+  static constexpr int kQBytes = BM * D * 2;        // Q' (A of QK^T), fp16
   static constexpr int kKVBytes = BN * D * 2;       // one fp16 K or V block
   static constexpr int kPBytes = BM * BN * 2;       // P (A of PV)
   static constexpr int kQ = 0;
@@ -94,12 +94,18 @@ struct Layout {
   static constexpr int kSlotOff = kMisc + kBarBytes;
   static constexpr int kListOff = kSlotOff + 64;    // BM uint16 vector indices
   static constexpr int kMask = kListOff + 2 * BM;   // row bitmasks, block flags, row flags
-  // byte stride between 8-row groups of core matrices (8 rows x 16 bytes each)
-  static constexpr int kGroupD = (D / 8) * 128;     // rows of D fp16 values (Q', K, V)
-  static constexpr int kGroupP = (BN / 8) * 128;    // rows of BN fp16 values (P)
+  // Q', K and P use the 128-byte swizzled K-major layout: slabs of 64 values
+  // (128-byte rows, chunks XOR-permuted by row mod 8) over all rows of the
+  // operand, one slab after the other along K
+  static constexpr int kSlabQ = BM * 128;           // one 64-channel slab of Q'
+  static constexpr int kSlabK = BN * 128;           // one 64-channel slab of a K block
+  // V (the MN-major B of PV) uses plain core matrices (8 positions x 16
+  // bytes): byte stride between 8-position groups
+  static constexpr int kGroupD = (D / 8) * 128;
   static constexpr int kOCol = 2 * BN;              // tensor-memory column of O (after S0, S1)
   static constexpr int kTmemCols = (kOCol + D) <= 256 ? 256 : 512;
   static_assert(kNumBars * 8 <= kBarBytes, "barriers");
+  static_assert(kK16 % 1024 == 0 && kP % 1024 == 0, "swizzle atoms are 1024-byte aligned");
   static_assert(kNumSlots * 4 <= 64, "slots");
 };
 
@@ -241,7 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
     tc::mbar_init(bar(kPVDone), 1);
     tc::mbar_init(bar(kDone), 1);
     tc::fence_mbar_init();
-    slot[kAbort] = 0;
+    // the swizzled operand layouts need 1024-byte aligned buffers
+    slot[kAbort] = (sbase & 1023u) != 0u;
     slot[kPMin] = INT_MAX;
     slot[kPMax] = -1;
     slot[kNumFp32] = 0;
@@ -304,8 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
   const int first = (bhi >= 0 && blk_any[blo]) ? blo : next_blk(blo);
 
   // ---------------- Q' = fp16(Q * k_scale) (softmax warps) ----------------
-  // Thread r stages its query vector as row r of the A operand: core matrix
-  // (r / 8, d / 8) holds rows r..r+7 x channels 8k..8k+7 (16 bytes per row).
+  // Thread r stages its query vector as row r of the A operand: channels
+  // 8c..8c+7 go to slab c / 8, row r, chunk (c % 8) ^ (r % 8).
   const int r = tid;  // softmax warps: the vector of this thread
   const long long vidx = v0 + r;
   const bool vec_live = warp < kSoftWarps && vidx < nvec;
@@ -314,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
   bool need_fp32 = false;
   if (warp < kSoftWarps) {
     const __half* qrow = reinterpret_cast<const __half*>(p.q) + ((long long)vrow * p.Hq + vh) * D;
-    uint8_t* qdst = smem + L::kQ + (r >> 3) * L::kGroupD + (r & 7) * 16;
+    uint8_t* qdst = smem + L::kQ + r * 128;
     bool bad = false;
     float err = 0.f;
 #pragma unroll 4
@@ -345,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
         }
         w = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      *reinterpret_cast<uint4*>(qdst + c * 128) = w;
+      *reinterpret_cast<uint4*>(qdst + (c >> 3) * L::kSlabQ + (((c & 7) ^ (r & 7)) << 4)) = w;
     }
     if (vec_live) {
       if (bad) flag_or(p.flags, I8KV_FLAG_QUERY_RANGE);
@@ -389,7 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
           }
         }
       };
-      auto convert = [&](const uint4 (&src)[kPairs][2], uint32_t dst16) {
+      // swz: K (128-byte swizzled slabs); else V (plain core matrices)
+      auto convert = [&](const uint4 (&src)[kPairs][2], uint32_t dst16, bool swz) {
 #pragma unroll
         for (int k = 0; k < kPairs; ++k) {
           const int q = ct + kCvtThreads * k;
@@ -398,13 +406,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
           for (int hh = 0; hh < 2; ++hh) {
             uint4 lo, hi;
             cvt16(src[k][hh], lo, hi);
-            // channels 32cp + 16hh .. +15 -> core matrices (pr / 8, 4cp + 2hh [+1])
-            const uint32_t a = dst16 + (pr >> 3) * L::kGroupD + (pr & 7) * 16 +
-                               (4 * cp + 2 * hh) * 128;
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(a), "r"(lo.x),
+            // channels 32cp + 16hh .. +15: 16-byte chunks c0 = 4cp + 2hh and c0 + 1
+            const int c0 = 4 * cp + 2 * hh;
+            uint32_t a0, a1;
+            if (swz) {
+              const uint32_t row = dst16 + (c0 >> 3) * L::kSlabK + pr * 128;
+              a0 = row + (((c0 & 7) ^ (pr & 7)) << 4);
+              a1 = row + ((((c0 + 1) & 7) ^ (pr & 7)) << 4);
+            } else {
+              a0 = dst16 + (pr >> 3) * L::kGroupD + (pr & 7) * 16 + c0 * 128;
+              a1 = a0 + 128;
+            }
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(a0), "r"(lo.x),
                          "r"(lo.y), "r"(lo.z), "r"(lo.w)
                          : "memory");
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(a + 128), "r"(hi.x),
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(a1), "r"(hi.x),
                          "r"(hi.y), "r"(hi.z), "r"(hi.w)
                          : "memory");
           }
@@ -421,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
           slot[kAbort] = 1;
           break;
         }
-        convert(kr, sbase + L::kK16 + b * L::kKVBytes);
+        convert(kr, sbase + L::kK16 + b * L::kKVBytes, true);
         tc::fence_smem_to_async();
         tc::mbar_arrive(bar(kKFull0 + b));
         if (nxt <= bhi) load(kc, nxt, kr);
@@ -429,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
           slot[kAbort] = 1;
           break;
         }
-        convert(vr, sbase + L::kV16 + b * L::kKVBytes);
+        convert(vr, sbase + L::kV16 + b * L::kKVBytes, false);
         tc::fence_smem_to_async();
         tc::mbar_arrive(bar(kVFull0 + b));
         if (nxt <= bhi) load(vc, nxt, vr);
@@ -453,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
           for (int kk = 0; kk < BN / 16; ++kk) {
             // A = P (K-major: M = vectors, K = positions), B = V (MN-major:
             // K = positions, N = channels)
-            const uint64_t ad = tc::smem_desc(p_s + kk * 256, 128, L::kGroupP);
+            const uint64_t ad = tc::smem_desc_sw128(p_s + kk * 32, 1024);
             const uint64_t bd = tc::smem_desc(v_s + kk * 2 * L::kGroupD, L::kGroupD, 128);
             tc::mma_f16(tbase + L::kOCol, ad, bd, kIdPV, j > 0 || kk > 0);
           }
@@ -474,8 +490,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
           for (int kk = 0; kk < D / 16; ++kk) {
             // A = Q' (K-major: M = vectors, K = channels), B = K (K-major:
             // N = positions, K = channels)
-            const uint64_t ad = tc::smem_desc(q_s + kk * 256, 128, L::kGroupD);
-            const uint64_t bd = tc::smem_desc(k_s + kk * 256, 128, L::kGroupD);
+            const uint32_t koff = (kk & 3) * 32;  // K step inside a 64-channel slab
+            const uint64_t ad = tc::smem_desc_sw128(q_s + (kk >> 2) * L::kSlabQ + koff, 1024);
+            const uint64_t bd = tc::smem_desc_sw128(k_s + (kk >> 2) * L::kSlabK + koff, 1024);
             tc::mma_f16(tbase + b * BN, ad, bd, kIdQK, kk > 0);
           }
           tc::mma_commit(bar(kSFull0 + b));
@@ -567,11 +584,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
           }
           tc::tmem_wait_st();
         }
-        // row r of P: core matrix (r / 8, k) holds positions 8k..8k+7
-        uint8_t* pdst = smem + L::kP + (r >> 3) * L::kGroupP + (r & 7) * 16;
+        // row r of P (one 128-byte swizzled slab): positions 8k..8k+7 in
+        // chunk k ^ (r % 8)
+        uint8_t* pdst = smem + L::kP + r * 128;
 #pragma unroll
         for (int k = 0; k < BN / 8; ++k)
-          *reinterpret_cast<uint4*>(pdst + k * 128) =
+          *reinterpret_cast<uint4*>(pdst + ((k ^ (r & 7)) << 4)) =
               make_uint4(ph[4 * k], ph[4 * k + 1], ph[4 * k + 2], ph[4 * k + 3]);
         tc::fence_smem_to_async();
         tc::fence_before_sync();

@@ -203,6 +203,21 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
+// Shared-memory matrix descriptor, 128-byte swizzle, K-major: rows of 64
+// 16-bit values (128 bytes) whose 16-byte chunks are XOR-permuted by the row
+// index mod 8, 8-row atoms of 1024 bytes (1024-byte aligned) at SBO; a K step
+// inside the 128-byte row advances the start address (the swizzle applies to
+// the address bits), so the leading-dimension offset is unused.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;  // LBO (unused by this layout)
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;  // layout type: 128-byte swizzle
+  return d;
+}
+
 // Instruction descriptor of kind::f16: fp16 A and B, fp32 D, dense, M x N.
 // a_mn / b_mn select the MN-major (transposed) form of each operand.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
