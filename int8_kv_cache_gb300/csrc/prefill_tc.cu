@@ -14,11 +14,13 @@
 // one KV head (the (row, head) pairs r*G + j, consecutive, so a tile spans
 // about 128 / G rows), builds a bitmask of each of its rows' candidates in
 // shared memory, and streams the cache positions those rows select in blocks
-// of 64 contiguous tokens:
-//   S[128 x 64] = Q'[128 x D] K_block^T      tcgen05 kind::f16, M=128, N=64
+// of 128 contiguous tokens:
+//   S[128 x 128] = Q'[128 x D] K_block^T     tcgen05 kind::f16, M=128, N=128
 //   softmax over the block with the row's mask (a position not in the row's
-//   list gets probability 0), the probability tile p * 2^15 as fp16
-//   O[128 x D] += P[128 x 64] V_block          tcgen05 kind::f16, M=128, N=D
+//   list gets probability 0), the probability tile p * 2^15 as fp16, written
+//   back into tensor memory over the block's scores
+//   O[128 x D] += P[128 x 128] V_block         tcgen05 kind::f16, M=128, N=D,
+//                                            P from tensor memory
 // so each cache block is converted int8 -> fp16 once per tile instead of once
 // per row that selects it, and both products are real dense contractions with
 // the accumulators in tensor memory.  The cost is the masked positions'
@@ -30,10 +32,12 @@
 //              (tensor-memory lane i): scores in, probabilities out, running
 //              max / sum, the O rescale when its max moves, the output row.
 //   warps 4-7  converters: load the raw int8 K and V rows of a block into
-//              registers (one block ahead), convert them exactly to fp16 core
-//              matrices in one of two buffers per operand (K as the K-major B
-//              operand of QK^T, V as the MN-major B operand of PV), signal the
-//              MMA thread.
+//              registers (one block ahead), convert them exactly to fp16 (K as
+//              the K-major B operand of QK^T, V as the MN-major B operand of
+//              PV), signal the MMA thread.
+// (An MMA instruction costs the same up to N = 128 columns and about twice as
+// much at N = 256, measured on this part: 128-token blocks keep QK^T at N=128
+// instead of wasting half of every instruction at N = 64.)
 //   warp 8     lane 0 issues the MMAs; the warp owns the tensor memory.
 // Hand-offs are mbarriers: every wait is bounded (about a second, or at once
 // after another thread gave up); a CTA that gives up writes NaN for its
@@ -62,7 +66,7 @@ namespace i8kv {
 namespace pf {
 
 constexpr int BM = 128;  // query vectors per tile (tensor-memory lanes)
-constexpr int BN = 64;   // cache positions per block
+constexpr int BN = 128;  // cache positions per block
 constexpr int kSoftWarps = 4;
 constexpr int kCvtWarps = 4;
 constexpr int kMmaWarp = 8;
@@ -74,8 +78,7 @@ constexpr float kBigVs = 65536.f;       // |value_scale| above which the tail ma
 
 // barrier slots (8 bytes each) in the misc area
 // (buffer b of a double-buffered pair: slot + b)
-enum Bar { kKFull0, kKFull1, kVFull0, kVFull1, kKFree0, kKFree1, kVFree0, kVFree1, kSFull0,
-           kSFull1, kSFree0, kSFree1, kPFull, kPVDone, kDone, kNumBars };
+enum Bar { kKFull, kKFree, kVFull, kSFull0, kSFull1, kPFull, kPVDone, kDone, kNumBars };
 // int slots after the barriers
 enum Slot { kTmem, kAbort, kPMin, kPMax, kNumFp32, kVsBig, kVsBad, kNumSlots };
 
@@ -83,18 +86,16 @@ template <int D>
 struct Layout {
   static constexpr int kQBytes = BM * D * 2;        // Q' (A of QK^T), fp16
   static constexpr int kKVBytes = BN * D * 2;       // one fp16 K or V block
-  static constexpr int kPBytes = BM * BN * 2;       // P (A of PV)
   static constexpr int kQ = 0;
-  static constexpr int kK16 = kQ + kQBytes;         // two K buffers
-  static constexpr int kV16 = kK16 + 2 * kKVBytes;  // two V buffers
-  static constexpr int kP = kV16 + 2 * kKVBytes;
-  static constexpr int kVs = kP + kPBytes;
+  static constexpr int kK16 = kQ + kQBytes;
+  static constexpr int kV16 = kK16 + kKVBytes;
+  static constexpr int kVs = kV16 + kKVBytes;
   static constexpr int kMisc = kVs + D * 4;         // barriers, ints, the FP32 vector list
   static constexpr int kBarBytes = 128;
   static constexpr int kSlotOff = kMisc + kBarBytes;
   static constexpr int kListOff = kSlotOff + 64;    // BM uint16 vector indices
   static constexpr int kMask = kListOff + 2 * BM;   // row bitmasks, block flags, row flags
-  // Q', K and P use the 128-byte swizzled K-major layout: slabs of 64 values
+  // Q' and K use the 128-byte swizzled K-major layout: slabs of 64 values
   // (128-byte rows, chunks XOR-permuted by row mod 8) over all rows of the
   // operand, one slab after the other along K
   static constexpr int kSlabQ = BM * 128;           // one 64-channel slab of Q'
@@ -102,10 +103,12 @@ struct Layout {
   // V (the MN-major B of PV) uses plain core matrices (8 positions x 16
   // bytes): byte stride between 8-position groups
   static constexpr int kGroupD = (D / 8) * 128;
-  static constexpr int kOCol = 2 * BN;              // tensor-memory column of O (after S0, S1)
+  // tensor memory: S0, S1 (BN fp32 columns each; P, fp16 pairs, is written
+  // over the first BN / 2 columns of its block's S), then O (D columns)
+  static constexpr int kOCol = 2 * BN;
   static constexpr int kTmemCols = (kOCol + D) <= 256 ? 256 : 512;
   static_assert(kNumBars * 8 <= kBarBytes, "barriers");
-  static_assert(kK16 % 1024 == 0 && kP % 1024 == 0, "swizzle atoms are 1024-byte aligned");
+  static_assert(kK16 % 1024 == 0, "swizzle atoms are 1024-byte aligned");
   static_assert(kNumSlots * 4 <= 64, "slots");
 };
 
@@ -234,15 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      tc::mbar_init(bar(kKFull0 + b), kCvtThreads);
-      tc::mbar_init(bar(kVFull0 + b), kCvtThreads);
-      tc::mbar_init(bar(kKFree0 + b), 1);
-      tc::mbar_init(bar(kVFree0 + b), 1);
-      tc::mbar_init(bar(kSFull0 + b), 1);
-      tc::mbar_init(bar(kSFree0 + b), 32 * kSoftWarps);
-    }
+    tc::mbar_init(bar(kKFull), kCvtThreads);
+    tc::mbar_init(bar(kKFree), 1);
+    tc::mbar_init(bar(kVFull), kCvtThreads);
+    tc::mbar_init(bar(kSFull0), 1);
+    tc::mbar_init(bar(kSFull1), 1);
     tc::mbar_init(bar(kPFull), 32 * kSoftWarps);
     tc::mbar_init(bar(kPVDone), 1);
     tc::mbar_init(bar(kDone), 1);
@@ -426,31 +425,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
           }
         }
       };
+      // K runs one block ahead of V: K(i + 1) is converted once QK(i) has
+      // read the K buffer, V(i) once PV(i - 1) has read the V buffer
       load(kc, first, kr);
       load(vc, first, vr);
+      bool ok = tc::mbar_wait(bar(kKFree), 1, slot);  // (passes at once)
+      if (ok) {
+        convert(kr, sbase + L::kK16, true);
+        tc::fence_smem_to_async();
+        tc::mbar_arrive(bar(kKFull));
+        const int second = next_blk(first);
+        if (second <= bhi) load(kc, second, kr);
+      }
       int i = 0;
-      for (int blk = first; blk <= bhi; ++i) {
+      for (int blk = first; ok && blk <= bhi; ++i) {
         const int nxt = next_blk(blk);
-        const int b = i & 1;
-        // buffer b is free once the products of block i - 2 have read it
-        if (!tc::mbar_wait(bar(kKFree0 + b), ((i >> 1) & 1) ^ 1, slot)) {
-          slot[kAbort] = 1;
-          break;
-        }
-        convert(kr, sbase + L::kK16 + b * L::kKVBytes, true);
+        if (!(ok = tc::mbar_wait(bar(kPVDone), (i & 1) ^ 1, slot))) break;
+        convert(vr, sbase + L::kV16, false);
         tc::fence_smem_to_async();
-        tc::mbar_arrive(bar(kKFull0 + b));
-        if (nxt <= bhi) load(kc, nxt, kr);
-        if (!tc::mbar_wait(bar(kVFree0 + b), ((i >> 1) & 1) ^ 1, slot)) {
-          slot[kAbort] = 1;
-          break;
+        tc::mbar_arrive(bar(kVFull));
+        if (nxt <= bhi) {
+          load(vc, nxt, vr);
+          if (!(ok = tc::mbar_wait(bar(kKFree), i & 1, slot))) break;
+          convert(kr, sbase + L::kK16, true);
+          tc::fence_smem_to_async();
+          tc::mbar_arrive(bar(kKFull));
+          const int nn = next_blk(nxt);
+          if (nn <= bhi) load(kc, nn, kr);
         }
-        convert(vr, sbase + L::kV16 + b * L::kKVBytes, false);
-        tc::fence_smem_to_async();
-        tc::mbar_arrive(bar(kVFull0 + b));
-        if (nxt <= bhi) load(vc, nxt, vr);
         blk = nxt;
       }
+      if (!ok) slot[kAbort] = 1;
     } else if (warp == kMmaWarp) {
       // ---- MMA issue (one thread) ----
       // order: QK(0), QK(1), PV(0), QK(2), PV(1), ...: the scores of block
@@ -458,34 +463,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
       if (lane == 0) {
         constexpr uint32_t kIdQK = tc::idesc_f16(BM, BN, false, false);
         constexpr uint32_t kIdPV = tc::idesc_f16(BM, D, false, true);
-        const uint32_t q_s = sbase + L::kQ, p_s = sbase + L::kP;
+        const uint32_t q_s = sbase + L::kQ, k_s = sbase + L::kK16, v_s = sbase + L::kV16;
         auto pv = [&](int j) -> bool {
-          const int b = j & 1;
           if (!tc::mbar_wait(bar(kPFull), j & 1, slot)) return false;
-          if (!tc::mbar_wait(bar(kVFull0 + b), (j >> 1) & 1, slot)) return false;
+          if (!tc::mbar_wait(bar(kVFull), j & 1, slot)) return false;
           tc::fence_after_sync();
-          const uint32_t v_s = sbase + L::kV16 + b * L::kKVBytes;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
-            // A = P (K-major: M = vectors, K = positions), B = V (MN-major:
-            // K = positions, N = channels)
-            const uint64_t ad = tc::smem_desc_sw128(p_s + kk * 32, 1024);
+            // A = P (tensor memory: lane = vector, fp16 pairs along the
+            // positions), B = V (MN-major: K = positions, N = channels)
             const uint64_t bd = tc::smem_desc(v_s + kk * 2 * L::kGroupD, L::kGroupD, 128);
-            tc::mma_f16(tbase + L::kOCol, ad, bd, kIdPV, j > 0 || kk > 0);
+            tc::mma_f16_ts(tbase + L::kOCol, tbase + (j & 1) * BN + 8 * kk, bd, kIdPV,
+                           j > 0 || kk > 0);
           }
-          tc::mma_commit(bar(kVFree0 + b));
           tc::mma_commit(bar(kPVDone));
           return true;
         };
         int i = 0;
         bool ok = true;
         for (int blk = first; blk <= bhi; blk = next_blk(blk), ++i) {
-          const int b = i & 1;
-          ok = tc::mbar_wait(bar(kKFull0 + b), (i >> 1) & 1, slot) &&
-               tc::mbar_wait(bar(kSFree0 + b), ((i >> 1) & 1) ^ 1, slot);
+          // S(i) overwrites P(i - 2): PV(i - 2) must have read it
+          ok = tc::mbar_wait(bar(kKFull), i & 1, slot) &&
+               (i < 2 || tc::mbar_wait(bar(kPVDone), i & 1, slot));
           if (!ok) break;
           tc::fence_after_sync();
-          const uint32_t k_s = sbase + L::kK16 + b * L::kKVBytes;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             // A = Q' (K-major: M = vectors, K = channels), B = K (K-major:
@@ -493,10 +494,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
             const uint32_t koff = (kk & 3) * 32;  // K step inside a 64-channel slab
             const uint64_t ad = tc::smem_desc_sw128(q_s + (kk >> 2) * L::kSlabQ + koff, 1024);
             const uint64_t bd = tc::smem_desc_sw128(k_s + (kk >> 2) * L::kSlabK + koff, 1024);
-            tc::mma_f16(tbase + b * BN, ad, bd, kIdQK, kk > 0);
+            tc::mma_f16(tbase + (i & 1) * BN, ad, bd, kIdQK, kk > 0);
           }
-          tc::mma_commit(bar(kSFull0 + b));
-          tc::mma_commit(bar(kKFree0 + b));
+          tc::mma_commit(bar(kSFull0 + (i & 1)));
+          tc::mma_commit(bar(kKFree));
           if (i > 0 && !(ok = pv(i - 1))) break;
         }
         if (ok && i > 0) ok = pv(i - 1);
@@ -518,6 +519,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
       auto wait_all = [&](int b, uint32_t parity) -> bool {
         return __all_sync(0xffffffffu, tc::mbar_wait(bar(b), parity, slot));
       };
+      // the row's selection of 32 positions starting at 32 * word
+      auto sel_word = [&](int word) -> uint32_t {
+        return vec_live && word < a.mask_words ? mrow[word] : 0u;
+      };
       int i = 0;
       for (int blk = first; blk <= bhi; blk = next_blk(blk), ++i) {
         if (!wait_all(kSFull0 + (i & 1), (i >> 1) & 1)) {
@@ -525,47 +530,50 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
           break;
         }
         tc::fence_after_sync();
-        float s[BN];
-#pragma unroll
-        for (int c = 0; c < BN / 16; ++c) {
-          float v16[16];
-          tc::tmem_ld16(tbase + t_lane + (i & 1) * BN + 16 * c, v16);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) s[16 * c + e] = v16[e];
-        }
-        tc::tmem_wait_ld();
-        tc::fence_before_sync();
-        tc::mbar_arrive(bar(kSFree0 + (i & 1)));
-        // the row's selection of positions blk*64 .. blk*64+63
-        const uint32_t w0 = vec_live ? mrow[2 * blk] : 0u;
-        const uint32_t w1 = vec_live && 2 * blk + 1 < a.mask_words ? mrow[2 * blk + 1] : 0u;
+        const uint32_t s_col = tbase + t_lane + (i & 1) * BN;
+        // pass 1: the block maximum over the selected positions (32 columns
+        // of scores at a time)
         float mx = neg_inf();
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float sv[32];
+          tc::tmem_ld32(s_col + 32 * c, sv);
+          tc::tmem_wait_ld();
+          const uint32_t w = sel_word(BN / 32 * blk + c);
 #pragma unroll
-        for (int j = 0; j < BN; ++j) {
-          const bool sel = ((j < 32 ? w0 >> j : w1 >> (j - 32)) & 1u) != 0u;
-          s[j] = sel ? s[j] * sigma : neg_inf();
-          mx = fmaxf(mx, s[j]);
+          for (int j = 0; j < 32; ++j)
+            if ((w >> j) & 1u) mx = fmaxf(mx, sv[j] * sigma);
         }
         const float m_new = fmaxf(m_run, mx);
         const float base = m_new == neg_inf() ? 0.f : m_new;
-        if (vs_big) {
-#pragma unroll
-          for (int j = 0; j < BN; ++j) deep |= s[j] != neg_inf() && s[j] < m_new - kTail;
-        }
         const float alpha = fast_exp2((m_run - base) * kLog2e);
+        // pass 2: probabilities p * 2^15 as fp16 pairs, written over the
+        // scores already read (columns 16c .. 16c + 15 after chunk c)
         float ps = 0.f;
-        uint32_t ph[BN / 2];
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float sv[32];
+          tc::tmem_ld32(s_col + 32 * c, sv);
+          tc::tmem_wait_ld();
+          const uint32_t w = sel_word(BN / 32 * blk + c);
+          uint32_t ph[16];
 #pragma unroll
-        for (int j = 0; j < BN / 2; ++j) {
-          const float p0 = fast_exp2((s[2 * j] - base) * kLog2e);
-          const float p1 = fast_exp2((s[2 * j + 1] - base) * kLog2e);
-          ps += p0 + p1;
-          ph[j] = pack_h2(p0 * kProbScale, p1 * kProbScale);
+          for (int j = 0; j < 16; ++j) {
+            const bool s0 = (w >> (2 * j)) & 1u, s1 = (w >> (2 * j + 1)) & 1u;
+            const float x0 = s0 ? sv[2 * j] * sigma : neg_inf();
+            const float x1 = s1 ? sv[2 * j + 1] * sigma : neg_inf();
+            if (vs_big) deep |= (s0 && x0 < m_new - kTail) || (s1 && x1 < m_new - kTail);
+            const float p0 = fast_exp2((x0 - base) * kLog2e);
+            const float p1 = fast_exp2((x1 - base) * kLog2e);
+            ps += p0 + p1;
+            ph[j] = pack_h2(p0 * kProbScale, p1 * kProbScale);
+          }
+          tc::tmem_st16u(s_col + 16 * c, ph);
         }
         l_run = l_run * alpha + ps;
         const bool rescale = i > 0 && m_new != m_run;
         m_run = m_new;
-        // P's buffer and O are free once the previous block's PV has completed
+        // O is current once the previous block's PV has completed
         if (i > 0 && !wait_all(kPVDone, (i - 1) & 1)) {
           loop_ok = false;
           break;
@@ -582,16 +590,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
             for (int e = 0; e < 32; ++e) o[e] *= f;
             tc::tmem_st32(tbase + t_lane + L::kOCol + 32 * c, o);
           }
-          tc::tmem_wait_st();
         }
-        // row r of P (one 128-byte swizzled slab): positions 8k..8k+7 in
-        // chunk k ^ (r % 8)
-        uint8_t* pdst = smem + L::kP + r * 128;
-#pragma unroll
-        for (int k = 0; k < BN / 8; ++k)
-          *reinterpret_cast<uint4*>(pdst + ((k ^ (r & 7)) << 4)) =
-              make_uint4(ph[4 * k], ph[4 * k + 1], ph[4 * k + 2], ph[4 * k + 3]);
-        tc::fence_smem_to_async();
+        tc::tmem_wait_st();  // P (and O) written before the MMA is told
         tc::fence_before_sync();
         tc::mbar_arrive(bar(kPFull));
       }
