@@ -27,18 +27,20 @@
 // products (at the pages' density of one in four, 3-4x the selected flops),
 // which the tensor cores absorb.
 //
-// Warp roles (288 threads, one CTA per SM):
-//   warps 0-3  softmax and epilogue; thread i owns query vector i of the tile
-//              (tensor-memory lane i): scores in, probabilities out, running
-//              max / sum, the O rescale when its max moves, the output row.
-//   warps 4-7  converters: load the raw int8 K and V rows of a block into
+// Warp roles (544 threads, one CTA per SM):
+//   warps 0-7  softmax and epilogue; warps q and q + 4 own query vectors
+//              32q .. 32q + 31 of the tile (tensor-memory lanes), warp q the
+//              first 64 positions of a block and the first D/2 output channels,
+//              warp q + 4 the others; the pair exchanges its block maxima (and
+//              at the end its row sums) through shared memory.
+//   warps 8-15 converters: load the raw int8 K and V rows of a block into
 //              registers (one block ahead), convert them exactly to fp16 (K as
 //              the K-major B operand of QK^T, V as the MN-major B operand of
 //              PV), signal the MMA thread.
 // (An MMA instruction costs the same up to N = 128 columns and about twice as
 // much at N = 256, measured on this part: 128-token blocks keep QK^T at N=128
 // instead of wasting half of every instruction at N = 64.)
-//   warp 8     lane 0 issues the MMAs; the warp owns the tensor memory.
+//   warp 16    lane 0 issues the MMAs; the warp owns the tensor memory.
 // Hand-offs are mbarriers: every wait is bounded (about a second, or at once
 // after another thread gave up); a CTA that gives up writes NaN for its
 // outputs and raises I8KV_FLAG_WAIT_TIMEOUT instead of hanging.
@@ -67,9 +69,9 @@ namespace pf {
 
 constexpr int BM = 128;  // query vectors per tile (tensor-memory lanes)
 constexpr int BN = 128;  // cache positions per block
-constexpr int kSoftWarps = 4;
-constexpr int kCvtWarps = 4;
-constexpr int kMmaWarp = 8;
+constexpr int kSoftWarps = 8;   // two per tensor-memory lane quarter (column halves)
+constexpr int kCvtWarps = 8;
+constexpr int kMmaWarp = 16;
 constexpr int kThreads = 32 * (kSoftWarps + kCvtWarps + 1);
 constexpr int kCvtThreads = 32 * kCvtWarps;
 constexpr float kQueryBudget = 0.125f;  // nats (the decode kernels' query-folding budget)
@@ -94,7 +96,11 @@ struct Layout {
   static constexpr int kBarBytes = 128;
   static constexpr int kSlotOff = kMisc + kBarBytes;
   static constexpr int kListOff = kSlotOff + 64;    // BM uint16 vector indices
-  static constexpr int kMask = kListOff + 2 * BM;   // row bitmasks, block flags, row flags
+  // [3][2 halves][BM] floats: block maxima (two block parities), row sums
+  static constexpr int kXchg = kListOff + 2 * BM;
+  static constexpr int kVFlag = kXchg + 6 * BM * 4; // per vector: bit 0 / 1 = FP32 path
+  static constexpr int kVote = kVFlag + BM;         // [2][4 quarters][2 halves] ints
+  static constexpr int kMask = kVote + 64;          // row bitmasks, block flags, row flags
   // Q' and K use the 128-byte swizzled K-major layout: slabs of 64 values
   // (128-byte rows, chunks XOR-permuted by row mod 8) over all rows of the
   // operand, one slab after the other along K
@@ -312,13 +318,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
   // ---------------- Q' = fp16(Q * k_scale) (softmax warps) ----------------
   // Thread r stages its query vector as row r of the A operand: channels
   // 8c..8c+7 go to slab c / 8, row r, chunk (c % 8) ^ (r % 8).
-  const int r = tid;  // softmax warps: the vector of this thread
+  const int half = (warp >> 2) & 1;         // softmax warps: column half
+  const int r = 32 * (warp & 3) + lane;      // softmax warps: the vector of this thread
   const long long vidx = v0 + r;
   const bool vec_live = warp < kSoftWarps && vidx < nvec;
+  uint8_t* vflag = smem + L::kVFlag;
   const int vrow = vec_live ? (int)(vidx / G) : r_lo;
   const int vh = vec_live ? g * G + (int)(vidx - (long long)vrow * G) : 0;
   bool need_fp32 = false;
-  if (warp < kSoftWarps) {
+  if (warp < kSoftWarps / 2) {
     const __half* qrow = reinterpret_cast<const __half*>(p.q) + ((long long)vrow * p.Hq + vh) * D;
     uint8_t* qdst = smem + L::kQ + r * 128;
     bool bad = false;
@@ -357,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
       if (bad) flag_or(p.flags, I8KV_FLAG_QUERY_RANGE);
       need_fp32 = bad || p.sigma * 128.f * err > kQueryBudget || vs_bad || row_dup[vrow - r_lo];
     }
+    vflag[r] = need_fp32 ? 1 : 0;
     tc::fence_smem_to_async();  // Q' is read by the tensor core
   }
   // a tile with nothing for the tensor cores (no selected block, or every
@@ -365,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  if (warp < kSoftWarps) need_fp32 = vflag[r] != 0;
 
   // ---------------- the pipeline ----------------
   if (run_tc) {
@@ -386,10 +396,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
           const int q = ct + kCvtThreads * k;
           const long long pos = (long long)blk * BN + q % BN;
           if (pos < N) {
-            const uint4* src =
-                reinterpret_cast<const uint4*>(base + (pos * Hkv + g) * D + 32 * (q / BN));
-            dst[k][0] = __ldg(src);
-            dst[k][1] = __ldg(src + 1);
+            // one 32-byte sector per lane, not kept in L1 (each is read once)
+            const int8_t* src = base + (pos * Hkv + g) * D + 32 * (q / BN);
+            asm volatile(
+                "ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                : "=r"(dst[k][0].x), "=r"(dst[k][0].y), "=r"(dst[k][0].z), "=r"(dst[k][0].w),
+                  "=r"(dst[k][1].x), "=r"(dst[k][1].y), "=r"(dst[k][1].z), "=r"(dst[k][1].w)
+                : "l"(src));
           } else {
             dst[k][0] = dst[k][1] = make_uint4(0u, 0u, 0u, 0u);
           }
@@ -426,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
         }
       };
       // K runs one block ahead of V: K(i + 1) is converted once QK(i) has
-      // read the K buffer, V(i) once PV(i - 1) has read the V buffer
+      // read the K buffer, then V(i) once PV(i - 1) has read the V buffer
       load(kc, first, kr);
       load(vc, first, vr);
       bool ok = tc::mbar_wait(bar(kKFree), 1, slot);  // (passes at once)
@@ -440,12 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
       int i = 0;
       for (int blk = first; ok && blk <= bhi; ++i) {
         const int nxt = next_blk(blk);
-        if (!(ok = tc::mbar_wait(bar(kPVDone), (i & 1) ^ 1, slot))) break;
-        convert(vr, sbase + L::kV16, false);
-        tc::fence_smem_to_async();
-        tc::mbar_arrive(bar(kVFull));
+        // K(i + 1) first: its buffer frees when QK(i) completes, which comes
+        // before PV(i - 1) is even issued
         if (nxt <= bhi) {
-          load(vc, nxt, vr);
           if (!(ok = tc::mbar_wait(bar(kKFree), i & 1, slot))) break;
           convert(kr, sbase + L::kK16, true);
           tc::fence_smem_to_async();
@@ -453,6 +463,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
           const int nn = next_blk(nxt);
           if (nn <= bhi) load(kc, nn, kr);
         }
+        if (!(ok = tc::mbar_wait(bar(kPVDone), (i & 1) ^ 1, slot))) break;
+        convert(vr, sbase + L::kV16, false);
+        tc::fence_smem_to_async();
+        tc::mbar_arrive(bar(kVFull));
+        if (nxt <= bhi) load(vc, nxt, vr);
         blk = nxt;
       }
       if (!ok) slot[kAbort] = 1;
@@ -473,7 +488,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
             // A = P (tensor memory: lane = vector, fp16 pairs along the
             // positions), B = V (MN-major: K = positions, N = channels)
             const uint64_t bd = tc::smem_desc(v_s + kk * 2 * L::kGroupD, L::kGroupD, 128);
-            tc::mma_f16_ts(tbase + L::kOCol, tbase + (j & 1) * BN + 8 * kk, bd, kIdPV,
+            // positions 64h .. 64h + 63 of the block (h = kk / 4) sit in
+            // columns 64h .. 64h + 31 of its S buffer
+            tc::mma_f16_ts(tbase + L::kOCol,
+                           tbase + (j & 1) * BN + 64 * (kk >> 2) + 8 * (kk & 3), bd, kIdPV,
                            j > 0 || kk > 0);
           }
           tc::mma_commit(bar(kPVDone));
@@ -508,16 +526,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
       }
       __syncwarp();
     } else {
-      // ---- softmax (one query vector per thread) ----
-      const uint32_t t_lane = (uint32_t)(32 * warp) << 16;
+      // ---- softmax (one query vector per thread and column half) ----
+      const uint32_t t_lane = (uint32_t)(32 * (warp & 3)) << 16;
       const uint32_t* mrow = mask + (vrow - r_lo) * a.mask_words;
       const float sigma = p.sigma;
-      float m_run = neg_inf(), l_run = 0.f;
+      float* xchg = reinterpret_cast<float*>(smem + L::kXchg);  // [3][2][BM]
+      float m_run = neg_inf(), l_half = 0.f;
       bool deep = false, loop_ok = true;
       // the warp's lanes take every decision together (tcgen05.ld / st are
       // warp-collective)
       auto wait_all = [&](int b, uint32_t parity) -> bool {
         return __all_sync(0xffffffffu, tc::mbar_wait(bar(b), parity, slot));
+      };
+      // the two warps of a lane quarter (64 threads, named barrier 1 + q)
+      auto pair_sync = [&]() {
+        asm volatile("bar.sync %0, %1;\n" ::"r"(1 + (warp & 3)), "r"(64) : "memory");
+      };
+      // Both warps of the pair take the same branch after every wait (so that
+      // neither reaches a pair barrier the other has left): each publishes
+      // its warp-uniform result, and both continue only if both succeeded.
+      volatile int* votes = reinterpret_cast<volatile int*>(smem + L::kVote);
+      int nvote = 0;
+      auto pair_all = [&](bool ok) -> bool {
+        volatile int* v = votes + (nvote++ & 1) * 8 + (warp & 3) * 2;
+        if (lane == 0) v[half] = ok ? 1 : 0;
+        pair_sync();
+        return v[0] != 0 && v[1] != 0;
       };
       // the row's selection of 32 positions starting at 32 * word
       auto sel_word = [&](int word) -> uint32_t {
@@ -525,37 +559,42 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
       };
       int i = 0;
       for (int blk = first; blk <= bhi; blk = next_blk(blk), ++i) {
-        if (!wait_all(kSFull0 + (i & 1), (i >> 1) & 1)) {
+        if (!pair_all(wait_all(kSFull0 + (i & 1), (i >> 1) & 1))) {
           loop_ok = false;
           break;
         }
         tc::fence_after_sync();
-        const uint32_t s_col = tbase + t_lane + (i & 1) * BN;
-        // pass 1: the block maximum over the selected positions (32 columns
-        // of scores at a time)
+        // this half's 64 positions: score columns 64h .. 64h + 63 of the block
+        const uint32_t s_col = tbase + t_lane + (i & 1) * BN + 64 * half;
+        // pass 1: the maximum over the selected positions of the half, then
+        // of the block (with the other half's)
         float mx = neg_inf();
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < 2; ++c) {
           float sv[32];
           tc::tmem_ld32(s_col + 32 * c, sv);
           tc::tmem_wait_ld();
-          const uint32_t w = sel_word(BN / 32 * blk + c);
+          const uint32_t w = sel_word(BN / 32 * blk + 2 * half + c);
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if ((w >> j) & 1u) mx = fmaxf(mx, sv[j] * sigma);
         }
+        float* xb = xchg + (i & 1) * 2 * BM;
+        xb[half * BM + r] = mx;
+        pair_sync();
+        mx = fmaxf(mx, xb[(half ^ 1) * BM + r]);
         const float m_new = fmaxf(m_run, mx);
         const float base = m_new == neg_inf() ? 0.f : m_new;
         const float alpha = fast_exp2((m_run - base) * kLog2e);
         // pass 2: probabilities p * 2^15 as fp16 pairs, written over the
-        // scores already read (columns 16c .. 16c + 15 after chunk c)
+        // half's scores already read (columns 64h + 16c .. + 15 after chunk c)
         float ps = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < 2; ++c) {
           float sv[32];
           tc::tmem_ld32(s_col + 32 * c, sv);
           tc::tmem_wait_ld();
-          const uint32_t w = sel_word(BN / 32 * blk + c);
+          const uint32_t w = sel_word(BN / 32 * blk + 2 * half + c);
           uint32_t ph[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -570,11 +609,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
           }
           tc::tmem_st16u(s_col + 16 * c, ph);
         }
-        l_run = l_run * alpha + ps;
+        l_half = l_half * alpha + ps;
         const bool rescale = i > 0 && m_new != m_run;
         m_run = m_new;
-        // O is current once the previous block's PV has completed
-        if (i > 0 && !wait_all(kPVDone, (i - 1) & 1)) {
+        // O is current once the previous block's PV has completed; this half
+        // rescales channels hD/2 .. hD/2 + D/2 - 1
+        if (!pair_all(i == 0 || wait_all(kPVDone, (i - 1) & 1))) {
           loop_ok = false;
           break;
         }
@@ -582,13 +622,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
         if (__any_sync(0xffffffffu, rescale)) {
           const float f = rescale ? alpha : 1.f;
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < D / 64; ++c) {
             float o[32];
-            tc::tmem_ld32(tbase + t_lane + L::kOCol + 32 * c, o);
+            const uint32_t oc = tbase + t_lane + L::kOCol + half * (D / 2) + 32 * c;
+            tc::tmem_ld32(oc, o);
             tc::tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] *= f;
-            tc::tmem_st32(tbase + t_lane + L::kOCol + 32 * c, o);
+            tc::tmem_st32(oc, o);
           }
         }
         tc::tmem_wait_st();  // P (and O) written before the MMA is told
@@ -596,10 +637,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
         tc::mbar_arrive(bar(kPFull));
       }
       // ---- epilogue: O / l, the sink, lse ----
-      const bool ok = __all_sync(0xffffffffu, loop_ok && !slot[kAbort]) &&
-                      (i == 0 || wait_all(kPVDone, (i - 1) & 1));
+      const bool ok = pair_all(__all_sync(0xffffffffu, loop_ok && !slot[kAbort]) &&
+                               (i == 0 || wait_all(kPVDone, (i - 1) & 1)));
       tc::fence_after_sync();
-      need_fp32 |= vec_live && vs_big && deep;
+      // the row sum and the tail flag of both halves (the pair left the loop
+      // at the same block: every exit above follows a pair vote)
+      float* lx = xchg + 4 * BM;
+      lx[half * BM + r] = l_half;
+      if (deep) atomicOr(reinterpret_cast<unsigned int*>(vflag) + (r >> 2), 2u << (8 * (r & 3)));
+      pair_sync();
+      const float l_run = l_half + lx[(half ^ 1) * BM + r];
+      need_fp32 = vec_live && vflag[r] != 0;
       const bool write = vec_live && !need_fp32;
       float sc = 0.f;
       const float lse_v = l_run > 0.f ? m_run + logf(l_run) : neg_inf();
@@ -610,9 +658,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
       __half* orow = reinterpret_cast<__half*>(p.out) + ((long long)vrow * p.Hq + vh) * D;
       if (ok && i > 0) {
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           float o[32];
-          tc::tmem_ld32(tbase + t_lane + L::kOCol + 32 * c, o);
+          const int d0 = half * (D / 2) + 32 * c;
+          tc::tmem_ld32(tbase + t_lane + L::kOCol + d0, o);
           tc::tmem_wait_ld();
           if (write) {
 #pragma unroll
@@ -620,28 +669,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
               uint32_t h[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const int d = 32 * c + 8 * u + 2 * e;
+                const int d = d0 + 8 * u + 2 * e;
                 h[e] = pack_h2(o[8 * u + 2 * e] * sc * svs[d], o[8 * u + 2 * e + 1] * sc * svs[d + 1]);
               }
-              *reinterpret_cast<uint4*>(orow + 32 * c + 8 * u) = make_uint4(h[0], h[1], h[2], h[3]);
+              *reinterpret_cast<uint4*>(orow + d0 + 8 * u) = make_uint4(h[0], h[1], h[2], h[3]);
             }
           }
         }
       } else if (ok && write) {  // no selected block: O = 0
-        for (int c = 0; c < D / 8; ++c)
-          *reinterpret_cast<uint4*>(orow + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
+        for (int c = 0; c < D / 16; ++c)
+          *reinterpret_cast<uint4*>(orow + half * (D / 2) + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
       }
-      if (ok && write && p.lse != nullptr) p.lse[(long long)vrow * p.Hq + vh] = lse_v;
+      if (ok && write && half == 0 && p.lse != nullptr) p.lse[(long long)vrow * p.Hq + vh] = lse_v;
       if (!ok) slot[kAbort] = 1;
+      if (half == 1) need_fp32 = false;  // one entry per vector in the FP32 list
       tc::fence_before_sync();
     }
-  } else if (warp < kSoftWarps && vec_live && !need_fp32) {
+  } else if (warp < kSoftWarps / 2 && vec_live && !need_fp32) {
     // no tensor-core work: every position of the tile is unselected
     __half* orow = reinterpret_cast<__half*>(p.out) + ((long long)vrow * p.Hq + vh) * D;
     for (int c = 0; c < D / 8; ++c)
       *reinterpret_cast<uint4*>(orow + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
     if (p.lse != nullptr) p.lse[(long long)vrow * p.Hq + vh] = neg_inf();
   }
+  if (!run_tc && warp >= kSoftWarps / 2) need_fp32 = false;  // listed by the first half
   if (need_fp32) {
     const int k = atomicAdd(slot_rw + kNumFp32, 1);
     fplist[k] = (uint16_t)r;
@@ -652,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
   if (aborted) {
     // the CTA gave up waiting: its outputs are marked invalid
     if (tid == 0) flag_or(p.flags, I8KV_FLAG_WAIT_TIMEOUT);
-    if (warp < kSoftWarps && vec_live) {
+    if (warp < kSoftWarps / 2 && vec_live) {
       __half* orow = reinterpret_cast<__half*>(p.out) + ((long long)vrow * p.Hq + vh) * D;
       for (int d = 0; d < D; ++d) orow[d] = __ushort_as_half(0x7E00);
       if (p.lse != nullptr) p.lse[(long long)vrow * p.Hq + vh] = __int_as_float(0x7FC00000);
