@@ -744,7 +744,11 @@ def _deep(torch, K, W, np, t, dev, bench_graph, hbm, cache):
 
 
 def _prefill(torch, K, W, np, t, bench_graph, peaks):
-    """Sparse prefill: 2048 rows over an 8192-token cache, 24/2 heads, D 256."""
+    """Sparse prefill: 2048 rows over an 8192-token cache, 24/2 heads, D 256.
+    The dense tensor-core kernel computes S and PV over every 128-token block
+    some row of a 128-vector tile selects (rows' unselected positions get
+    probability 0): `executed_tflops` counts those products, `tflops` only the
+    selected candidates' (the algorithmic flops)."""
     c = W.sparse_prefill(seed=0)
     d = dict(q=t(c.q), k=t(c.k_codes), v=t(c.v_codes), ks=t(c.k_scale), vs=t(c.v_scale),
              idx=t(c.idx))
@@ -754,16 +758,37 @@ def _prefill(torch, K, W, np, t, bench_graph, peaks):
         K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"], c.sigma,
                       out=out)
     sec = bench_graph(fn, 1, reps=10)
+    S, Hq, Dh = c.q.shape
+    N, Hkv, _ = c.k_codes.shape
+    G = Hq // Hkv
     n_att = int((c.idx >= 0).sum())
-    flops = n_att * 24 * 256 * 4
-    gathered = n_att * 2 * 256 * 2
+    flops = n_att * Hq * Dh * 4
+    gathered = n_att * Hkv * 2 * Dh
+    # blocks of 128 positions each 128-vector tile runs (the same for every KV
+    # head: the tiles cover (row, head) pairs of one KV head)
+    blk = np.where(c.idx >= 0, c.idx // 128, -1)
+    nblk = (N + 127) // 128
+    rowsel = np.zeros((S, nblk), bool)
+    for r in range(S):
+        b = blk[r][blk[r] >= 0]
+        rowsel[r, b] = True
+    tiles = (S * G + 127) // 128
+    executed_blocks = 0
+    for tt in range(tiles):
+        r0, r1 = (tt * 128) // G, min(tt * 128 + 127, S * G - 1) // G
+        executed_blocks += int(rowsel[r0:r1 + 1].any(axis=0).sum())
+    executed = executed_blocks * Hkv * 128 * 128 * Dh * 4
     peak_tf = peaks["bf16_tflops"]
     return dict(
         workload="sparse prefill: 2048 rows at positions 6144+i over an 8192-token int8 cache, "
                  "2048 candidates per row, 24/2 heads, head_dim 256",
+        kernel="prefill_tc_kernel<256> (tcgen05, dense 128-token blocks with row masks)",
         ms_per_call=round(sec * 1e3, 4), tflops=round(flops / sec / 1e12, 2),
         frac_of_tensor=round(flops / sec / 1e12 / peak_tf, 4), tensor_peak=peak_tf,
-        gathered_gbs=round(gathered / sec / 1e9, 1), flops_per_call=flops)
+        executed_tflops=round(executed / sec / 1e12, 2),
+        executed_frac_of_tensor=round(executed / sec / 1e12 / peak_tf, 4),
+        gathered_gbs=round(gathered / sec / 1e9, 1), flops_per_call=flops,
+        executed_flops_per_call=executed)
 
 
 def reference_arm(args, rank, world):
