@@ -31,7 +31,6 @@ combine_kernel(const float* __restrict__ acc, const float* __restrict__ m,
   const int wid = blockIdx.x;  // (unit, head) pair
   const int lane = threadIdx.x & 31;
   grid_dependency_wait();  // the partials come from the preceding decode kernel
-  grid_launch_dependents();  // the next kernel may start launching (it waits for us)
   const int u = wid / G, j = wid - (wid / G) * G;
   const long long ml0 = (long long)u * ns * G + j;  // split k at ml0 + k*G
   const int c0 = threadIdx.x * V;                    // first channel of this thread

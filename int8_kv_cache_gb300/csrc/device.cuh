@@ -136,16 +136,11 @@ __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
-// Let the next grid of the stream start launching before this one ends (its
-// CTAs still block in grid_dependency_wait until this grid has completed and
-// its writes are visible, so this only hides launch latency).  Used by the
-// combine kernel only: measured on the sparse decode (S = 8, graphs of 32
-// calls), a trigger at combine entry took a call from 11.55 to 11.26 us, while
-// one at decode entry made the call slower (12.68 us) and the decode kernel
-// alone slower too (8.78 -> 8.89 us).
-__device__ __forceinline__ void grid_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-}
+// No kernel here lets its dependents launch early (griddepcontrol.
+// launch_dependents): measured on graphs of decode calls, an early trigger at
+// decode entry made the calls slower, and one at combine entry took the sparse
+// decode (S = 8) from 11.53 to 11.22 us per call but the ragged paged decode
+// from 37.3 to 40.8 us.
 
 __device__ __forceinline__ void flag_or(uint32_t* flags, uint32_t bits) {
   if (flags != nullptr) atomicOr(flags, bits);
