@@ -566,18 +566,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
         tc::fence_after_sync();
         // this half's 64 positions: score columns 64h .. 64h + 63 of the block
         const uint32_t s_col = tbase + t_lane + (i & 1) * BN + 64 * half;
-        // pass 1: the maximum over the selected positions of the half, then
-        // of the block (with the other half's)
+        // the half's 64 scores, read once: selected ones scaled by sigma,
+        // the others -inf; the maximum over the half, then over the block
+        // (with the other half's)
+        float sv[64];
+        tc::tmem_ld32(s_col, *reinterpret_cast<float(*)[32]>(&sv[0]));
+        tc::tmem_ld32(s_col + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+        tc::tmem_wait_ld();
         float mx = neg_inf();
-#pragma unroll 1
+#pragma unroll
         for (int c = 0; c < 2; ++c) {
-          float sv[32];
-          tc::tmem_ld32(s_col + 32 * c, sv);
-          tc::tmem_wait_ld();
           const uint32_t w = sel_word(BN / 32 * blk + 2 * half + c);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if ((w >> j) & 1u) mx = fmaxf(mx, sv[j] * sigma);
+          for (int j = 0; j < 32; ++j) {
+            const float x = ((w >> j) & 1u) ? sv[32 * c + j] * sigma : neg_inf();
+            sv[32 * c + j] = x;
+            mx = fmaxf(mx, x);
+          }
         }
         float* xb = xchg + (i & 1) * 2 * BM;
         xb[half * BM + r] = mx;
@@ -586,22 +591,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
         const float m_new = fmaxf(m_run, mx);
         const float base = m_new == neg_inf() ? 0.f : m_new;
         const float alpha = fast_exp2((m_run - base) * kLog2e);
-        // pass 2: probabilities p * 2^15 as fp16 pairs, written over the
-        // half's scores already read (columns 64h + 16c .. + 15 after chunk c)
+        // probabilities p * 2^15 as fp16 pairs, written over the half's
+        // scores (columns 64h .. 64h + 31)
         float ps = 0.f;
-#pragma unroll 1
+#pragma unroll
         for (int c = 0; c < 2; ++c) {
-          float sv[32];
-          tc::tmem_ld32(s_col + 32 * c, sv);
-          tc::tmem_wait_ld();
-          const uint32_t w = sel_word(BN / 32 * blk + 2 * half + c);
           uint32_t ph[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const bool s0 = (w >> (2 * j)) & 1u, s1 = (w >> (2 * j + 1)) & 1u;
-            const float x0 = s0 ? sv[2 * j] * sigma : neg_inf();
-            const float x1 = s1 ? sv[2 * j + 1] * sigma : neg_inf();
-            if (vs_big) deep |= (s0 && x0 < m_new - kTail) || (s1 && x1 < m_new - kTail);
+            const float x0 = sv[32 * c + 2 * j], x1 = sv[32 * c + 2 * j + 1];
+            if (vs_big)
+              deep |= (x0 != neg_inf() && x0 < m_new - kTail) ||
+                      (x1 != neg_inf() && x1 < m_new - kTail);
             const float p0 = fast_exp2((x0 - base) * kLog2e);
             const float p1 = fast_exp2((x1 - base) * kLog2e);
             ps += p0 + p1;
