@@ -27,20 +27,20 @@
 // products (at the pages' density of one in four, 3-4x the selected flops),
 // which the tensor cores absorb.
 //
-// Warp roles (512 threads, one CTA per SM):
+// Warp roles (544 threads, one CTA per SM):
 //   warps 0-7  softmax and epilogue; warps q and q + 4 own query vectors
 //              32q .. 32q + 31 of the tile (tensor-memory lanes), warp q the
 //              first 64 positions of a block and the first D/2 output channels,
 //              warp q + 4 the others; the pair exchanges its block maxima (and
 //              at the end its row sums) through shared memory.
-//   warps 8-14 converters: load the raw int8 K and V rows of a block into
+//   warps 8-15 converters: load the raw int8 K and V rows of a block into
 //              registers (one block ahead), convert them exactly to fp16 (K as
 //              the K-major B operand of QK^T, V as the MN-major B operand of
 //              PV), signal the MMA thread.
 // (An MMA instruction costs the same up to N = 128 columns and about twice as
 // much at N = 256, measured on this part: 128-token blocks keep QK^T at N=128
 // instead of wasting half of every instruction at N = 64.)
-//   warp 15    lane 0 issues the MMAs; the warp owns the tensor memory.
+//   warp 16    lane 0 issues the MMAs; the warp owns the tensor memory.
 // Hand-offs are mbarriers: every wait is bounded (about a second, or at once
 // after another thread gave up); a CTA that gives up writes NaN for its
 // outputs and raises I8KV_FLAG_WAIT_TIMEOUT instead of hanging.
@@ -70,8 +70,8 @@ namespace pf {
 constexpr int BM = 128;  // query vectors per tile (tensor-memory lanes)
 constexpr int BN = 128;  // cache positions per block
 constexpr int kSoftWarps = 8;   // two per tensor-memory lane quarter (column halves)
-constexpr int kCvtWarps = 7;  // 16 warps in all: 128 registers per thread
-constexpr int kMmaWarp = 15;
+constexpr int kCvtWarps = 8;
+constexpr int kMmaWarp = 16;
 constexpr int kThreads = 32 * (kSoftWarps + kCvtWarps + 1);
 constexpr int kCvtThreads = 32 * kCvtWarps;
 constexpr float kQueryBudget = 0.125f;  // nats (the decode kernels' query-folding budget)
@@ -386,8 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
       // stores).  Its pieces of the next block are loaded into registers while
       // the tensor cores work on the current ones.
       const int ct = tid - 32 * kSoftWarps;
-      constexpr int kAll = BN * D / 32;  // 32-byte pieces per block and matrix
-      constexpr int kPairs = (kAll + kCvtThreads - 1) / kCvtThreads;
+      constexpr int kPairs = BN * D / 32 / kCvtThreads;
       const int8_t* kc = reinterpret_cast<const int8_t*>(p.k);
       const int8_t* vc = reinterpret_cast<const int8_t*>(p.v);
       uint4 kr[kPairs][2], vr[kPairs][2];
@@ -395,7 +394,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
 #pragma unroll
         for (int k = 0; k < kPairs; ++k) {
           const int q = ct + kCvtThreads * k;
-          if (kAll % kCvtThreads != 0 && q >= kAll) break;
           const long long pos = (long long)blk * BN + q % BN;
           if (pos < N) {
             // one 32-byte sector per lane, not kept in L1 (each is read once)
@@ -415,7 +413,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
 #pragma unroll
         for (int k = 0; k < kPairs; ++k) {
           const int q = ct + kCvtThreads * k;
-          if (kAll % kCvtThreads != 0 && q >= kAll) break;
           const int pr = q % BN, cp = q / BN;
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
