@@ -148,7 +148,11 @@ size_t split_workspace_bytes(int32_t units, int32_t num_splits, int32_t G, int32
  *   split_geometry.  wave_ctas = SM count x resident CTAs per SM of the
  *   selected decode kernel (queried from the CUDA occupancy API and cached per
  *   device); granule = 64 (POW2_TILES) or 16 (WAVE); min_chunk = 128;
- *   max_splits = I8KV_MAX_SPLITS.
+ *   max_splits = I8KV_MAX_SPLITS.  For the paged path in WAVE mode with
+ *   override_value 0 the chunk is then moved to the multiple of 64 positions
+ *   (one round of the paged kernel's 4 warps x 16 positions) nearer to
+ *   ceil(cap / num_splits) -- the lower one only if it is >= 128 and gives at
+ *   most I8KV_MAX_SPLITS splits -- and num_splits = ceil(cap / chunk).
  * Outputs: *num_splits, *chunk, *workspace_bytes (0 when one split), and, if
  * wave_ctas is not NULL, the wave used.  Errors as for the decode calls'
  * shape checks, I8KV_ECUDA if the device cannot be queried.

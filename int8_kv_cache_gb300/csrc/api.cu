@@ -112,6 +112,24 @@ i8kv_status wave_of(const KernelKey& key, int32_t* wave) {
 constexpr int32_t kGranuleWave = 16;   // the kernel's 16-token slice
 constexpr int32_t kGranuleTiles = 64;  // the pages' 64-candidate tile
 constexpr int32_t kMinChunk = 128;     // MIN_CHUNK of the wave rule
+constexpr int32_t kPagedRound = 64;    // one round of a paged decode CTA: 4 warps x 16 positions
+
+// The paged decode kernel deals a split's 16-position steps to its 4 warps in
+// turn, so a chunk that is not a multiple of 64 positions leaves some warps a
+// step (and an HBM round trip) longer than the rest.  The automatic wave-rule
+// chunk ceil(cap / n) therefore goes to the multiple of 64 nearer to it (the
+// lower one only while it stays >= MIN_CHUNK and within MAX_SPLITS), and n
+// follows as ceil(cap / chunk).  Still a function of cap and units only.
+void snap_to_round(int64_t cap, int32_t* ns, int32_t* chunk) {
+  const int64_t raw = cdiv(cap, *ns);
+  const int64_t up = cdiv(raw, kPagedRound) * kPagedRound;
+  const int64_t dn = raw / kPagedRound * kPagedRound;
+  int64_t ch = up;
+  if (dn >= kMinChunk && raw - dn < up - raw && cdiv(cap, dn) <= I8KV_MAX_SPLITS) ch = dn;
+  if (ch > INT32_MAX) return;
+  *chunk = static_cast<int32_t>(ch);
+  *ns = static_cast<int32_t>(cdiv(cap, ch));
+}
 
 i8kv_status plan(const KernelKey& key, int64_t cap, int32_t units, int32_t mode, int32_t ovr,
                  int32_t* ns, int32_t* chunk, int32_t* wave_out) {
@@ -120,7 +138,11 @@ i8kv_status plan(const KernelKey& key, int64_t cap, int32_t units, int32_t mode,
   if (st != I8KV_OK) return st;
   if (wave_out) *wave_out = wave;
   const int32_t granule = mode == I8KV_GEOM_POW2_TILES ? kGranuleTiles : kGranuleWave;
-  return split_geometry(cap, units, wave, granule, kMinChunk, I8KV_MAX_SPLITS, mode, ovr, ns, chunk);
+  st = split_geometry(cap, units, wave, granule, kMinChunk, I8KV_MAX_SPLITS, mode, ovr, ns, chunk);
+  if (st != I8KV_OK) return st;
+  if (key.path == Path::kPaged && mode == I8KV_GEOM_WAVE && ovr == 0 && cap > 0 && *ns > 1)
+    snap_to_round(cap, ns, chunk);
+  return I8KV_OK;
 }
 
 // Geometry given by the caller: num_splits in [1, 32], chunk a positive

@@ -91,3 +91,53 @@ def test_tail_depth_rule(q0, vs, fp32):
     assert bool(f & FP32_PATH) == fp32
     assert np.all(np.abs(o - ref_o) <= 2e-3 + 1e-2 * np.abs(ref_o))
     assert_lse_close(l, ref_l, 1e-5)
+
+
+@pytest.mark.parametrize("S,Hq,Hkv,D,N,max_sel", [
+    (50, 16, 1, 128, 333, 120),    # G = 16: a tile spans 9 rows; N not a multiple of 128
+    (9, 12, 1, 256, 129, 40),      # one selected position in the last, 1-token block
+    (4, 8, 2, 256, 2000, 300),     # 4 * max_sel < N: the gathering kernel serves it
+    (6, 8, 2, 64, 200, 100),       # head_dim 64: the gathering kernel serves it
+])
+def test_shapes_on_either_kernel(S, Hq, Hkv, D, N, max_sel):
+    c = W.random_sparse(seed=S + N, S=S, Hq=Hq, Hkv=Hkv, D=D, N=N, max_sel=max_sel,
+                        invalid_frac=0.05, sink=True, sigma=1.0 / 16)
+    if N == 129:
+        c.idx[0, 0] = 128  # the only position of the last block
+    ref_o, ref_l = oracle_dsa(c)
+    o, l, f = _run(c)
+    assert not f & WAIT_TIMEOUT
+    assert_close_oracle(o, ref_o, "prefill shape")
+    assert_lse_oracle(l, ref_l, bound_of(c))
+
+
+def test_prefill_can_be_captured_and_replayed():
+    # the kernel choice and its launch depend on shapes only: a captured call
+    # replays to the same result as an eager one, over new inputs
+    import int8_kv_cache_gb300 as K
+    from helpers import sparse_to_device
+    c = W.random_sparse(seed=21, S=30, Hq=24, Hkv=2, D=256, N=700, max_sel=300, sigma=1.0 / 16)
+    d = sparse_to_device(c)
+    out = torch.empty_like(d["q"])
+    s = torch.cuda.Stream()
+
+    def call():
+        K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"], c.sigma,
+                      out=out)
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    eager = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    out.zero_()
+    d["q"].copy_(torch.flip(d["q"], dims=[0]))  # new query rows, same buffer
+    g.replay()
+    torch.cuda.synchronize()
+    flipped = out.clone()
+    d["q"].copy_(torch.flip(d["q"], dims=[0]))  # back to the original rows
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    assert not torch.equal(flipped, eager)
