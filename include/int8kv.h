@@ -149,8 +149,9 @@ size_t split_workspace_bytes(int32_t units, int32_t num_splits, int32_t G, int32
  *   selected decode kernel (queried from the CUDA occupancy API and cached per
  *   device); granule = 64 (POW2_TILES) or 16 (WAVE); min_chunk = 128;
  *   max_splits = I8KV_MAX_SPLITS.  For the paged path in WAVE mode with
- *   override_value 0 the chunk is then moved to the multiple of 64 positions
- *   (one round of the paged kernel's 4 warps x 16 positions) nearer to
+ *   override_value 0 the chunk is then moved to the multiple of one round of
+ *   the paged kernel's CTA (4 warps x its step: 128 positions for an int8 or
+ *   e4m3fn cache with head_dim <= 128, else 64) nearer to
  *   ceil(cap / num_splits) -- the lower one only if it is >= 128 and gives at
  *   most I8KV_MAX_SPLITS splits -- and num_splits = ceil(cap / chunk).
  * Outputs: *num_splits, *chunk, *workspace_bytes (0 when one split), and, if

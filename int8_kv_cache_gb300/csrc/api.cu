@@ -16,6 +16,7 @@
 namespace {
 
 using i8kv::DecodeParams;
+using i8kv::KernelInfo;
 using i8kv::KernelKey;
 using i8kv::Path;
 
@@ -66,20 +67,28 @@ KernelKey make_key(Path path, int32_t D, int32_t G, int32_t cache_dtype, bool p_
   return k;
 }
 
-cudaError_t launch_key(const KernelKey& key, const DecodeParams& p, cudaStream_t s, int* occ) {
+cudaError_t launch_key(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
+                       KernelInfo* info) {
   if (key.path == Path::kDsa) {
-    return key.p_lo ? i8kv::launch_dsa_decode(key, p, s, occ) : i8kv::launch_dsa_prefill(key, p, s, occ);
+    return key.p_lo ? i8kv::launch_dsa_decode(key, p, s, info)
+                    : i8kv::launch_dsa_prefill(key, p, s, info);
   }
-  if (key.fp16_cache) return i8kv::launch_paged_fp16(key, p, s, occ);
-  if (key.fp8_cache) return i8kv::launch_paged_fp8(key, p, s, occ);
-  return i8kv::launch_paged_int8(key, p, s, occ);
+  if (key.fp16_cache) return i8kv::launch_paged_fp16(key, p, s, info);
+  if (key.fp8_cache) return i8kv::launch_paged_fp8(key, p, s, info);
+  return i8kv::launch_paged_int8(key, p, s, info);
 }
 
 // One occupancy wave (SM count x resident CTAs per SM) of a kernel on the
-// current device, cached per (device, kernel).
-i8kv_status wave_of(const KernelKey& key, int32_t* wave) {
+// current device and the positions of one round of its CTA, cached per
+// (device, kernel).
+struct WaveInfo {
+  int32_t wave;
+  int32_t round;
+};
+
+i8kv_status wave_of(const KernelKey& key, WaveInfo* out) {
   static std::mutex mu;
-  static std::map<std::tuple<int, int, int, int, int, int, int>, int32_t> cache;
+  static std::map<std::tuple<int, int, int, int, int, int, int>, WaveInfo> cache;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -90,40 +99,41 @@ i8kv_status wave_of(const KernelKey& key, int32_t* wave) {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(k);
     if (it != cache.end()) {
-      *wave = it->second;
+      *out = it->second;
       return I8KV_OK;
     }
   }
-  int sms = 0, occ = 0;
+  int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail(e);
   DecodeParams dummy{};
-  e = launch_key(key, dummy, nullptr, &occ);
+  KernelInfo info{0, 0};
+  e = launch_key(key, dummy, nullptr, &info);
   if (e != cudaSuccess) return cuda_fail(e);
-  const int32_t w = std::max(1, sms * std::max(occ, 1));
+  const WaveInfo w{std::max(1, sms * std::max(info.occupancy, 1)), std::max(info.round, 16)};
   {
     std::lock_guard<std::mutex> lock(mu);
     cache[k] = w;
   }
-  *wave = w;
+  *out = w;
   return I8KV_OK;
 }
 
-constexpr int32_t kGranuleWave = 16;   // the kernel's 16-token slice
+constexpr int32_t kGranuleWave = 16;   // the kernels' 16-position MMA tile
 constexpr int32_t kGranuleTiles = 64;  // the pages' 64-candidate tile
 constexpr int32_t kMinChunk = 128;     // MIN_CHUNK of the wave rule
-constexpr int32_t kPagedRound = 64;    // one round of a paged decode CTA: 4 warps x 16 positions
 
-// The paged decode kernel deals a split's 16-position steps to its 4 warps in
-// turn, so a chunk that is not a multiple of 64 positions leaves some warps a
-// step (and an HBM round trip) longer than the rest.  The automatic wave-rule
-// chunk ceil(cap / n) therefore goes to the multiple of 64 nearer to it (the
-// lower one only while it stays >= MIN_CHUNK and within MAX_SPLITS), and n
-// follows as ceil(cap / chunk).  Still a function of cap and units only.
-void snap_to_round(int64_t cap, int32_t* ns, int32_t* chunk) {
+// The paged decode kernel deals a split's steps (16 or 32 positions) to its 4
+// warps in turn, so a chunk that is not a multiple of one round (warps x step:
+// 64 or 128 positions) leaves some warps a step, and an HBM round trip, longer
+// than the rest.  The automatic wave-rule chunk ceil(cap / n) therefore goes
+// to the multiple of the round nearer to it (the lower one only while it stays
+// >= MIN_CHUNK and within MAX_SPLITS), and n follows as ceil(cap / chunk).
+// Still a function of cap, units and the kernel only.
+void snap_to_round(int64_t cap, int64_t round, int32_t* ns, int32_t* chunk) {
   const int64_t raw = cdiv(cap, *ns);
-  const int64_t up = cdiv(raw, kPagedRound) * kPagedRound;
-  const int64_t dn = raw / kPagedRound * kPagedRound;
+  const int64_t up = cdiv(raw, round) * round;
+  const int64_t dn = raw / round * round;
   int64_t ch = up;
   if (dn >= kMinChunk && raw - dn < up - raw && cdiv(cap, dn) <= I8KV_MAX_SPLITS) ch = dn;
   if (ch > INT32_MAX) return;
@@ -133,15 +143,16 @@ void snap_to_round(int64_t cap, int32_t* ns, int32_t* chunk) {
 
 i8kv_status plan(const KernelKey& key, int64_t cap, int32_t units, int32_t mode, int32_t ovr,
                  int32_t* ns, int32_t* chunk, int32_t* wave_out) {
-  int32_t wave = 0;
-  i8kv_status st = wave_of(key, &wave);
+  WaveInfo w{0, 0};
+  i8kv_status st = wave_of(key, &w);
   if (st != I8KV_OK) return st;
-  if (wave_out) *wave_out = wave;
+  if (wave_out) *wave_out = w.wave;
   const int32_t granule = mode == I8KV_GEOM_POW2_TILES ? kGranuleTiles : kGranuleWave;
-  st = split_geometry(cap, units, wave, granule, kMinChunk, I8KV_MAX_SPLITS, mode, ovr, ns, chunk);
+  st = split_geometry(cap, units, w.wave, granule, kMinChunk, I8KV_MAX_SPLITS, mode, ovr, ns,
+                      chunk);
   if (st != I8KV_OK) return st;
   if (key.path == Path::kPaged && mode == I8KV_GEOM_WAVE && ovr == 0 && cap > 0 && *ns > 1)
-    snap_to_round(cap, ns, chunk);
+    snap_to_round(cap, w.round, ns, chunk);
   return I8KV_OK;
 }
 

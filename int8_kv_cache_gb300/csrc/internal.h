@@ -53,19 +53,25 @@ struct KernelKey {
   bool p_lo;       // probability tile as fp16 high + low parts
 };
 
+// What the geometry needs to know of a decode kernel instantiation.
+struct KernelInfo {
+  int occupancy;  // resident CTAs per SM (the CUDA occupancy API)
+  int round;      // positions one round of the CTA's warps covers (warps x step)
+};
+
 // Per-path launchers (one per translation unit): grid (rows * Hkv, num_splits);
-// with occupancy != NULL nothing is launched and the resident CTAs per SM of
-// the selected kernel are returned there instead.
+// with info != NULL nothing is launched and the selected kernel's KernelInfo
+// is returned there instead.
 cudaError_t launch_dsa_decode(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
-                              int* occupancy);
+                              KernelInfo* info);
 cudaError_t launch_dsa_prefill(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
-                               int* occupancy);
+                               KernelInfo* info);
 cudaError_t launch_paged_int8(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
-                              int* occupancy);
+                              KernelInfo* info);
 cudaError_t launch_paged_fp16(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
-                              int* occupancy);
+                              KernelInfo* info);
 cudaError_t launch_paged_fp8(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
-                             int* occupancy);
+                             KernelInfo* info);
 
 // The dense tensor-core prefill (prefill_tc.cu): whether it serves a shape
 // (and with how much shared memory / how many mask rows), and its launch.

@@ -1,9 +1,9 @@
 // Instantiations of the decode kernel: DSA sparse-candidate decode.
-#include "decode_kernel.cuh"
+#include "decode_launch.cuh"
 
 namespace i8kv {
 cudaError_t launch_dsa_decode(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
-                              int* occupancy) {
-  return dispatch_decode<false, false, true>(key, p, s, occupancy);
+                              KernelInfo* info) {
+  return dispatch_decode<false, false, true>(key, p, s, info);
 }
 }  // namespace i8kv

@@ -1,9 +1,9 @@
 // Instantiations of the decode kernel: paged decode over a float8 e4m3fn cache.
-#include "decode_kernel.cuh"
+#include "decode_launch.cuh"
 
 namespace i8kv {
 cudaError_t launch_paged_fp8(const KernelKey& key, const DecodeParams& p, cudaStream_t s,
-                             int* occupancy) {
-  return dispatch_decode<true, false, true, true>(key, p, s, occupancy);
+                             KernelInfo* info) {
+  return dispatch_decode<true, false, true, true>(key, p, s, info);
 }
 }  // namespace i8kv
