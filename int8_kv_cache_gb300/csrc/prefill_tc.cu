@@ -21,11 +21,15 @@
 //   back into tensor memory over the block's scores
 //   O[128 x D] += P[128 x 128] V_block         tcgen05 kind::f16, M=128, N=D,
 //                                            P from tensor memory
-// so each cache block is converted int8 -> fp16 once per tile instead of once
+// So each cache block is converted int8 -> fp16 once per tile instead of once
 // per row that selects it, and both products are real dense contractions with
 // the accumulators in tensor memory.  The cost is the masked positions'
 // products (at the pages' density of one in four, 3-4x the selected flops),
 // which the tensor cores absorb.
+// The exponentials take a base that follows the running maximum lazily: it
+// moves only once the maximum has outgrown it by more than kLazy = 0.5 nats
+// (p <= e^0.5 keeps p * 2^15 under the fp16 maximum), so O is rescaled on few
+// blocks; O, the row sum and lse all use that base, so the result is the same.
 //
 // Warp roles (544 threads, one CTA per SM):
 //   warps 0-7  softmax and epilogue; warps q and q + 4 own query vectors
@@ -76,6 +80,7 @@ constexpr int kThreads = 32 * (kSoftWarps + kCvtWarps + 1);
 constexpr int kCvtThreads = 32 * kCvtWarps;
 constexpr float kQueryBudget = 0.125f;  // nats (the decode kernels' query-folding budget)
 constexpr float kTail = 20.f;           // nats below the running maximum
+constexpr float kLazy = 0.5f;           // nats the maximum may outgrow the base
 constexpr float kBigVs = 65536.f;       // |value_scale| above which the tail matters
 
 // barrier slots (8 bytes each) in the misc area
@@ -531,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
       const uint32_t* mrow = mask + (vrow - r_lo) * a.mask_words;
       const float sigma = p.sigma;
       float* xchg = reinterpret_cast<float*>(smem + L::kXchg);  // [3][2][BM]
-      float m_run = neg_inf(), l_half = 0.f;
+      float m_run = neg_inf(), m_top = neg_inf(), l_half = 0.f;
       bool deep = false, loop_ok = true;
       // the warp's lanes take every decision together (tcgen05.ld / st are
       // warp-collective)
@@ -588,7 +593,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
         xb[half * BM + r] = mx;
         pair_sync();
         mx = fmaxf(mx, xb[(half ^ 1) * BM + r]);
-        const float m_new = fmaxf(m_run, mx);
+        const float top = fmaxf(m_top, mx);  // the running maximum
+        // the base of the exponentials moves to the running maximum only once
+        // that has grown by more than kLazy nats (p <= e^kLazy keeps p * 2^15
+        // within fp16), so that O is rescaled only on those blocks
+        const float m_new = top > m_run + kLazy ? top : m_run;
         const float base = m_new == neg_inf() ? 0.f : m_new;
         const float alpha = fast_exp2((m_run - base) * kLog2e);
         // probabilities p * 2^15 as fp16 pairs, written over the half's
@@ -601,26 +610,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
           for (int j = 0; j < 16; ++j) {
             const float x0 = sv[32 * c + 2 * j], x1 = sv[32 * c + 2 * j + 1];
             if (vs_big)
-              deep |= (x0 != neg_inf() && x0 < m_new - kTail) ||
-                      (x1 != neg_inf() && x1 < m_new - kTail);
-            const float p0 = fast_exp2((x0 - base) * kLog2e);
-            const float p1 = fast_exp2((x1 - base) * kLog2e);
+              deep |= (x0 != neg_inf() && x0 < top - kTail) ||
+                      (x1 != neg_inf() && x1 < top - kTail);
+            // p * 2^15: the factor enters as 15 in the exponent (exact)
+            const float p0 = fast_exp2(fmaf(x0 - base, kLog2e, 15.f));
+            const float p1 = fast_exp2(fmaf(x1 - base, kLog2e, 15.f));
             ps += p0 + p1;
-            ph[j] = pack_h2(p0 * kProbScale, p1 * kProbScale);
+            ph[j] = pack_h2(p0, p1);
           }
           tc::tmem_st16u(s_col + 16 * c, ph);
         }
-        l_half = l_half * alpha + ps;
+        l_half = l_half * alpha + ps * kInvProbScale;
         const bool rescale = i > 0 && m_new != m_run;
         m_run = m_new;
+        m_top = top;
         // O is current once the previous block's PV has completed; this half
-        // rescales channels hD/2 .. hD/2 + D/2 - 1
+        // rescales channels hD/2 .. hD/2 + D/2 - 1.  (The wait stays even
+        // when no vector rescales: it also keeps every softmax warp's arrival
+        // for this block from counting toward the previous one.)
+        const bool any_rescale = __any_sync(0xffffffffu, rescale);
         if (!pair_all(i == 0 || wait_all(kPVDone, (i - 1) & 1))) {
           loop_ok = false;
           break;
         }
         tc::fence_after_sync();
-        if (__any_sync(0xffffffffu, rescale)) {
+        if (any_rescale) {
           const float f = rescale ? alpha : 1.f;
 #pragma unroll 1
           for (int c = 0; c < D / 64; ++c) {
