@@ -753,13 +753,18 @@ def _prefill(torch, K, W, np, t, bench_graph, peaks):
     d = dict(q=t(c.q), k=t(c.k_codes), v=t(c.v_codes), ks=t(c.k_scale), vs=t(c.v_scale),
              idx=t(c.idx))
     out = torch.empty_like(d["q"])
-
-    def fn():
-        K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"], c.sigma,
-                      out=out)
-    sec = bench_graph(fn, 1, reps=10)
     S, Hq, Dh = c.q.shape
     N, Hkv, _ = c.k_codes.shape
+    # the staged form: the call converts the cache once into fp16 operand
+    # images in this workspace (allocated once, like a decode's split workspace)
+    ws = torch.empty(K.prefill_workspace_bytes(S, Hq, Hkv, Dh, N, c.idx.shape[1]),
+                     dtype=torch.uint8, device=d["q"].device)
+
+    def fn(staged=True):
+        K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"], c.sigma,
+                      out=out, workspace=ws if staged else None)
+    sec = bench_graph(fn, 1, reps=10)
+    sec_conv = bench_graph(lambda: fn(False), 1, reps=10)
     G = Hq // Hkv
     n_att = int((c.idx >= 0).sum())
     flops = n_att * Hq * Dh * 4
@@ -782,8 +787,11 @@ def _prefill(torch, K, W, np, t, bench_graph, peaks):
     return dict(
         workload="sparse prefill: 2048 rows at positions 6144+i over an 8192-token int8 cache, "
                  "2048 candidates per row, 24/2 heads, head_dim 256",
-        kernel="prefill_tc_kernel<256> (tcgen05, dense 128-token blocks with row masks)",
+        kernel="prefill_stage_kernel<256> + prefill_tc_kernel<256, staged> (tcgen05, dense "
+               "128-token blocks with row masks, fp16 operand images copied in by one thread)",
         ms_per_call=round(sec * 1e3, 4), tflops=round(flops / sec / 1e12, 2),
+        converting_form_ms_per_call=round(sec_conv * 1e3, 4),
+        workspace_bytes=int(ws.numel()),
         frac_of_tensor=round(flops / sec / 1e12 / peak_tf, 4), tensor_peak=peak_tf,
         executed_tflops=round(executed / sec / 1e12, 2),
         executed_frac_of_tensor=round(executed / sec / 1e12 / peak_tf, 4),

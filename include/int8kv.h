@@ -216,6 +216,37 @@ i8kv_status dsa_prefill(const uint16_t* q, const int8_t* k_cache, const int8_t* 
                         void* stream);
 
 /*
+ * dsa_prefill_workspace_bytes -- bytes of the workspace that lets dsa_prefill_ws
+ * take the staged form of the tensor-core kernel for this shape: Hkv x
+ * ceil(N / 128) x 2 x 128 x D x 2 (the cache as fp16 operand images), or 0
+ * when the tensor-core kernel does not serve the shape (head_dim other than
+ * 128 / 256, 4 * max_sel < N, S, N or max_sel < 1, bad heads).  Host
+ * arithmetic only.
+ */
+size_t dsa_prefill_workspace_bytes(int32_t S, int32_t Hq, int32_t Hkv, int32_t D, int64_t N,
+                                   int32_t max_sel);
+
+/*
+ * dsa_prefill_ws -- dsa_prefill with an optional workspace (the caller's device
+ * memory, 16-byte aligned, workspace_bytes >= dsa_prefill_workspace_bytes).
+ * With one, where the tensor-core kernel serves the shape, the call first
+ * converts the cache once into fp16 operand images in the workspace (a
+ * kernel of its own, about 3 bytes written per cache byte read) and the
+ * prefill kernel copies each block in with one bulk copy instead of
+ * converting it in every CTA; the results are the same bit for bit.  With
+ * workspace NULL, or where the gathering kernel serves the shape, it is
+ * dsa_prefill.  The workspace holds nothing the caller needs afterwards.
+ * Errors: as dsa_prefill; I8KV_EWORKSPACE if workspace_bytes is too small,
+ * I8KV_EALIGN if the workspace is not 16-byte aligned.
+ */
+i8kv_status dsa_prefill_ws(const uint16_t* q, const int8_t* k_cache, const int8_t* v_cache,
+                           const float* k_scale, const float* v_scale, int32_t scale_kind,
+                           const int32_t* idx, int32_t S, int32_t Hq, int32_t Hkv, int32_t D,
+                           int64_t N, int32_t max_sel, float softmax_scale,
+                           const float* head_sink, void* workspace, size_t workspace_bytes,
+                           uint16_t* out, float* lse, uint32_t* flags, void* stream);
+
+/*
  * paged_decode -- split-KV decode over a paged block-table cache
  * (onnxruntime PR 29912, CUDA kernels: "split-KV, block-table-aware decode
  * with native head-sink ... and on-the-fly cache dequantization").

@@ -365,11 +365,30 @@ i8kv_status dsa_prefill(const uint16_t* q, const int8_t* k_cache, const int8_t* 
                         int64_t N, int32_t max_sel, float softmax_scale,
                         const float* head_sink, uint16_t* out, float* lse, uint32_t* flags,
                         void* stream) {
+  return dsa_prefill_ws(q, k_cache, v_cache, k_scale, v_scale, scale_kind, idx, S, Hq, Hkv, D, N,
+                        max_sel, softmax_scale, head_sink, nullptr, 0, out, lse, flags, stream);
+}
+
+size_t dsa_prefill_workspace_bytes(int32_t S, int32_t Hq, int32_t Hkv, int32_t D, int64_t N,
+                                   int32_t max_sel) {
+  if (S < 1 || N < 1 || max_sel < 1 || check_heads(Hq, Hkv, D) != I8KV_OK) return 0;
+  int smem = 0, mask_rows = 0;
+  if (!i8kv::prefill_tc_plan(D, Hq / Hkv, S, N, max_sel, &smem, &mask_rows)) return 0;
+  return i8kv::prefill_stage_bytes(N, Hkv, D);
+}
+
+i8kv_status dsa_prefill_ws(const uint16_t* q, const int8_t* k_cache, const int8_t* v_cache,
+                           const float* k_scale, const float* v_scale, int32_t scale_kind,
+                           const int32_t* idx, int32_t S, int32_t Hq, int32_t Hkv, int32_t D,
+                           int64_t N, int32_t max_sel, float softmax_scale,
+                           const float* head_sink, void* workspace, size_t workspace_bytes,
+                           uint16_t* out, float* lse, uint32_t* flags, void* stream) {
   DecodeParams p;
   i8kv_status st = dsa_common(q, k_cache, v_cache, k_scale, v_scale, scale_kind, idx, S, Hq, Hkv,
                               D, N, max_sel, softmax_scale, head_sink, out, lse, flags, p);
   if (st != I8KV_OK) return st;
   if (S > 0 && out == nullptr) return I8KV_EINVAL;
+  if (!aligned(workspace, 16)) return I8KV_EALIGN;
   if (S == 0) return I8KV_OK;
   p.num_splits = 1;
   p.chunk = static_cast<int32_t>(std::max<int64_t>(16, cdiv(max_sel, 16) * 16));
@@ -378,7 +397,14 @@ i8kv_status dsa_prefill(const uint16_t* q, const int8_t* k_cache, const int8_t* 
   // gathering mma.sync kernel
   int smem = 0, mask_rows = 0;
   if (i8kv::prefill_tc_plan(D, p.G, S, N, max_sel, &smem, &mask_rows)) {
-    cudaError_t e = i8kv::launch_dsa_prefill_tc(p, D, smem, mask_rows,
+    // with a workspace: the staged form (fp16 operand images made once per
+    // call, copied in by one thread); without: the converting form
+    void* stage = nullptr;
+    if (workspace != nullptr) {
+      if (workspace_bytes < i8kv::prefill_stage_bytes(N, Hkv, D)) return I8KV_EWORKSPACE;
+      stage = workspace;
+    }
+    cudaError_t e = i8kv::launch_dsa_prefill_tc(p, D, smem, mask_rows, stage,
                                                 static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? I8KV_OK : cuda_fail(e);
   }

@@ -77,8 +77,11 @@ cudaError_t launch_paged_fp8(const KernelKey& key, const DecodeParams& p, cudaSt
 // (and with how much shared memory / how many mask rows), and its launch.
 bool prefill_tc_plan(int D, int G, int rows, long long N, int max_sel, int* smem_bytes,
                      int* mask_rows);
+// stage: NULL for the converting form; else the staged form's operand images
+// (prefill_stage_bytes of them, 16-byte aligned), written by the call itself.
 cudaError_t launch_dsa_prefill_tc(const DecodeParams& p, int D, int smem, int mask_rows,
-                                  cudaStream_t s);
+                                  void* stage, cudaStream_t s);
+size_t prefill_stage_bytes(long long N, int Hkv, int D);
 
 cudaError_t launch_combine(const float* acc, const float* m, const float* l, int units,
                            int num_splits, int Hq, int Hkv, int D, const float* sink, void* out,

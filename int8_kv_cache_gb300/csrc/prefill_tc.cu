@@ -75,9 +75,17 @@ constexpr int BM = 128;  // query vectors per tile (tensor-memory lanes)
 constexpr int BN = 128;  // cache positions per block
 constexpr int kSoftWarps = 8;   // two per tensor-memory lane quarter (column halves)
 constexpr int kCvtWarps = 8;
-constexpr int kMmaWarp = 16;
-constexpr int kThreads = 32 * (kSoftWarps + kCvtWarps + 1);
 constexpr int kCvtThreads = 32 * kCvtWarps;
+// Warp roles of the two forms: the converting form reads the int8 cache and
+// converts it in the kernel (8 converter warps, then the MMA warp); the staged
+// form copies fp16 operand images that prefill_stage_kernel made (one loader
+// warp after the MMA warp).
+template <bool STAGED>
+struct Roles {
+  static constexpr int kMmaWarp = STAGED ? kSoftWarps : kSoftWarps + kCvtWarps;
+  static constexpr int kLoadWarp = kSoftWarps + 1;  // staged form only
+  static constexpr int kThreads = 32 * (STAGED ? kSoftWarps + 2 : kSoftWarps + kCvtWarps + 1);
+};
 constexpr float kQueryBudget = 0.125f;  // nats (the decode kernels' query-folding budget)
 constexpr float kTail = 20.f;           // nats below the running maximum
 constexpr float kLazy = 0.5f;           // nats the maximum may outgrow the base
@@ -125,11 +133,22 @@ struct Layout {
 
 struct Args {
   DecodeParams p;
+  const uint8_t* stage;  // staged form: the fp16 operand images (else null)
   int tiles_per_head;  // ceil(rows * G / 128)
   int mask_rows;       // rows a tile can span
   int mask_words;      // ceil(N / 32)
   int nblocks;         // ceil(N / BN)
 };
+
+// Byte offset, inside a block's fp16 operand, of the 16-byte chunk c0
+// (channels 8c0 .. 8c0 + 7) of position pr: K (swz) in the 128-byte swizzled
+// K-major slabs, V in plain core matrices (8 positions x 16 bytes).
+template <int D>
+__device__ __forceinline__ uint32_t chunk_offset(int pr, int c0, bool swz) {
+  using L = Layout<D>;
+  return swz ? (c0 >> 3) * L::kSlabK + pr * 128 + (((c0 & 7) ^ (pr & 7)) << 4)
+             : (pr >> 3) * L::kGroupD + (pr & 7) * 16 + c0 * 128;
+}
 
 // Exact int8 -> fp16 of 16 codes (one 16-byte chunk) in channel order.
 __device__ __forceinline__ void cvt16(const uint4 raw, uint4& lo, uint4& hi) {
@@ -214,9 +233,52 @@ __device__ __noinline__ void fp32_vector(const DecodeParams& p, int row, int h, 
     p.lse[(long long)row * p.Hq + h] = l > 0.f ? m + logf(l) : neg_inf();
 }
 
+// The staged form's operand images, one per (KV head g, block b) in that
+// order: the block's K exactly as the converters leave it in shared memory
+// (fp16, 128-byte swizzled K-major slabs), then its V (plain core matrices);
+// positions at or past N are zero.  One CTA per image; thread ct converts
+// the same 32-byte pieces a converter thread would.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
+__global__ void __launch_bounds__(kCvtThreads) prefill_stage_kernel(const Args a, uint8_t* img) {
   using L = Layout<D>;
+  const DecodeParams& p = a.p;
+  constexpr int kPairs = BN * D / 32 / kCvtThreads;
+  const int b = blockIdx.x % a.nblocks, g = blockIdx.x / a.nblocks;
+  const int ct = threadIdx.x;
+  uint8_t* dst = img + ((long long)g * a.nblocks + b) * (2 * L::kKVBytes);
+  grid_dependency_wait();  // the cache may come from the previous kernel of the stream
+#pragma unroll
+  for (int kv = 0; kv < 2; ++kv) {
+    const int8_t* src = reinterpret_cast<const int8_t*>(kv == 0 ? p.k : p.v);
+    uint8_t* out = dst + kv * L::kKVBytes;
+#pragma unroll
+    for (int k = 0; k < kPairs; ++k) {
+      const int q = ct + kCvtThreads * k;
+      const int pr = q % BN, cp = q / BN;
+      const long long pos = (long long)b * BN + pr;
+      uint4 raw[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+      if (pos < p.cache_rows) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + (pos * p.Hkv + g) * D + 32 * cp);
+        raw[0] = __ldg(s4);
+        raw[1] = __ldg(s4 + 1);
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint4 lo, hi;
+        cvt16(raw[hh], lo, hi);
+        const int c0 = 4 * cp + 2 * hh;
+        *reinterpret_cast<uint4*>(out + chunk_offset<D>(pr, c0, kv == 0)) = lo;
+        *reinterpret_cast<uint4*>(out + chunk_offset<D>(pr, c0 + 1, kv == 0)) = hi;
+      }
+    }
+  }
+}
+
+template <int D, bool STAGED>
+__global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(const Args a) {
+  using L = Layout<D>;
+  constexpr int kThreads = Roles<STAGED>::kThreads;
+  constexpr int kMmaWarp = Roles<STAGED>::kMmaWarp;
   const DecodeParams& p = a.p;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -248,9 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    tc::mbar_init(bar(kKFull), kCvtThreads);
+    tc::mbar_init(bar(kKFull), STAGED ? 1 : kCvtThreads);
     tc::mbar_init(bar(kKFree), 1);
-    tc::mbar_init(bar(kVFull), kCvtThreads);
+    tc::mbar_init(bar(kVFull), STAGED ? 1 : kCvtThreads);
     tc::mbar_init(bar(kSFull0), 1);
     tc::mbar_init(bar(kSFull1), 1);
     tc::mbar_init(bar(kPFull), 32 * kSoftWarps);
@@ -383,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
 
   // ---------------- the pipeline ----------------
   if (run_tc) {
-    if (warp >= kSoftWarps && warp < kSoftWarps + kCvtWarps) {
+    if (!STAGED && warp >= kSoftWarps && warp < kSoftWarps + kCvtWarps) {
       // ---- converters ----
       // Thread ct owns 32-byte pieces (row pr, channels 32cp .. 32cp + 31) of
       // every block's K and V: q = ct + 128k -> pr = q % BN, cp = q / BN, so
@@ -425,15 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
             cvt16(src[k][hh], lo, hi);
             // channels 32cp + 16hh .. +15: 16-byte chunks c0 = 4cp + 2hh and c0 + 1
             const int c0 = 4 * cp + 2 * hh;
-            uint32_t a0, a1;
-            if (swz) {
-              const uint32_t row = dst16 + (c0 >> 3) * L::kSlabK + pr * 128;
-              a0 = row + (((c0 & 7) ^ (pr & 7)) << 4);
-              a1 = row + ((((c0 + 1) & 7) ^ (pr & 7)) << 4);
-            } else {
-              a0 = dst16 + (pr >> 3) * L::kGroupD + (pr & 7) * 16 + c0 * 128;
-              a1 = a0 + 128;
-            }
+            const uint32_t a0 = dst16 + chunk_offset<D>(pr, c0, swz);
+            const uint32_t a1 = dst16 + chunk_offset<D>(pr, c0 + 1, swz);
             asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(a0), "r"(lo.x),
                          "r"(lo.y), "r"(lo.z), "r"(lo.w)
                          : "memory");
@@ -476,6 +531,43 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
         blk = nxt;
       }
       if (!ok) slot[kAbort] = 1;
+    } else if (STAGED && warp == Roles<STAGED>::kLoadWarp) {
+      // ---- loader (one thread): the blocks' fp16 operand images, K running
+      // one block ahead of V exactly as the converters do ----
+      if (lane == 0) {
+        constexpr uint32_t kImg = 2 * L::kKVBytes;
+        const uint8_t* img = a.stage + (long long)g * a.nblocks * kImg;
+        int nk = 0, nv = 0;  // copies issued
+        auto copy_in = [&](int blk, bool is_v) {
+          const int b = is_v ? kVFull : kKFull;
+          ++(is_v ? nv : nk);
+          tc::mbar_arrive_expect_tx(bar(b), L::kKVBytes);
+          tc::bulk_g2s(sbase + (is_v ? L::kV16 : L::kK16),
+                       img + (long long)blk * kImg + (is_v ? L::kKVBytes : 0), L::kKVBytes,
+                       bar(b));
+        };
+        bool ok = true;
+        copy_in(first, false);
+        int i = 0;
+        for (int blk = first; blk <= bhi; ++i) {
+          const int nxt = next_blk(blk);
+          if (nxt <= bhi) {
+            if (!(ok = tc::mbar_wait(bar(kKFree), i & 1, slot))) break;
+            copy_in(nxt, false);
+          }
+          if (!(ok = tc::mbar_wait(bar(kPVDone), (i & 1) ^ 1, slot))) break;
+          copy_in(blk, true);
+          blk = nxt;
+        }
+        if (!ok) slot[kAbort] = 1;
+        // every copy issued has landed before the loader leaves: the MMA
+        // thread waited for each one it used; after an abort this waits
+        // (bounded) for the others.  Only this thread arrives on the two
+        // barriers, so the last copy's phase is the latest one.
+        if (nk > 0 && !tc::mbar_wait(bar(kKFull), (nk - 1) & 1)) slot[kAbort] = 1;
+        if (nv > 0 && !tc::mbar_wait(bar(kVFull), (nv - 1) & 1)) slot[kAbort] = 1;
+      }
+      __syncwarp();
     } else if (warp == kMmaWarp) {
       // ---- MMA issue (one thread) ----
       // order: QK(0), QK(1), PV(0), QK(2), PV(1), ...: the scores of block
@@ -530,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Args a) {
         if (!tc::mbar_wait(bar(kDone), 0)) slot[kAbort] = 1;
       }
       __syncwarp();
-    } else {
+    } else if (warp < kSoftWarps) {
       // ---- softmax (one query vector per thread and column half) ----
       const uint32_t t_lane = (uint32_t)(32 * (warp & 3)) << 16;
       const uint32_t* mrow = mask + (vrow - r_lo) * a.mask_words;
@@ -765,9 +857,9 @@ bool prefill_tc_plan(int D, int G, int rows, long long N, int max_sel, int* smem
   return true;
 }
 
-template <int D>
+template <int D, bool STAGED>
 static cudaError_t run_prefill_tc(const pf::Args& a, int smem, int tiles, cudaStream_t s) {
-  auto kern = pf::prefill_tc_kernel<D>;
+  auto kern = pf::prefill_tc_kernel<D, STAGED>;
   static std::atomic<unsigned long long> done{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -778,32 +870,51 @@ static cudaError_t run_prefill_tc(const pf::Args& a, int smem, int tiles, cudaSt
     if (e != cudaSuccess) return e;
     done.fetch_or(bit);
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)tiles);
-  cfg.blockDim = dim3(pf::kThreads);
-  cfg.dynamicSmemBytes = (size_t)smem;
-  cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (STAGED) {
+    // the operand images first (their kernel waits for the previous one of
+    // the stream; the prefill kernel waits for this one)
+    cfg.gridDim = dim3((unsigned)(a.p.Hkv * a.nblocks));
+    cfg.blockDim = dim3(pf::kCvtThreads);
+    cfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&cfg, pf::prefill_stage_kernel<D>, a,
+                           const_cast<uint8_t*>(a.stage));
+    if (e != cudaSuccess) return e;
+  }
+  cfg.gridDim = dim3((unsigned)tiles);
+  cfg.blockDim = dim3(pf::Roles<STAGED>::kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
+size_t prefill_stage_bytes(long long N, int Hkv, int D) {
+  if (N < 1 || Hkv < 1 || (D != 128 && D != 256)) return 0;
+  return (size_t)Hkv * (size_t)((N + pf::BN - 1) / pf::BN) * 2 * pf::BN * D * 2;
+}
+
 cudaError_t launch_dsa_prefill_tc(const DecodeParams& p, int D, int smem, int mask_rows,
-                                  cudaStream_t s) {
+                                  void* stage, cudaStream_t s) {
   pf::Args a;
   a.p = p;
+  a.stage = static_cast<const uint8_t*>(stage);
   const long long nvec = (long long)p.rows * p.G;
   a.tiles_per_head = (int)((nvec + pf::BM - 1) / pf::BM);
   a.mask_rows = mask_rows;
   a.mask_words = (int)((p.cache_rows + 31) / 32);
   a.nblocks = (int)((p.cache_rows + pf::BN - 1) / pf::BN);
   const long long tiles = (long long)a.tiles_per_head * p.Hkv;
-  if (tiles > INT32_MAX) return cudaErrorInvalidValue;
-  return D == 256 ? run_prefill_tc<256>(a, smem, (int)tiles, s)
-                  : run_prefill_tc<128>(a, smem, (int)tiles, s);
+  if (tiles > INT32_MAX || (long long)a.nblocks * p.Hkv > INT32_MAX) return cudaErrorInvalidValue;
+  if (stage != nullptr)
+    return D == 256 ? run_prefill_tc<256, true>(a, smem, (int)tiles, s)
+                    : run_prefill_tc<128, true>(a, smem, (int)tiles, s);
+  return D == 256 ? run_prefill_tc<256, false>(a, smem, (int)tiles, s)
+                  : run_prefill_tc<128, false>(a, smem, (int)tiles, s);
 }
 
 }  // namespace i8kv

@@ -39,6 +39,26 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
       : "memory");
 }
 
+// Arrive and add `bytes` to the transaction count of the current phase: the
+// phase completes once the arrivals are in and that many bytes have landed.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 st, [%0], %1;\n}\n"
+      ::"r"(bar), "r"(bytes)
+      : "memory");
+}
+
+// Bulk copy global -> shared (the async proxy): `bytes` (a multiple of 16,
+// both addresses 16-byte aligned) land at dst and count toward bar's
+// transaction bytes.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

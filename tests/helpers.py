@@ -44,17 +44,23 @@ def _unpack_partials(ws, units, ns, G, D):
     return m, l, acc
 
 
-def run_dsa(c, d=None, num_splits=0, chunk=0, prefill=False, flags=None, partials=False):
+def run_dsa(c, d=None, num_splits=0, chunk=0, prefill=False, flags=None, partials=False,
+            staged=False):
     """Sparse decode (or prefill) through the binding: (O, lse) as float64, or
-    with ``partials`` the workspace partials of a partials-only decode call."""
+    with ``partials`` the workspace partials of a partials-only decode call.
+    ``staged``: the prefill with a workspace (filled with 0xFF bytes first)."""
     d = d or sparse_to_device(c)
     S, Hq, D = c.q.shape
     Hkv = c.k_codes.shape[1]
     out = torch.full((S, Hq, D), float("nan"), dtype=torch.float16, device="cuda")
     lse = torch.full((S, Hq), float("nan"), dtype=torch.float32, device="cuda")
     if prefill:
+        ws = None
+        if staged:
+            wsb = K.prefill_workspace_bytes(S, Hq, Hkv, D, c.k_codes.shape[0], c.idx.shape[1])
+            ws = torch.full((max(wsb, 16),), 255, dtype=torch.uint8, device="cuda")
         K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"], c.sigma,
-                      d["sink"], out=out, lse=lse, flags=flags)
+                      d["sink"], out=out, lse=lse, flags=flags, workspace=ws)
     else:
         ns = num_splits
         if ns == 0:

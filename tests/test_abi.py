@@ -194,3 +194,27 @@ def test_paged_decode_ex_validation(lib):
     assert call(window=0, ns=1, chunk=16) == 0
     assert call(window=-1, ns=1, chunk=128) == 1        # no window: the cap 512
     assert call(window=5000, ns=1, chunk=496) == 1      # wide window: the cap
+
+
+def test_prefill_workspace_rules(lib):
+    # host arithmetic: the staged prefill's workspace is the cache as fp16
+    # operand images (Hkv x ceil(N / 128) blocks x K and V x 128 x D x 2 bytes),
+    # and only for the shapes the tensor-core kernel serves
+    need = lib.dsa_prefill_workspace_bytes
+    assert need(16, 24, 2, 256, 300, 100) == 2 * 3 * 2 * 128 * 256 * 2
+    assert need(2048, 24, 2, 256, 8192, 2048) == 2 * 64 * 2 * 128 * 256 * 2
+    assert need(16, 8, 2, 128, 1000, 300) == 2 * 8 * 2 * 128 * 128 * 2
+    assert need(16, 24, 2, 256, 3000, 100) == 0   # 4 * max_sel < N: the gathering kernel
+    assert need(16, 8, 2, 64, 300, 100) == 0      # head_dim 64: the gathering kernel
+    assert need(0, 24, 2, 256, 300, 100) == 0
+    assert need(16, 24, 5, 256, 300, 100) == 0    # Hq not a multiple of Hkv
+
+
+def test_prefill_workspace_errors_before_any_launch(lib):
+    # checked before anything touches the device: the addresses are never read
+    fake = 1 << 20
+    args = [fake, fake, fake, fake, fake, 2, fake, 16, 24, 2, 256, 300, 100, 1.0 / 16, None]
+    tail = [fake, None, None, None]
+    need = lib.dsa_prefill_workspace_bytes(16, 24, 2, 256, 300, 100)
+    assert lib.dsa_prefill_ws(*args, fake, need - 16, *tail) == 4   # I8KV_EWORKSPACE
+    assert lib.dsa_prefill_ws(*args, fake + 8, need, *tail) == 3    # I8KV_EALIGN

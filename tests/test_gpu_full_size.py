@@ -82,9 +82,10 @@ def test_deep_context_full_size(cache):
         assert_lse_close(l, l1, 1e-4)
 
 
-def test_sparse_prefill_full_size_sampled_rows():
+@pytest.mark.parametrize("staged", [False, True], ids=["converting", "staged"])
+def test_sparse_prefill_full_size_sampled_rows(staged):
     c = W.sparse_prefill(seed=0)
-    o, l = run_dsa(c, prefill=True)
+    o, l = run_dsa(c, prefill=True, staged=staged)
     rows = np.linspace(0, c.q.shape[0] - 1, 64).astype(np.int64)
     sub = dataclasses.replace(c, q=c.q[rows], idx=c.idx[rows])
     ref_o, ref_l = oracle_dsa(sub)

@@ -28,10 +28,17 @@ def _flags():
     return torch.zeros(1, dtype=torch.int32, device="cuda")
 
 
-def _run(c):
+def _run(c, staged=False):
     f = _flags()
-    o, l = run_dsa(c, prefill=True, flags=f)
+    o, l = run_dsa(c, prefill=True, flags=f, staged=staged)
     return o, l, int(f.item())
+
+
+# both forms of the kernel: converting the int8 cache in every CTA, and staged
+# (fp16 operand images made once per call in a workspace)
+@pytest.fixture(params=[False, True], ids=["converting", "staged"])
+def staged(request):
+    return request.param
 
 
 @pytest.mark.parametrize("S,Hq,Hkv,D,N,max_sel,kind", [
@@ -40,17 +47,17 @@ def _run(c):
     (3, 2, 2, 256, 500, 200, W.SCALE_PER_CHANNEL),     # G = 1: a tile spans 128 rows
     (130, 1, 1, 128, 256, 64, W.SCALE_PER_CHANNEL),    # G = 1, two tiles
 ])
-def test_unsorted_lists_with_invalid_entries(S, Hq, Hkv, D, N, max_sel, kind):
+def test_unsorted_lists_with_invalid_entries(S, Hq, Hkv, D, N, max_sel, kind, staged):
     c = W.random_sparse(seed=S * 7 + D, S=S, Hq=Hq, Hkv=Hkv, D=D, N=N, max_sel=max_sel,
                         invalid_frac=0.15, scale_kind=kind, sink=True, sigma=1.0 / 16)
     ref_o, ref_l = oracle_dsa(c)
-    o, l, f = _run(c)
+    o, l, f = _run(c, staged)
     assert not f & WAIT_TIMEOUT
     assert_close_oracle(o, ref_o, "dense prefill")
     assert_lse_oracle(l, ref_l, bound_of(c))
 
 
-def test_repeated_entries_and_empty_rows():
+def test_repeated_entries_and_empty_rows(staged):
     c = W.random_sparse(seed=11, S=24, Hq=24, Hkv=2, D=256, N=600, max_sel=256, sink=True,
                         sigma=1.0 / 16)
     c.idx[3, 10:20] = c.idx[3, 0:10]        # row 3 lists ten candidates twice
@@ -58,7 +65,7 @@ def test_repeated_entries_and_empty_rows():
     c.idx[12, :] = -1                       # row 12 attends nothing
     c.idx[13, :] = 600 + np.arange(256)     # row 13: every entry out of range
     ref_o, ref_l = oracle_dsa(c)
-    o, l, f = _run(c)
+    o, l, f = _run(c, staged)
     assert f & FP32_PATH                     # the repeating rows took the FP32 path
     assert not f & WAIT_TIMEOUT
     assert_close_oracle(o, ref_o, "repeated entries")
@@ -79,7 +86,7 @@ def test_matches_the_decode_kernel_on_the_same_rows():
 
 
 @pytest.mark.parametrize("q0,vs,fp32", [(336.0, 2.0 ** 28, True), (320.0, 2.0 ** 28, False)])
-def test_tail_depth_rule(q0, vs, fp32):
+def test_tail_depth_rule(q0, vs, fp32, staged):
     """A candidate 21 nats below the maximum under a value scale of 2^28 goes to
     the FP32 path; exactly 20 nats down stays on the tensor cores."""
     c = W.tiny_probability_case(q0, 1, vs, D=128)
@@ -87,7 +94,7 @@ def test_tail_depth_rule(q0, vs, fp32):
     c.k_codes = np.concatenate([c.k_codes] * 2, axis=1)
     c.v_codes = np.concatenate([c.v_codes] * 2, axis=1)
     ref_o, ref_l = oracle_dsa(c)
-    o, l, f = _run(c)
+    o, l, f = _run(c, staged)
     assert bool(f & FP32_PATH) == fp32
     assert np.all(np.abs(o - ref_o) <= 2e-3 + 1e-2 * np.abs(ref_o))
     assert_lse_close(l, ref_l, 1e-5)
@@ -99,13 +106,13 @@ def test_tail_depth_rule(q0, vs, fp32):
     (4, 8, 2, 256, 2000, 300),     # 4 * max_sel < N: the gathering kernel serves it
     (6, 8, 2, 64, 200, 100),       # head_dim 64: the gathering kernel serves it
 ])
-def test_shapes_on_either_kernel(S, Hq, Hkv, D, N, max_sel):
+def test_shapes_on_either_kernel(S, Hq, Hkv, D, N, max_sel, staged):
     c = W.random_sparse(seed=S + N, S=S, Hq=Hq, Hkv=Hkv, D=D, N=N, max_sel=max_sel,
                         invalid_frac=0.05, sink=True, sigma=1.0 / 16)
     if N == 129:
         c.idx[0, 0] = 128  # the only position of the last block
     ref_o, ref_l = oracle_dsa(c)
-    o, l, f = _run(c)
+    o, l, f = _run(c, staged)
     assert not f & WAIT_TIMEOUT
     assert_close_oracle(o, ref_o, "prefill shape")
     assert_lse_oracle(l, ref_l, bound_of(c))
@@ -141,3 +148,38 @@ def test_prefill_can_be_captured_and_replayed():
     torch.cuda.synchronize()
     assert torch.equal(out, eager)
     assert not torch.equal(flipped, eager)
+
+
+@pytest.mark.parametrize("S,Hq,Hkv,D,N,max_sel", [
+    (37, 24, 2, 256, 700, 400), (20, 8, 2, 128, 1000, 300), (130, 1, 1, 128, 256, 64),
+])
+def test_staged_form_is_bit_identical(S, Hq, Hkv, D, N, max_sel):
+    # the operand images hold exactly what the converters write, and the
+    # products and the softmax are the same code: the outputs agree bit for bit
+    c = W.random_sparse(seed=S + 3, S=S, Hq=Hq, Hkv=Hkv, D=D, N=N, max_sel=max_sel,
+                        invalid_frac=0.1, sink=True, sigma=1.0 / 16)
+    o1, l1, f1 = _run(c, False)
+    o2, l2, f2 = _run(c, True)
+    assert f1 == f2
+    assert np.array_equal(o1, o2, equal_nan=True)
+    assert np.array_equal(l1, l2, equal_nan=True)
+
+
+def test_staged_workspace_is_sized_and_checked():
+    import ctypes
+    import int8_kv_cache_gb300 as K
+    from helpers import sparse_to_device
+    c = W.random_sparse(seed=8, S=16, Hq=24, Hkv=2, D=256, N=300, max_sel=100, sigma=1.0 / 16)
+    need = K.prefill_workspace_bytes(16, 24, 2, 256, 300, 100)
+    assert need == 2 * 3 * 2 * 128 * 256 * 2  # Hkv x blocks x (K, V) x 128 x D x fp16
+    d = sparse_to_device(c)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    with pytest.raises(K.Int8KVError, match="workspace"):
+        K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"], c.sigma,
+                      workspace=ws[: need - 16])
+    with pytest.raises(K.Int8KVError):
+        K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"], c.sigma,
+                      workspace=ws[8:])  # not 16-byte aligned
+    # the gathering kernel's shapes need none (and ignore one)
+    assert K.prefill_workspace_bytes(16, 24, 2, 256, 3000, 100) == 0
+    assert K.prefill_workspace_bytes(16, 8, 2, 64, 300, 100) == 0
