@@ -613,6 +613,8 @@ def extra_configs(torch, K, W, np, dev, stream, peaks, args):
 
     if args.extra in ("all", "paged"):
         res["paged_decode"] = _paged(torch, K, W, np, t, dev, bench_graph, hbm)
+        res["paged_decode_balanced"] = _paged(torch, K, W, np, t, dev, bench_graph, hbm,
+                                              balanced=True)
     if args.extra in ("all", "paged", "variants"):
         res["paged_decode_softcap"] = _paged(torch, K, W, np, t, dev, bench_graph, hbm,
                                              softcap=30.0)
@@ -663,9 +665,11 @@ def _quantize(torch, K, np, t, dev, bench_graph, hbm, cache="int8"):
                 rotating_sets=R)
 
 
-def _paged(torch, K, W, np, t, dev, bench_graph, hbm, softcap=0.0, window=-1, cache="int8"):
+def _paged(torch, K, W, np, t, dev, bench_graph, hbm, softcap=0.0, window=-1, cache="int8",
+           balanced=False):
     """Paged decode: 16 sequences, lengths U[512, 8192], 32/8 heads, D 128
-    (optionally with a softcap and a sliding window, or a float8 e4m3fn cache)."""
+    (optionally with a softcap and a sliding window, or a float8 e4m3fn cache;
+    with ``balanced``, the balanced pieces instead of the wave rule's chunks)."""
     c = W.paged_decode(seed=0, cache=cache)
     dt = K.CACHE_FP8 if cache == "fp8" else K.CACHE_INT8
     B, Hq, Dh = c.q.shape
@@ -676,7 +680,8 @@ def _paged(torch, K, W, np, t, dev, bench_graph, hbm, softcap=0.0, window=-1, ca
     q, ks, vs = t(c.q), t(c.k_scale), t(c.v_scale)
     bt, lens, sink = t(c.block_table), t(c.seq_lens), t(c.sink)
     ns, chunk, wsb, wave = K.decode_plan(K.PATH_PAGED, dt, K.window_span(cap, window),
-                                         B, Hq, Hkv, Dh, K.GEOM_WAVE)
+                                         B, Hq, Hkv, Dh,
+                                         K.GEOM_BALANCED if balanced else K.GEOM_WAVE)
     ws = torch.empty(max(wsb // 4, 4), dtype=torch.float32, device=dev)
     out = torch.empty_like(q)
     live = np.minimum(c.seq_lens, window + 1) if window >= 0 else c.seq_lens
@@ -692,6 +697,8 @@ def _paged(torch, K, W, np, t, dev, bench_graph, hbm, softcap=0.0, window=-1, ca
                            window=window)
     sec = bench_graph(fn, R)
     opts = ""
+    if balanced:
+        opts += ", balanced pieces (device-cut, about one wave)"
     if softcap > 0:
         opts += f", softcap {softcap:g}"
     if window >= 0:

@@ -73,6 +73,7 @@ typedef enum {
 
 #define I8KV_GEOM_WAVE 0       /* onnx-genai PR 1350 rule (num_splits from one wave)        */
 #define I8KV_GEOM_POW2_TILES 1 /* onnxruntime PR 33707 rule (power-of-two tiles per split)  */
+#define I8KV_GEOM_BALANCED 2   /* decode_plan, paged path: balanced pieces (see paged_decode) */
 
 #define I8KV_PATH_DSA 1   /* sparse-candidate decode kernel */
 #define I8KV_PATH_PAGED 2 /* paged decode kernel            */
@@ -148,6 +149,9 @@ size_t split_workspace_bytes(int32_t units, int32_t num_splits, int32_t G, int32
  *   split_geometry.  wave_ctas = SM count x resident CTAs per SM of the
  *   selected decode kernel (queried from the CUDA occupancy API and cached per
  *   device); granule = 64 (POW2_TILES) or 16 (WAVE); min_chunk = 128;
+ *   mode I8KV_GEOM_BALANCED (paged path only, else I8KV_EUNSUPPORTED):
+ *   num_splits = min(32, max(2, 2 x the WAVE rule's automatic count)) partial
+ *   slots and chunk = 0, for paged_decode's balanced pieces;
  *   max_splits = I8KV_MAX_SPLITS.  For the paged path in WAVE mode with
  *   override_value 0 the chunk is then moved to the multiple of one round of
  *   the paged kernel's CTA (4 warps x its step: 128 positions for an int8 or
@@ -260,7 +264,17 @@ i8kv_status dsa_prefill_ws(const uint16_t* q, const int8_t* k_cache, const int8_
  *                cap = max_blocks * block_size (I8KV_FLAG_LEN_CLAMPED)
  *   block_size   a multiple of 16
  *   num_splits, chunk  as for dsa_decode over token positions, with cap =
- *                max_blocks*block_size; num_splits = 0: automatic (WAVE rule)
+ *                max_blocks*block_size; num_splits = 0: automatic (WAVE rule).
+ *                num_splits in [2, 32] with chunk = 0: balanced pieces (not on
+ *                the pages; decode_plan's I8KV_GEOM_BALANCED gives the values):
+ *                num_splits partial slots per row and ceil(num_splits / 2)
+ *                CTAs per (row, KV head), all fixed by the arguments, while
+ *                each CTA cuts its piece of a row's live range on the device
+ *                from all live lengths, so that the pieces are about equally
+ *                long across a ragged batch (about one occupancy wave of
+ *                them); the combine merges the used slots, the others are
+ *                marked empty.  Needs B <= 128 and slots_out NULL
+ *                (I8KV_EUNSUPPORTED otherwise).
  *   slots_out    [B, cap] int32 or NULL       debug output: the gathered row of
  *                every token position, -1 past the live length
  *   other arguments as for dsa_decode.

@@ -23,7 +23,7 @@ __all__ = [
     "FLAG_BAD_SLOT", "FLAG_FP32_PATH", "FLAG_WAIT_TIMEOUT", "paged_decode_ex", "window_span",
     "CACHE_FP8", "fp8_to_fp16",
     "SCALE_PER_TENSOR", "SCALE_PER_CHANNEL", "CACHE_INT8", "CACHE_FP16", "GEOM_WAVE",
-    "GEOM_POW2_TILES", "PATH_DSA", "PATH_PAGED", "MAX_SPLITS", "FLAG_LEN_CLAMPED",
+    "GEOM_POW2_TILES", "GEOM_BALANCED", "PATH_DSA", "PATH_PAGED", "MAX_SPLITS", "FLAG_LEN_CLAMPED",
     "FLAG_QUERY_RANGE", "FLAG_BAD_BLOCK",
 ]
 
@@ -34,6 +34,7 @@ CACHE_FP16 = 2
 CACHE_FP8 = 3
 GEOM_WAVE = 0
 GEOM_POW2_TILES = 1
+GEOM_BALANCED = 2
 PATH_DSA = 1
 PATH_PAGED = 2
 MAX_SPLITS = 32

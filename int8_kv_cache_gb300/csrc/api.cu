@@ -324,8 +324,18 @@ i8kv_status decode_plan(int32_t path, int32_t cache_dtype, int64_t cap, int32_t 
   const KernelKey key = make_key(path == I8KV_PATH_DSA ? Path::kDsa : Path::kPaged, D, G,
                                  cache_dtype, true);
   const int32_t units = std::max(1, rows * Hkv);
-  if ((st = plan(key, cap, units, mode, override_value, num_splits, chunk, wave_ctas)) != I8KV_OK)
+  if (mode == I8KV_GEOM_BALANCED) {
+    // balanced pieces: twice the wave rule's splits as partial slots (at most
+    // MAX_SPLITS), chunk 0 (the pieces are cut on the device)
+    if (path != I8KV_PATH_PAGED) return I8KV_EUNSUPPORTED;
+    if ((st = plan(key, cap, units, I8KV_GEOM_WAVE, 0, num_splits, chunk, wave_ctas)) != I8KV_OK)
+      return st;
+    *num_splits = std::min<int32_t>(I8KV_MAX_SPLITS, std::max<int32_t>(2, 2 * *num_splits));
+    *chunk = 0;
+  } else if ((st = plan(key, cap, units, mode, override_value, num_splits, chunk, wave_ctas)) !=
+             I8KV_OK) {
     return st;
+  }
   *workspace_bytes = split_workspace_bytes(rows * Hkv, *num_splits, G, D);
   return I8KV_OK;
 }
@@ -454,8 +464,15 @@ i8kv_status paged_common(const uint16_t* q, const void* k_cache, const void* v_c
     st = plan(key, span, std::max(1, B * Hkv), I8KV_GEOM_WAVE, 0, &num_splits, &chunk, nullptr);
     if (st != I8KV_OK) return st;
   }
-  if ((st = check_geometry(span, num_splits, chunk, window >= 0 ? cap : 0)) != I8KV_OK)
+  // chunk 0 with num_splits > 1: balanced pieces cut on the device (at most
+  // num_splits per row)
+  const bool balanced = num_splits > 1 && chunk == 0;
+  if (balanced) {
+    if (num_splits > I8KV_MAX_SPLITS) return I8KV_EINVAL;
+    if (slots_out != nullptr || B > i8kv::kLptMaxRows) return I8KV_EUNSUPPORTED;
+  } else if ((st = check_geometry(span, num_splits, chunk, window >= 0 ? cap : 0)) != I8KV_OK) {
     return st;
+  }
   DecodeParams p{};
   if ((st = set_workspace(p, workspace, workspace_bytes, B * Hkv, num_splits, G, D)) != I8KV_OK)
     return st;
@@ -491,7 +508,17 @@ i8kv_status paged_common(const uint16_t* q, const void* k_cache, const void* v_c
   p.window = window;
   // longest-first dispatch: ragged batches of long chunks (a property of the
   // geometry, so eager and captured launches make the same choice)
-  p.lpt = B <= i8kv::kLptMaxRows && chunk >= i8kv::kLptMinChunk;
+  p.lpt = !balanced && B <= i8kv::kLptMaxRows && chunk >= i8kv::kLptMinChunk;
+  if (balanced) {
+    // about one wave of CTAs over the KV heads, at least one piece per row,
+    // at most what the grid of ceil(num_splits / 2) CTAs per unit holds
+    WaveInfo w{0, 0};
+    if ((st = wave_of(key, &w)) != I8KV_OK) return st;
+    p.balanced = 1;
+    p.bal_round = w.round;
+    p.bal_pieces = std::min<int32_t>(std::max<int32_t>(w.wave / Hkv, B),
+                                     B * ((num_splits + 1) / 2));
+  }
   return run(key, p, static_cast<cudaStream_t>(stream));
 }
 

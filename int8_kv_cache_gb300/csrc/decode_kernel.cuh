@@ -144,7 +144,7 @@ constexpr float kMaxValueScale = 65536.f;    // |value_scale| above which the ta
 
 template <int D, bool PAGED, bool FP16C, bool FP8, int kThreads>
 __device__ __noinline__ void attend_fp32(const DecodeParams p, float* q32, const float* svs,
-                                         int unit, int split) {
+                                         int unit, int split, int chunk) {
   constexpr int kWarps = kThreads / 32;
   constexpr int C = D / 32;  // channels per lane
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -159,8 +159,8 @@ __device__ __noinline__ void attend_fp32(const DecodeParams p, float* q32, const
     len = min(max(p.seq_lens[row], 0), cap);
     if (p.window >= 0) wlo = max(0, len - 1 - p.window);
   }
-  const int lo = (wlo & ~15) + split * p.chunk;
-  const int hi = min(min(lo + p.chunk, cap), len);
+  const int lo = (wlo & ~15) + split * chunk;
+  const int hi = min(min(lo + chunk, cap), len);
   // Q * k_scale in fp32, not rounded to fp16
   const __half* qrow =
       reinterpret_cast<const __half*>(p.q) + ((long long)row * p.Hq + g * G) * D;
@@ -394,6 +394,105 @@ static __device__ __noinline__ int2 lpt_item(const DecodeParams p, int pos) {
   return make_int2(blockIdx.x, blockIdx.y);  // not reached: the ranks cover the grid
 }
 
+// ---------------------------------------------------------------------------
+// Balanced pieces (paged, chunk 0 on the API).  The split geometry of the
+// pages fixes a chunk from the capacity, so a ragged batch's longest rows
+// carry chunks of the full length while the short rows' CTAs finish early.
+// Here the grid and the partial slots still come from the capacity and the
+// row count alone (capture-safe), but each CTA derives its piece on the device
+// from all live lengths: row b gets n_b = min(S, 1 + floor(eff_b * (P - B) /
+// sum eff)) pieces (S partial slots per row, P the (row, piece) pairs the
+// batch may use, about one wave of CTAs over the KV heads), each
+// ceil(eff_b / n_b) rounded up to the CTA's round of positions, and n_b
+// recomputed from that.  The pieces are dealt piece-index-major: all rows'
+// first pieces, then the second pieces of the rows that have one, ...  CTA c
+// also marks the partial slots 2c and 2c + 1 (unit-major) empty when no piece
+// uses them, so the combine sees (m = -inf, l = 0) there.
+// Returns (unit, piece, piece length, 1), or (.., 0) for a CTA without a piece.
+// ---------------------------------------------------------------------------
+static __device__ __noinline__ int4 balanced_item(const DecodeParams p, int c) {
+  constexpr int J = kLptMaxRows / 32;  // rows per lane: lane, lane + 32, ...
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int B = p.rows, Hkv = p.Hkv, S = p.num_splits, rnd = p.bal_round;
+  const int cap = p.max_blocks * p.bs;
+  const int jn = (B + 31) / 32;
+  int eff[J], n[J], pl[J];
+  bool has[J];
+  long long tot = 0;
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int r = lane + 32 * j;
+    has[j] = r < B;
+    eff[j] = 0;
+    if (has[j]) {
+      const int live = min(max(p.seq_lens[r], 0), cap);
+      const int base = p.window >= 0 ? (max(0, live - 1 - p.window) & ~15) : 0;
+      eff[j] = live - base;
+    }
+    tot += eff[j];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  const int extra = max(p.bal_pieces - B, 0);
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    int k = 1 + (tot > 0 ? (int)((long long)eff[j] * extra / tot) : 0);
+    k = min(k, S);
+    pl[j] = eff[j] > 0 ? (eff[j] + k - 1) / k : rnd;
+    pl[j] = (pl[j] + rnd - 1) / rnd * rnd;
+    n[j] = eff[j] > 0 ? (eff[j] + pl[j] - 1) / pl[j] : 1;
+  }
+  // value of row r's entry of a per-lane array (every lane takes part)
+  auto of_row = [&](const int (&a)[J], int r) -> int {
+    int out = 0;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int v = __shfl_sync(0xffffffffu, a[j], r & 31);
+      if (j == r / 32) out = v;
+    }
+    return out;
+  };
+  // the partial slots 2c, 2c + 1 that no piece fills: empty
+  if (warp == 0) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const long long t = 2LL * c + e;
+      const int u = (int)(t / S), k = (int)(t - (long long)u * S);
+      const int nu = u < B * Hkv ? of_row(n, u / Hkv) : 0;  // (uniform over the warp)
+      if (u < B * Hkv && k >= nu && lane < p.G) {
+        const long long sb = ((long long)u * S + k) * p.G + lane;
+        p.ws_m[sb] = neg_inf();
+        p.ws_l[sb] = 0.f;
+      }
+    }
+  }
+  // piece-index-major order: round k holds the rows with more than k pieces
+  int cum = 0;
+  for (int k = 0; k < S; ++k) {
+    unsigned m[J];
+    int cnt = 0;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      m[j] = j < jn ? __ballot_sync(0xffffffffu, has[j] && n[j] > k) : 0u;
+      cnt += __popc(m[j]);
+    }
+    if (cnt == 0) break;
+    if (c < cum + Hkv * cnt) {
+      const int q = c - cum;
+      int rank = q / Hkv, r = -1;
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const int cj = __popc(m[j]);
+        if (r < 0 && rank < cj) r = 32 * j + nth_set_lane(m[j], rank);
+        if (r < 0) rank -= cj;
+      }
+      return make_int4(r * Hkv + q % Hkv, k, of_row(pl, r), 1);
+    }
+    cum += Hkv * cnt;
+  }
+  return make_int4(0, 0, 0, 0);
+}
+
 template <int D, int NT, bool PAGED, bool FP16C, bool PLO, bool FP8>
 __global__ void __launch_bounds__((Tile<D, NT, FP16C, PAGED>::kThreads),
                                   (Tile<D, NT, FP16C, PAGED>::kMinBlocks))
@@ -453,7 +552,7 @@ decode_kernel(const DecodeParams p) {
       return pos < end ? __ldg(p.idx + (long long)row_ * p.max_sel + pos) : -1;
     }
   };
-  auto setup = [&](int unit_, int split_, Item& it) {
+  auto setup = [&](int unit_, int split_, int chunk_, Item& it) {
     it.unit = unit_;
     it.split = split_;
     it.row = unit_ / p.Hkv;
@@ -503,20 +602,26 @@ decode_kernel(const DecodeParams p) {
         it.base = it.wlo & ~15;
       }
     }
-    it.lo = it.base + split_ * p.chunk;
-    it.nhi = min(it.lo + p.chunk, cap);  // nominal end (capacity-bounded)
+    it.lo = it.base + split_ * chunk_;
+    it.nhi = min(it.lo + chunk_, cap);  // nominal end (capacity-bounded)
     // the first keys, fetched against the nominal end before the live length
     // of a paged sequence is known
 #pragma unroll
     for (int k = 0; k <= T::kStages; ++k) it.pf[k] = key_of(it.row, it.lo, it.nhi, k);
   };
   Item it;
-  {
+  int chunk = p.chunk;  // the CTA's piece length (balanced pieces: its own)
+  if (PAGED && p.balanced) {
+    const int4 x = balanced_item(p, blockIdx.y * gridDim.x + blockIdx.x);
+    if (!x.w) return;  // no piece for this CTA (uniform: every warp computes the same)
+    chunk = x.z;
+    setup(x.x, x.y, chunk, it);
+  } else {
     // one call site: the natural item, then (paged, rarely) the dispatched one
     int u = blockIdx.x, sp = blockIdx.y;
 #pragma unroll 1
     for (int pass = 0;; ++pass) {
-      setup(u, sp, it);
+      setup(u, sp, chunk, it);
       if constexpr (!PAGED) {
         break;
       } else {
@@ -740,7 +845,7 @@ decode_kernel(const DecodeParams p) {
     __syncthreads();  // every warp's gathers have landed: the ring is free
     if (threadIdx.x == 0) flag_or(p.flags, I8KV_FLAG_FP32_PATH);
     attend_fp32<D, PAGED, FP16C, FP8, kThreads>(p, reinterpret_cast<float*>(smem), svs, unit,
-                                                split);
+                                                split, chunk);
     return;
   }
   // B fragments of Q'^T (k = channel, n = head) in the contraction order of the
@@ -1038,7 +1143,7 @@ decode_kernel(const DecodeParams p) {
   if (vs_big_cta && __syncthreads_or(deep)) {
     if (threadIdx.x == 0) flag_or(p.flags, I8KV_FLAG_FP32_PATH);
     attend_fp32<D, PAGED, FP16C, FP8, kThreads>(p, reinterpret_cast<float*>(smem), svs, unit,
-                                                split);
+                                                split, chunk);
     return;
   }
 

@@ -38,7 +38,9 @@ cudaError_t run_decode(const DecodeParams& p, cudaStream_t s, KernelInfo* info) 
                                                          T::kSmem);
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.rows * p.Hkv), (unsigned)p.num_splits);
+  // (balanced pieces: ceil(num_splits / 2) CTAs per unit for num_splits slots)
+  cfg.gridDim = dim3((unsigned)(p.rows * p.Hkv),
+                     (unsigned)(p.balanced ? (p.num_splits + 1) / 2 : p.num_splits));
   cfg.blockDim = dim3(T::kThreads);
   cfg.dynamicSmemBytes = T::kSmem;
   cfg.stream = s;

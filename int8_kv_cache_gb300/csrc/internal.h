@@ -37,6 +37,14 @@ struct DecodeParams {
   float softcap;             // paged: > 0 caps scores to softcap * tanh(s / softcap); 0 off
   int32_t window;            // paged: >= 0 attends [len - 1 - window, len); -1 off
   int32_t lpt;               // paged: longest-first dispatch of the (unit, split) items
+  // paged, balanced pieces (chunk 0 on the API): the live lengths are cut on
+  // the device into pieces of about equal length across the batch, at most
+  // num_splits per row (the partial slots), bal_pieces (row, piece) pairs in
+  // all, each a multiple of bal_round positions; the grid has
+  // ceil(num_splits / 2) CTAs per unit (decode_kernel.cuh, balanced_item)
+  int32_t balanced;
+  int32_t bal_round;
+  int32_t bal_pieces;
 };
 
 // Longest-first dispatch of the paged decode (decode_kernel.cuh, lpt_item):
