@@ -295,10 +295,12 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
   // ---------------- the tile ----------------
   const int G = p.G, Hkv = p.Hkv;
   const long long N = p.cache_rows;
-  const int tile = gridDim.x - 1 - blockIdx.x;  // later rows (longer causal lists) first
-  const int g = tile / a.tiles_per_head;
+  // later rows (longer causal lists) first, the KV heads interleaved, so that
+  // the CTAs start in about decreasing order of work across the whole grid
+  const int g = blockIdx.x % Hkv;
+  const int t_in_head = a.tiles_per_head - 1 - blockIdx.x / Hkv;
   const long long nvec = (long long)p.rows * G;
-  const long long v0 = (long long)(tile - g * a.tiles_per_head) * BM;
+  const long long v0 = (long long)t_in_head * BM;
   const int r_lo = (int)(v0 / G);
   const int r_hi = (int)((v0 + BM - 1 < nvec ? v0 + BM - 1 : nvec - 1) / G);
   const int nrows = r_hi - r_lo + 1;
