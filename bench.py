@@ -548,7 +548,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
                 "traffic": ncu_traffic("deep_context_int8"),
                 "kernel": "decode_kernel<128,1,paged,int8,hi+lo>", "us_per_launch": a["kernel_us"],
                 "bytes_per_launch": kb, "us_per_call": a["us_per_call"],
-                "workload": deep["workload"] + ", automatic geometry (wave rule, chunk on the 64-position CTA round)",
+                "workload": deep["workload"] + ", automatic geometry (wave rule, chunk on the CTA round of positions)",
                 "peak_source": f"{peak_src} hbm_gbs"}
     return out
 
