@@ -31,20 +31,27 @@
 // (p <= e^0.5 keeps p * 2^15 under the fp16 maximum), so O is rescaled on few
 // blocks; O, the row sum and lse all use that base, so the result is the same.
 //
-// Warp roles (544 threads, one CTA per SM):
+// Warp roles (one CTA per SM), in two forms:
 //   warps 0-7  softmax and epilogue; warps q and q + 4 own query vectors
 //              32q .. 32q + 31 of the tile (tensor-memory lanes), warp q the
 //              first 64 positions of a block and the first D/2 output channels,
 //              warp q + 4 the others; the pair exchanges its block maxima (and
 //              at the end its row sums) through shared memory.
+//   converting form (544 threads; dsa_prefill without a workspace):
 //   warps 8-15 converters: load the raw int8 K and V rows of a block into
 //              registers (one block ahead), convert them exactly to fp16 (K as
 //              the K-major B operand of QK^T, V as the MN-major B operand of
 //              PV), signal the MMA thread.
+//   warp 16    lane 0 issues the MMAs; the warp owns the tensor memory.
+//   staged form (320 threads; dsa_prefill_ws): prefill_stage_kernel first
+//              writes every block's fp16 K and V exactly as the converters
+//              would lay them out in shared memory;
+//   warp 8     lane 0 issues the MMAs; the warp owns the tensor memory;
+//   warp 9     lane 0 brings each K or V block in with one bulk copy (the
+//              mbarrier counts the bytes), K one block ahead of V.
 // (An MMA instruction costs the same up to N = 128 columns and about twice as
 // much at N = 256, measured on this part: 128-token blocks keep QK^T at N=128
 // instead of wasting half of every instruction at N = 64.)
-//   warp 16    lane 0 issues the MMAs; the warp owns the tensor memory.
 // Hand-offs are mbarriers: every wait is bounded (about a second, or at once
 // after another thread gave up); a CTA that gives up writes NaN for its
 // outputs and raises I8KV_FLAG_WAIT_TIMEOUT instead of hanging.
