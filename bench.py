@@ -279,11 +279,12 @@ def measured_peaks():
             "fallback"
 
 
-def kernel_sources_digest():
-    """Digest of the decode kernel's code (comments and blank lines dropped, so
-    that only a change of the code itself retires a committed ncu figure)."""
+def kernel_sources_digest(files=("decode_kernel.cuh", "device.cuh")):
+    """Digest of a kernel's code (comments and blank lines dropped, so that only
+    a change of the code itself retires a committed ncu figure); by default the
+    decode kernel's."""
     h = hashlib.sha256()
-    for f in ("decode_kernel.cuh", "device.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "int8_kv_cache_gb300", "csrc", f)) as fh:
             for line in fh:
                 code = line.split("//", 1)[0].strip()
@@ -301,9 +302,14 @@ def ncu_traffic(name: str):
     except OSError:
         return None
     e = d.get(name)
-    if not e or e.get("kernel_digest") != kernel_sources_digest():
+    files = PREFILL_SOURCES if name.startswith("sparse_prefill") else ("decode_kernel.cuh",
+                                                                       "device.cuh")
+    if not e or e.get("kernel_digest") != kernel_sources_digest(files):
         return None
     return e.get("dram_bytes_per_launch")
+
+
+PREFILL_SOURCES = ("prefill_tc.cu", "tc.cuh", "device.cuh")
 
 
 def time_graph(torch, graph, replays: int, stream):
@@ -550,6 +556,21 @@ def gpu_arm(args, rank, world, local_rank, dist):
                 "bytes_per_launch": kb, "us_per_call": a["us_per_call"],
                 "workload": deep["workload"] + ", automatic geometry (wave rule, chunk on the CTA round of positions)",
                 "peak_source": f"{peak_src} hbm_gbs"}
+        pf = out["other_configs"].get("sparse_prefill")
+        if pf is not None:
+            # the tensor-core prefill against the tensor roofline: the selected
+            # candidates' products per call (the algorithmic flops) over the
+            # call's time, the executed (masked dense) products beside them
+            out["roofline_prefill"] = {
+                "bound": "tensor", "achieved": pf["tflops"], "peak": pf["tensor_peak"],
+                "unit": "TFLOP/s", "frac": pf["frac_of_tensor"],
+                "traffic": ncu_traffic("sparse_prefill_staged"),
+                "kernel": "prefill_tc_kernel<256, staged> (+ prefill_stage_kernel<256>)",
+                "ms_per_call": pf["ms_per_call"], "flops_per_call": pf["flops_per_call"],
+                "executed_tflops": pf["executed_tflops"],
+                "executed_frac": pf["executed_frac_of_tensor"],
+                "workload": pf["workload"],
+                "peak_source": f"{peak_src} bf16_tflops (burst; fp16 taken equal)"}
     return out
 
 
