@@ -183,3 +183,18 @@ def test_staged_workspace_is_sized_and_checked():
     # the gathering kernel's shapes need none (and ignore one)
     assert K.prefill_workspace_bytes(16, 24, 2, 256, 3000, 100) == 0
     assert K.prefill_workspace_bytes(16, 8, 2, 64, 300, 100) == 0
+
+
+def test_largest_cache_the_masks_allow(staged):
+    # 16384 cache positions: 512 mask words per row and 128 blocks per tile,
+    # near the shared-memory limit of the row masks at 12 query heads per KV
+    # head (about 20k positions; longer caches take the gathering kernel)
+    import int8_kv_cache_gb300 as K
+    assert K.prefill_workspace_bytes(16, 24, 2, 256, 16384, 4096) > 0
+    c = W.random_sparse(seed=31, S=16, Hq=24, Hkv=2, D=256, N=16384, max_sel=4096,
+                        sigma=1.0 / 16)
+    ref_o, ref_l = oracle_dsa(c)
+    o, l, f = _run(c, staged)
+    assert not f & WAIT_TIMEOUT
+    assert_close_oracle(o, ref_o, "large cache")
+    assert_lse_oracle(l, ref_l, bound_of(c))
