@@ -17,6 +17,10 @@
 //   * Dispatch order (paged, long chunks).  A CTA may take another (unit,
 //     split) item than its grid position names, so that the longest chunks of
 //     a ragged batch start first (lpt_item below); the geometry is unchanged.
+//   * Balanced pieces (paged, chunk 0 on the API).  The grid and the partial
+//     slots still follow the arguments, but each CTA cuts its own piece of a
+//     row's live range from all live lengths, so that a ragged batch's pieces
+//     come out about equally long (balanced_item below).
 //   * Warp-private pipelines.  Warp w owns the steps w, w + kWarps, ... of the
 //     split (a step is 16 tokens, or 32 when two tiles fit the registers).  It
 //     gathers each step's K and V rows with 16-byte cp.async copies into its
