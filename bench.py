@@ -647,7 +647,8 @@ def extra_configs(torch, K, W, np, dev, stream, peaks, args):
         for cache in (("fp8",) if args.extra == "fp8" else ("int8", "fp8", "fp16")):
             res[f"deep_context_{cache}"] = _deep(torch, K, W, np, t, dev, bench_graph, hbm, cache)
     if args.extra in ("all", "prefill"):
-        res["sparse_prefill"] = _prefill(torch, K, W, np, t, bench_graph, peaks)
+        res["sparse_prefill"] = _prefill(torch, K, W, np, t, bench_graph, peaks, dev, stream)
+        res["sparse_prefill_table"] = _prefill_table(torch, K, W, np, t, bench_graph, peaks)
     if args.extra in ("all", "quantize", "fp8"):
         res["quantize_on_write"] = _quantize(torch, K, np, t, dev, bench_graph, hbm)
         res["quantize_on_write_fp8"] = _quantize(torch, K, np, t, dev, bench_graph, hbm, "fp8")
@@ -771,7 +772,7 @@ def _deep(torch, K, W, np, t, dev, bench_graph, hbm, cache):
                          "heads, head_dim 128", bytes_per_call=byts, rotating_copies=R, **row)
 
 
-def _prefill(torch, K, W, np, t, bench_graph, peaks):
+def _prefill(torch, K, W, np, t, bench_graph, peaks, dev, stream):
     """Sparse prefill: 2048 rows over an 8192-token cache, 24/2 heads, D 256.
     The dense tensor-core kernel computes S and PV over every 128-token block
     some row of a 128-vector tile selects (rows' unselected positions get
@@ -793,6 +794,21 @@ def _prefill(torch, K, W, np, t, bench_graph, peaks):
                       out=out, workspace=ws if staged else None)
     sec = bench_graph(fn, 1, reps=10)
     sec_conv = bench_graph(lambda: fn(False), 1, reps=10)
+    # the SM clock while the staged form runs back to back for about 0.1 s
+    # (dense tensor work at this rate runs into the board's power limit)
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    sampler = ClockSampler(dev.index or 0, uuid and "GPU-" + str(uuid).replace("GPU-", ""))
+    g = capture(torch, fn, stream)
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            g.replay()
+    torch.cuda.synchronize()
+    sampler.start()
+    sampler.mark(True)
+    sec_long = time_graph(torch, g, 300, stream) / 300
+    sampler.mark(False)
+    clk = sampler.stop()
     G = Hq // Hkv
     n_att = int((c.idx >= 0).sum())
     flops = n_att * Hq * Dh * 4
@@ -824,7 +840,47 @@ def _prefill(torch, K, W, np, t, bench_graph, peaks):
         executed_tflops=round(executed / sec / 1e12, 2),
         executed_frac_of_tensor=round(executed / sec / 1e12 / peak_tf, 4),
         gathered_gbs=round(gathered / sec / 1e9, 1), flops_per_call=flops,
-        executed_flops_per_call=executed)
+        executed_flops_per_call=executed,
+        back_to_back=dict(calls=300, ms_per_call=round(sec_long * 1e3, 4), clocks=clk))
+
+
+def _prefill_table(torch, K, W, np, t, bench_graph, peaks):
+    """Sparse prefill at the pages' row counts and contexts (128 / 2048 / 8192
+    rows, the last rows of an 8192- or 32768-token cache, 2048 candidates per
+    row, 24/2 heads, head_dim 256).  Each call runs the path the library picks:
+    the tensor-core kernel over dense blocks (staged form, with a workspace)
+    where the lists cover at least a quarter of the cache, else the gathering
+    kernel."""
+    rows_out = []
+    peak_tf = peaks["bf16_tflops"]
+    for ctx in (8192, 32768):
+        for rows in (128, 2048, 8192):
+            c = W.sparse_prefill(seed=0, rows=rows, N=ctx)
+            d = dict(q=t(c.q), k=t(c.k_codes), v=t(c.v_codes), ks=t(c.k_scale),
+                     vs=t(c.v_scale), idx=t(c.idx))
+            out = torch.empty_like(d["q"])
+            S, Hq, Dh = c.q.shape
+            N, Hkv, _ = c.k_codes.shape
+            wsb = K.prefill_workspace_bytes(S, Hq, Hkv, Dh, N, c.idx.shape[1])
+            ws = torch.empty(wsb, dtype=torch.uint8, device=d["q"].device) if wsb else None
+
+            def fn():
+                K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"],
+                              c.sigma, out=out, workspace=ws)
+            sec = bench_graph(fn, 1, reps=5 if rows > 2048 else 10)
+            flops = int((c.idx >= 0).sum()) * Hq * Dh * 4
+            rows_out.append(dict(
+                rows=rows, context=ctx,
+                kernel="prefill_tc_kernel<256, staged> (tcgen05)" if wsb else
+                       "decode_kernel<256, sparse, int8, one probability tile> (mma.sync, "
+                       "gathered rows, no splits)",
+                ms_per_call=round(sec * 1e3, 4), tflops=round(flops / sec / 1e12, 2),
+                frac_of_tensor=round(flops / sec / 1e12 / peak_tf, 4)))
+            del d, out, ws
+    return dict(workload="sparse prefill, rows at positions N - rows + i of an N-token int8 "
+                         "cache, 2048 sorted unique candidates per row from [0, position], "
+                         "24/2 heads, head_dim 256, per-channel scales, softmax scale 1/16",
+                tensor_peak=peak_tf, cases=rows_out)
 
 
 def reference_arm(args, rank, world):
