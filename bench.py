@@ -869,9 +869,14 @@ def _prefill_table(torch, K, W, np, t, bench_graph, peaks):
                               c.sigma, out=out, workspace=ws)
             sec = bench_graph(fn, 1, reps=5 if rows > 2048 else 10)
             flops = int((c.idx >= 0).sum()) * Hq * Dh * 4
+            # the automatic split count, from the workspace it asked for
+            stage = Hkv * ((N + 127) // 128) * 2 * 128 * Dh * 2
+            splits = 1 if wsb <= stage else \
+                (wsb - (stage + 255) // 256 * 256) // (S * Hq * (Dh + 2) * 4)
             rows_out.append(dict(
                 rows=rows, context=ctx,
-                kernel="prefill_tc_kernel<256, staged> (tcgen05)" if wsb else
+                kernel=(f"prefill_tc_kernel<256, staged> (tcgen05), {splits} split(s)" +
+                        (" + combine_kernel<256>" if splits > 1 else "")) if wsb else
                        "decode_kernel<256, sparse, int8, one probability tile> (mma.sync, "
                        "gathered rows, no splits)",
                 ms_per_call=round(sec * 1e3, 4), tflops=round(flops / sec / 1e12, 2),

@@ -221,34 +221,53 @@ i8kv_status dsa_prefill(const uint16_t* q, const int8_t* k_cache, const int8_t* 
 
 /*
  * dsa_prefill_workspace_bytes -- bytes of the workspace that lets dsa_prefill_ws
- * take the staged form of the tensor-core kernel for this shape: Hkv x
- * ceil(N / 128) x 2 x 128 x D x 2 (the cache as fp16 operand images), or 0
- * when the tensor-core kernel does not serve the shape (head_dim other than
- * 128 / 256, 4 * max_sel < N, S, N or max_sel < 1, bad heads).  Host
- * arithmetic only.
+ * take the staged form of the tensor-core kernel for this shape and split
+ * count (num_splits as for dsa_prefill_ws; 0 = the automatic count on the
+ * current device): Hkv x ceil(N / 128) x 2 x 128 x D x 2 (the cache as fp16
+ * operand images), plus with more than one split, from the next 256-byte
+ * boundary, S x Hq x splits x (D + 2) x 4 (the splits' fp32 partials: the
+ * accumulators, then m, then l).  0 when the tensor-core kernel does not
+ * serve the shape (head_dim other than 128 / 256, 4 * max_sel < N, masks too
+ * large for shared memory, S, N or max_sel < 1, bad heads) or num_splits is
+ * outside [0, 32].  Host only (the automatic count reads the SM count).
  */
 size_t dsa_prefill_workspace_bytes(int32_t S, int32_t Hq, int32_t Hkv, int32_t D, int64_t N,
-                                   int32_t max_sel);
+                                   int32_t max_sel, int32_t num_splits);
 
 /*
  * dsa_prefill_ws -- dsa_prefill with an optional workspace (the caller's device
- * memory, 16-byte aligned, workspace_bytes >= dsa_prefill_workspace_bytes).
- * With one, where the tensor-core kernel serves the shape, the call first
- * converts the cache once into fp16 operand images in the workspace (a
- * kernel of its own, about 3 bytes written per cache byte read) and the
- * prefill kernel copies each block in with one bulk copy instead of
- * converting it in every CTA; the results are the same bit for bit.  With
- * workspace NULL, or where the gathering kernel serves the shape, it is
- * dsa_prefill.  The workspace holds nothing the caller needs afterwards.
- * Errors: as dsa_prefill; I8KV_EWORKSPACE if workspace_bytes is too small,
- * I8KV_EALIGN if the workspace is not 16-byte aligned.
+ * memory, 16-byte aligned, workspace_bytes >= dsa_prefill_workspace_bytes for
+ * the same num_splits).  With one, where the tensor-core kernel serves the
+ * shape, the call first converts the cache once into fp16 operand images in
+ * the workspace (a kernel of its own, about 3 bytes written per cache byte
+ * read) and the prefill kernel copies each block in with one bulk copy
+ * instead of converting it in every CTA; unsplit, the results are the same
+ * bit for bit.
+ *   num_splits  0: automatic -- where a KV head's tiles of 128 (row, head)
+ *               vectors number fewer than half the SMs, each tile's blocks
+ *               are split over min(8, SMs / tiles) CTAs, else 1;
+ *               1 .. 32: that many (a split may get no block).
+ *               With more than one, each CTA writes the fp32 partials of its
+ *               share of the tile's blocks (and of the candidates at their
+ *               positions; a vector sent to the FP32 path publishes an FP32
+ *               partial of its share), and the split_combine kernel merges
+ *               them with the sink into out and lse (onnxruntime PR 33707,
+ *               Summary of Changes §2: the split-K partials and their merge).
+ * With workspace NULL, or where the gathering kernel serves the shape, it is
+ * dsa_prefill (unsplit; num_splits has no effect on the gathering kernel).
+ * The workspace holds nothing the caller needs afterwards.
+ * Errors: as dsa_prefill; I8KV_EINVAL if num_splits is outside [0, 32];
+ * I8KV_EWORKSPACE if workspace_bytes is too small, or workspace is NULL with
+ * num_splits > 1 on the tensor-core path; I8KV_EALIGN if the workspace is not
+ * 16-byte aligned.
  */
 i8kv_status dsa_prefill_ws(const uint16_t* q, const int8_t* k_cache, const int8_t* v_cache,
                            const float* k_scale, const float* v_scale, int32_t scale_kind,
                            const int32_t* idx, int32_t S, int32_t Hq, int32_t Hkv, int32_t D,
                            int64_t N, int32_t max_sel, float softmax_scale,
-                           const float* head_sink, void* workspace, size_t workspace_bytes,
-                           uint16_t* out, float* lse, uint32_t* flags, void* stream);
+                           const float* head_sink, int32_t num_splits, void* workspace,
+                           size_t workspace_bytes, uint16_t* out, float* lse, uint32_t* flags,
+                           void* stream);
 
 /*
  * paged_decode -- split-KV decode over a paged block-table cache

@@ -70,10 +70,11 @@ _SIGNATURES = {
     "dsa_prefill": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i32, _c_vp, _c_i32, _c_i32,
                              _c_i32, _c_i32, _c_i64, _c_i32, _c_f32, _c_vp, _c_vp, _c_vp, _c_vp,
                              _c_vp]),
-    "dsa_prefill_workspace_bytes": (_c_sz, [_c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_i32]),
+    "dsa_prefill_workspace_bytes": (_c_sz, [_c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_i32,
+                                            _c_i32]),
     "dsa_prefill_ws": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i32, _c_vp, _c_i32, _c_i32,
-                                _c_i32, _c_i32, _c_i64, _c_i32, _c_f32, _c_vp, _c_vp, _c_sz,
-                                _c_vp, _c_vp, _c_vp, _c_vp]),
+                                _c_i32, _c_i32, _c_i64, _c_i32, _c_f32, _c_vp, _c_i32, _c_vp,
+                                _c_sz, _c_vp, _c_vp, _c_vp, _c_vp]),
     "paged_decode": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_i32, _c_vp, _c_vp, _c_i32, _c_vp, _c_vp,
                               _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_f32,
                               _c_vp, _c_i32, _c_i32, _c_vp, _c_sz, _c_vp, _c_vp, _c_vp, _c_vp,
@@ -228,20 +229,22 @@ def dsa_decode(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, idx,
     return out
 
 
-def prefill_workspace_bytes(S: int, Hq: int, Hkv: int, D: int, N: int, max_sel: int) -> int:
+def prefill_workspace_bytes(S: int, Hq: int, Hkv: int, D: int, N: int, max_sel: int,
+                            num_splits: int = 0) -> int:
     """Bytes of the workspace that gives dsa_prefill the staged tensor-core form
-    for this shape (the library's dsa_prefill_workspace_bytes; 0 where that
-    kernel does not serve the shape)."""
-    return int(load().dsa_prefill_workspace_bytes(S, Hq, Hkv, D, N, max_sel))
+    for this shape and split count (the library's dsa_prefill_workspace_bytes;
+    0 where that kernel does not serve the shape)."""
+    return int(load().dsa_prefill_workspace_bytes(S, Hq, Hkv, D, N, max_sel, num_splits))
 
 
 def dsa_prefill(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, idx,
                 softmax_scale: float, head_sink=None, out=None, lse=None, flags=None,
-                stream=None, workspace=None):
-    """Sparse-candidate prefill (tensor-core path, no splits).  With a
-    workspace (a device tensor of prefill_workspace_bytes bytes or more) the
-    call takes dsa_prefill_ws: the cache is converted once into fp16 operand
-    images there (same results, fewer instructions in the prefill kernel)."""
+                stream=None, workspace=None, num_splits: int = 0):
+    """Sparse-candidate prefill.  With a workspace (a device tensor of
+    prefill_workspace_bytes(..., num_splits) bytes or more) the call takes
+    dsa_prefill_ws: the cache is converted once into fp16 operand images
+    there, and with num_splits (0: automatic) each tile's blocks may be split
+    over several CTAs whose partials the combine kernel merges."""
     _on_current_device(q, "q")
     S, Hq, D = q.shape
     N, Hkv, _ = k_cache.shape
@@ -254,13 +257,14 @@ def dsa_prefill(q, k_cache, v_cache, k_scale, v_scale, scale_kind: int, idx,
             Hq, Hkv, D, N, max_sel, softmax_scale, _t(head_sink, torch.float32, "head_sink"))
     tail = (_t(out, torch.float16, "out"), _t(lse, torch.float32, "lse"),
             _t(flags, torch.int32, "flags"), _stream(stream))
-    if workspace is None:
+    if workspace is None and num_splits == 0:
         _check("dsa_prefill", load().dsa_prefill(*args, *tail))
     else:
-        _on_current_device(workspace, "workspace")
+        if workspace is not None:
+            _on_current_device(workspace, "workspace")
         _check("dsa_prefill_ws", load().dsa_prefill_ws(
-            *args, _t(workspace, None, "workspace"),
-            workspace.numel() * workspace.element_size(), *tail))
+            *args, num_splits, _t(workspace, None, "workspace"),
+            0 if workspace is None else workspace.numel() * workspace.element_size(), *tail))
     return out
 
 

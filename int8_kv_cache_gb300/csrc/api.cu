@@ -119,6 +119,52 @@ i8kv_status wave_of(const KernelKey& key, WaveInfo* out) {
   return I8KV_OK;
 }
 
+// SMs of the current device (cached per device).
+i8kv_status sm_count(int* sms) {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) {
+      *sms = it->second;
+      return I8KV_OK;
+    }
+  }
+  int n = 0;
+  e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  std::lock_guard<std::mutex> lock(mu);
+  cache[dev] = n;
+  *sms = n;
+  return I8KV_OK;
+}
+
+// The dense prefill's split count: num_splits (1 .. I8KV_MAX_SPLITS), or with 0
+// the automatic count on the current device.
+i8kv_status prefill_splits(int32_t S, int32_t G, int32_t Hkv, int32_t num_splits, int* ns) {
+  if (num_splits > 0) {
+    *ns = num_splits;
+    return I8KV_OK;
+  }
+  int sms = 0;
+  const i8kv_status st = sm_count(&sms);
+  if (st != I8KV_OK) return st;
+  *ns = i8kv::prefill_auto_splits(S, G, Hkv, sms);
+  return I8KV_OK;
+}
+
+// The staged prefill's workspace: the operand images, then (with splits) the
+// partials at the next 256-byte boundary.
+size_t prefill_ws_bytes(int32_t S, int32_t Hq, int32_t Hkv, int32_t D, int64_t N, int ns) {
+  const size_t stage = i8kv::prefill_stage_bytes(N, Hkv, D);
+  if (ns <= 1) return stage;
+  return (stage + 255) / 256 * 256 + i8kv::prefill_partial_bytes(S, Hq, D, ns);
+}
+
 constexpr int32_t kGranuleWave = 16;   // the kernels' 16-position MMA tile
 constexpr int32_t kGranuleTiles = 64;  // the pages' 64-candidate tile
 constexpr int32_t kMinChunk = 128;     // MIN_CHUNK of the wave rule
@@ -376,28 +422,33 @@ i8kv_status dsa_prefill(const uint16_t* q, const int8_t* k_cache, const int8_t* 
                         const float* head_sink, uint16_t* out, float* lse, uint32_t* flags,
                         void* stream) {
   return dsa_prefill_ws(q, k_cache, v_cache, k_scale, v_scale, scale_kind, idx, S, Hq, Hkv, D, N,
-                        max_sel, softmax_scale, head_sink, nullptr, 0, out, lse, flags, stream);
+                        max_sel, softmax_scale, head_sink, 0, nullptr, 0, out, lse, flags, stream);
 }
 
 size_t dsa_prefill_workspace_bytes(int32_t S, int32_t Hq, int32_t Hkv, int32_t D, int64_t N,
-                                   int32_t max_sel) {
+                                   int32_t max_sel, int32_t num_splits) {
   if (S < 1 || N < 1 || max_sel < 1 || check_heads(Hq, Hkv, D) != I8KV_OK) return 0;
+  if (num_splits < 0 || num_splits > I8KV_MAX_SPLITS) return 0;
   int smem = 0, mask_rows = 0;
   if (!i8kv::prefill_tc_plan(D, Hq / Hkv, S, N, max_sel, &smem, &mask_rows)) return 0;
-  return i8kv::prefill_stage_bytes(N, Hkv, D);
+  int ns = 1;
+  if (prefill_splits(S, Hq / Hkv, Hkv, num_splits, &ns) != I8KV_OK) return 0;
+  return prefill_ws_bytes(S, Hq, Hkv, D, N, ns);
 }
 
 i8kv_status dsa_prefill_ws(const uint16_t* q, const int8_t* k_cache, const int8_t* v_cache,
                            const float* k_scale, const float* v_scale, int32_t scale_kind,
                            const int32_t* idx, int32_t S, int32_t Hq, int32_t Hkv, int32_t D,
                            int64_t N, int32_t max_sel, float softmax_scale,
-                           const float* head_sink, void* workspace, size_t workspace_bytes,
-                           uint16_t* out, float* lse, uint32_t* flags, void* stream) {
+                           const float* head_sink, int32_t num_splits, void* workspace,
+                           size_t workspace_bytes, uint16_t* out, float* lse, uint32_t* flags,
+                           void* stream) {
   DecodeParams p;
   i8kv_status st = dsa_common(q, k_cache, v_cache, k_scale, v_scale, scale_kind, idx, S, Hq, Hkv,
                               D, N, max_sel, softmax_scale, head_sink, out, lse, flags, p);
   if (st != I8KV_OK) return st;
   if (S > 0 && out == nullptr) return I8KV_EINVAL;
+  if (num_splits < 0 || num_splits > I8KV_MAX_SPLITS) return I8KV_EINVAL;
   if (!aligned(workspace, 16)) return I8KV_EALIGN;
   if (S == 0) return I8KV_OK;
   p.num_splits = 1;
@@ -408,13 +459,24 @@ i8kv_status dsa_prefill_ws(const uint16_t* q, const int8_t* k_cache, const int8_
   int smem = 0, mask_rows = 0;
   if (i8kv::prefill_tc_plan(D, p.G, S, N, max_sel, &smem, &mask_rows)) {
     // with a workspace: the staged form (fp16 operand images made once per
-    // call, copied in by one thread); without: the converting form
+    // call, copied in by one thread), its tiles' blocks split over several
+    // CTAs where the tiles alone leave SMs idle; without: the converting form,
+    // unsplit
     void* stage = nullptr;
+    int ns = 1;
+    float* part = nullptr;
     if (workspace != nullptr) {
-      if (workspace_bytes < i8kv::prefill_stage_bytes(N, Hkv, D)) return I8KV_EWORKSPACE;
+      st = prefill_splits(S, p.G, Hkv, num_splits, &ns);
+      if (st != I8KV_OK) return st;
+      if (workspace_bytes < prefill_ws_bytes(S, Hq, Hkv, D, N, ns)) return I8KV_EWORKSPACE;
       stage = workspace;
+      if (ns > 1)
+        part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        (i8kv::prefill_stage_bytes(N, Hkv, D) + 255) / 256 * 256);
+    } else if (num_splits > 1) {
+      return I8KV_EWORKSPACE;  // the partials need one
     }
-    cudaError_t e = i8kv::launch_dsa_prefill_tc(p, D, smem, mask_rows, stage,
+    cudaError_t e = i8kv::launch_dsa_prefill_tc(p, D, smem, mask_rows, stage, ns, part,
                                                 static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? I8KV_OK : cuda_fail(e);
   }

@@ -111,8 +111,9 @@ struct Layout {
   static constexpr int kQ = 0;
   static constexpr int kK16 = kQ + kQBytes;
   static constexpr int kV16 = kK16 + kKVBytes;
-  static constexpr int kVs = kV16 + kKVBytes;
-  static constexpr int kMisc = kVs + D * 4;         // barriers, ints, the FP32 vector list
+  static constexpr int kVs = kV16 + kKVBytes;       // the KV head's value scales
+  static constexpr int kKs = kVs + D * 4;           // and its key scales
+  static constexpr int kMisc = kKs + D * 4;         // barriers, ints, the FP32 vector list
   static constexpr int kBarBytes = 128;
   static constexpr int kSlotOff = kMisc + kBarBytes;
   static constexpr int kListOff = kSlotOff + 64;    // BM uint16 vector indices
@@ -141,6 +142,12 @@ struct Layout {
 struct Args {
   DecodeParams p;
   const uint8_t* stage;  // staged form: the fp16 operand images (else null)
+  // splits of each tile's blocks (1: the kernel writes O and lse; more: each
+  // CTA writes the partials of its share, which the combine kernel merges)
+  int nsplit;
+  float* part_acc;     // [rows * Hkv, nsplit, G, D]   value-scaled accumulators
+  float* part_m;       // [rows * Hkv, nsplit, G]      base of the exponentials
+  float* part_l;       // [rows * Hkv, nsplit, G]      row sums
   int tiles_per_head;  // ceil(rows * G / 128)
   int mask_rows;       // rows a tile can span
   int mask_words;      // ceil(N / 32)
@@ -172,7 +179,8 @@ __device__ __forceinline__ void cvt16(const uint4 raw, uint4& lo, uint4& hi) {
 // the weights; terms more than 80 nats down accumulate 2^80 larger.
 template <int D>
 __device__ __noinline__ void fp32_vector(const DecodeParams& p, int row, int h, int g,
-                                         const float* svs) {
+                                         const float* svs, long long pos_lo, long long pos_hi,
+                                         float* pacc, float* pm, float* pl) {
   constexpr int C = D / 32;
   const int lane = threadIdx.x & 31;
   const long long N = p.cache_rows;
@@ -195,10 +203,12 @@ __device__ __noinline__ void fp32_vector(const DecodeParams& p, int row, int h, 
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     return acc * p.sigma;
   };
+  // (a split covers the candidates at positions pos_lo .. pos_hi - 1)
+  const long long lo = pos_lo > 0 ? pos_lo : 0, hi = pos_hi < N ? pos_hi : N;
   float m = neg_inf();
   for (int j = 0; j < p.max_sel; ++j) {
     const int t = list[j];
-    if (t >= 0 && t < N) m = fmaxf(m, score(t));
+    if (t >= lo && t < hi) m = fmaxf(m, score(t));
   }
   float l = 0.f, a[C], b[C];
 #pragma unroll
@@ -206,7 +216,7 @@ __device__ __noinline__ void fp32_vector(const DecodeParams& p, int row, int h, 
   if (m != neg_inf()) {
     for (int j = 0; j < p.max_sel; ++j) {
       const int t = list[j];
-      if (t < 0 || t >= N) continue;
+      if (t < lo || t >= hi) continue;
       const float z = score(t) - m;
       const float w = expf(z);
       l += w;
@@ -223,6 +233,20 @@ __device__ __noinline__ void fp32_vector(const DecodeParams& p, int row, int h, 
                       b[c]);
       }
     }
+  }
+  if (pm != nullptr) {
+    // a split's partial: the value-scaled accumulator relative to e^m
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      const int d = lane + 32 * c;
+      const float vs = svs[d];
+      pacc[d] = l > 0.f ? a[c] * vs + b[c] * (vs * 0x1p-80f) : 0.f;
+    }
+    if (lane == 0) {
+      *pm = l > 0.f ? m : neg_inf();
+      *pl = l;
+    }
+    return;
   }
   float sc = 0.f;
   if (l > 0.f) {
@@ -295,6 +319,7 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
   int* slot_rw = reinterpret_cast<int*>(smem + L::kSlotOff);
   uint16_t* fplist = reinterpret_cast<uint16_t*>(smem + L::kListOff);
   float* svs = reinterpret_cast<float*>(smem + L::kVs);
+  float* sks = reinterpret_cast<float*>(smem + L::kKs);
   uint32_t* mask = reinterpret_cast<uint32_t*>(smem + L::kMask);
   uint8_t* blk_any = reinterpret_cast<uint8_t*>(mask + a.mask_rows * a.mask_words);
   uint8_t* row_dup = blk_any + a.nblocks;
@@ -304,10 +329,18 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
   const long long N = p.cache_rows;
   // later rows (longer causal lists) first, the KV heads interleaved, so that
   // the CTAs start in about decreasing order of work across the whole grid
-  const int g = blockIdx.x % Hkv;
-  const int t_in_head = a.tiles_per_head - 1 - blockIdx.x / Hkv;
+  // (the splits of a tile are consecutive CTAs)
+  const int sidx = blockIdx.x % a.nsplit;
+  const int tb = blockIdx.x / a.nsplit;
+  const int g = tb % Hkv;
+  const int t_in_head = a.tiles_per_head - 1 - tb / Hkv;
   const long long nvec = (long long)p.rows * G;
   const long long v0 = (long long)t_in_head * BM;
+  // index of a query vector's partial of this split: unit row * Hkv + g (the
+  // decode partials' layout, which the combine kernel reads)
+  auto vpart = [&](int row, int h) -> long long {
+    return (((long long)row * Hkv + g) * a.nsplit + sidx) * G + (h - g * G);
+  };
   const int r_lo = (int)(v0 / G);
   const int r_hi = (int)((v0 + BM - 1 < nvec ? v0 + BM - 1 : nvec - 1) / G);
   const int nrows = r_hi - r_lo + 1;
@@ -346,18 +379,69 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
 
   // ---------------- the rows' candidate bitmasks ----------------
   {
+    // The tile's rows' lists are consecutive in memory: each thread takes
+    // every kThreads-th group of four entries of them (one 16-byte load where
+    // the lists' alignment allows, else one entry per group), kListBatch
+    // groups in flight at a time (one dependent load per entry would wait out
+    // a memory latency per kThreads entries).  A group's entries that fall in
+    // one mask word are ORed in with one shared-memory atomic.
+    constexpr int kListBatch = 8;
+    const int32_t* lists = p.idx + (long long)r_lo * p.max_sel;
+    const bool vec4 = (p.max_sel & 3) == 0 && (reinterpret_cast<uintptr_t>(lists) & 15) == 0;
+    const int per = vec4 ? 4 : 1;  // entries per group
     int lo = INT_MAX, hi = -1;
-    for (int rr = 0; rr < nrows; ++rr) {
-      const int32_t* list = p.idx + (long long)(r_lo + rr) * p.max_sel;
-      uint32_t* mrow = mask + rr * a.mask_words;
-      for (int j = tid; j < p.max_sel; j += kThreads) {
-        const int t = __ldg(list + j);
-        if (t < 0 || t >= N) continue;
-        const uint32_t bit = 1u << (t & 31);
-        if (atomicOr(mrow + (t >> 5), bit) & bit) row_dup[rr] = 1;  // a repeated entry
-        blk_any[t / BN] = 1;
-        lo = min(lo, t);
-        hi = max(hi, t);
+    auto flush = [&](int rr, int w, uint32_t bits) {
+      if (bits == 0u) return;
+      if (atomicOr(mask + rr * a.mask_words + w, bits) & bits) row_dup[rr] = 1;  // repeated
+      blk_any[w / (BN / 32)] = 1;
+    };
+    int rr = 0, j = tid * per;  // the row and list slot of this thread's next group
+    while (rr < nrows && j >= p.max_sel) {
+      j -= p.max_sel;
+      ++rr;
+    }
+    while (rr < nrows) {
+      int4 tv[kListBatch];
+      int rv[kListBatch];
+#pragma unroll
+      for (int u = 0; u < kListBatch; ++u) {
+        rv[u] = rr;
+        tv[u] = make_int4(-1, -1, -1, -1);
+        if (rr < nrows) {
+          const int32_t* src = lists + (long long)rr * p.max_sel + j;
+          if (vec4)
+            tv[u] = __ldg(reinterpret_cast<const int4*>(src));
+          else
+            tv[u].x = __ldg(src);
+        }
+        j += kThreads * per;
+        while (rr < nrows && j >= p.max_sel) {
+          j -= p.max_sel;
+          ++rr;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kListBatch; ++u) {
+        if (rv[u] >= nrows) continue;
+        const int te[4] = {tv[u].x, tv[u].y, tv[u].z, tv[u].w};
+        int cw = -1;
+        uint32_t cb = 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = te[e];
+          if (t < 0 || t >= N) continue;
+          const uint32_t bit = 1u << (t & 31);
+          if ((t >> 5) != cw) {
+            flush(rv[u], cw, cb);
+            cw = t >> 5;
+            cb = 0u;
+          }
+          if (cb & bit) row_dup[rv[u]] = 1;  // repeated within the group
+          cb |= bit;
+          lo = min(lo, t);
+          hi = max(hi, t);
+        }
+        flush(rv[u], cw, cb);
       }
     }
 #pragma unroll
@@ -370,17 +454,41 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
       atomicMax(slot_rw + kPMax, hi);
     }
   }
-  // value scales of the KV head
+  // value and key scales of the KV head
   for (int d = tid; d < D; d += kThreads) {
     const float vs = p.per_channel ? p.v_scale[g * D + d] : p.v_scale[0];
+    sks[d] = p.per_channel ? p.k_scale[g * D + d] : p.k_scale[0];
     svs[d] = vs;
     if (!(fabsf(vs) <= 3.4028235e38f)) slot[kVsBad] = 1;
     if (fabsf(vs) > kBigVs) slot[kVsBig] = 1;
   }
   __syncthreads();
   const int pmax = slot[kPMax];
-  const int blo = pmax >= 0 ? slot[kPMin] / BN : 0;
-  const int bhi = pmax >= 0 ? pmax / BN : -1;
+  const int tile_lo = pmax >= 0 ? slot[kPMin] / BN : 0;
+  const int tile_hi = pmax >= 0 ? pmax / BN : -1;
+  // Split sidx takes the tile's selected blocks of ranks [r0, r1), r0 =
+  // sidx * cnt / nsplit, and the candidates at positions [pos_lo, pos_hi):
+  // from its first block to the next split's first (split 0 from 0, the last
+  // one to N), so that every candidate of the tile's rows falls in one split.
+  int blo = tile_lo, bhi = tile_hi;
+  long long pos_lo = 0, pos_hi = N;
+  if (a.nsplit > 1) {
+    int cnt = 0;
+    for (int b = tile_lo; b <= tile_hi; ++b) cnt += blk_any[b];
+    const int r0 = (int)((long long)sidx * cnt / a.nsplit);
+    const int r1 = (int)((long long)(sidx + 1) * cnt / a.nsplit);
+    int b0 = tile_hi + 1, b1 = tile_hi + 1, rank = 0;  // the blocks of ranks r0 and r1
+    for (int b = tile_lo; b <= tile_hi; ++b) {
+      if (!blk_any[b]) continue;
+      if (rank == r0) b0 = b;
+      if (rank == r1) b1 = b;
+      ++rank;
+    }
+    blo = b0;
+    bhi = b1 - 1;
+    if (sidx > 0) pos_lo = (long long)b0 * BN;
+    if (sidx < a.nsplit - 1) pos_hi = (long long)b1 * BN;
+  }
   const bool vs_bad = slot[kVsBad] != 0;
   const bool vs_big = slot[kVsBig] != 0;
   // the blocks some row of the tile selects, in order: blo, next(blo), ...
@@ -389,7 +497,7 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
     while (b <= bhi && !blk_any[b]) ++b;
     return b;
   };
-  const int first = (bhi >= 0 && blk_any[blo]) ? blo : next_blk(blo);
+  const int first = (blo <= bhi && blk_any[blo]) ? blo : next_blk(blo);
 
   // ---------------- Q' = fp16(Q * k_scale) (softmax warps) ----------------
   // Thread r stages its query vector as row r of the A operand: channels
@@ -407,35 +515,37 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
     uint8_t* qdst = smem + L::kQ + r * 128;
     bool bad = false;
     float err = 0.f;
-#pragma unroll 4
-    for (int c = 0; c < D / 8; ++c) {
-      uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (vec_live) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(qrow + 8 * c);
-        const __half2* qh = reinterpret_cast<const __half2*>(&raw);
-        float ks[8];
-        if (p.per_channel) {
-          const float4 k0 = *reinterpret_cast<const float4*>(p.k_scale + g * D + 8 * c);
-          const float4 k1 = *reinterpret_cast<const float4*>(p.k_scale + g * D + 8 * c + 4);
-          ks[0] = k0.x; ks[1] = k0.y; ks[2] = k0.z; ks[3] = k0.w;
-          ks[4] = k1.x; ks[5] = k1.y; ks[6] = k1.z; ks[7] = k1.w;
-        } else {
+    // the query row in batches of kQBatch 16-byte loads in flight
+    constexpr int kQBatch = D / 8 < 16 ? D / 8 : 16;
+    for (int c0 = 0; c0 < D / 8; c0 += kQBatch) {
+      uint4 raw[kQBatch];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) ks[e] = p.k_scale[0];
-        }
-        uint32_t o[4];
+      for (int u = 0; u < kQBatch; ++u)
+        raw[u] = vec_live ? *reinterpret_cast<const uint4*>(qrow + 8 * (c0 + u))
+                          : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __half22float2(qh[e]);
-          const float x0 = f.x * ks[2 * e], x1 = f.y * ks[2 * e + 1];
-          bad |= !(fabsf(x0) <= 65504.f) || !(fabsf(x1) <= 65504.f);
-          o[e] = pack_h2(x0, x1);
-          const float2 rr2 = __half22float2(*reinterpret_cast<const __half2*>(&o[e]));
-          err += fabsf(x0 - rr2.x) + fabsf(x1 - rr2.y);
+      for (int u = 0; u < kQBatch; ++u) {
+        const int c = c0 + u;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (vec_live) {
+          const __half2* qh = reinterpret_cast<const __half2*>(&raw[u]);
+          const float4 k0 = *reinterpret_cast<const float4*>(sks + 8 * c);
+          const float4 k1 = *reinterpret_cast<const float4*>(sks + 8 * c + 4);
+          const float ks[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(qh[e]);
+            const float x0 = f.x * ks[2 * e], x1 = f.y * ks[2 * e + 1];
+            bad |= !(fabsf(x0) <= 65504.f) || !(fabsf(x1) <= 65504.f);
+            o[e] = pack_h2(x0, x1);
+            const float2 rr2 = __half22float2(*reinterpret_cast<const __half2*>(&o[e]));
+            err += fabsf(x0 - rr2.x) + fabsf(x1 - rr2.y);
+          }
+          w = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        w = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(qdst + (c >> 3) * L::kSlabQ + (((c & 7) ^ (r & 7)) << 4)) = w;
       }
-      *reinterpret_cast<uint4*>(qdst + (c >> 3) * L::kSlabQ + (((c & 7) ^ (r & 7)) << 4)) = w;
     }
     if (vec_live) {
       if (bad) flag_or(p.flags, I8KV_FLAG_QUERY_RANGE);
@@ -765,6 +875,38 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
       const float l_run = l_half + lx[(half ^ 1) * BM + r];
       need_fp32 = vec_live && vflag[r] != 0;
       const bool write = vec_live && !need_fp32;
+      if (a.nsplit > 1) {
+        // this split's partial: O * 2^-15 * value_scale, relative to e^m_run
+        const long long pv = vpart(vrow, vh);
+        float* pacc = a.part_acc + pv * D;
+        if (ok && i > 0) {
+#pragma unroll 1
+          for (int c = 0; c < D / 64; ++c) {
+            float o[32];
+            const int d0 = half * (D / 2) + 32 * c;
+            tc::tmem_ld32(tbase + t_lane + L::kOCol + d0, o);
+            tc::tmem_wait_ld();
+            if (write) {
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int d = d0 + 4 * u;
+                *reinterpret_cast<float4*>(pacc + d) =
+                    make_float4(o[4 * u] * kInvProbScale * svs[d],
+                                o[4 * u + 1] * kInvProbScale * svs[d + 1],
+                                o[4 * u + 2] * kInvProbScale * svs[d + 2],
+                                o[4 * u + 3] * kInvProbScale * svs[d + 3]);
+              }
+            }
+          }
+        }
+        if (ok && write && half == 0) {
+          a.part_m[pv] = l_run > 0.f ? m_run : neg_inf();
+          a.part_l[pv] = l_run;
+        }
+        if (!ok) slot[kAbort] = 1;
+        if (half == 1) need_fp32 = false;  // one entry per vector in the FP32 list
+        tc::fence_before_sync();
+      } else {
       float sc = 0.f;
       const float lse_v = l_run > 0.f ? m_run + logf(l_run) : neg_inf();
       if (l_run > 0.f) {
@@ -800,13 +942,21 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
       if (!ok) slot[kAbort] = 1;
       if (half == 1) need_fp32 = false;  // one entry per vector in the FP32 list
       tc::fence_before_sync();
+      }
     }
   } else if (warp < kSoftWarps / 2 && vec_live && !need_fp32) {
-    // no tensor-core work: every position of the tile is unselected
-    __half* orow = reinterpret_cast<__half*>(p.out) + ((long long)vrow * p.Hq + vh) * D;
-    for (int c = 0; c < D / 8; ++c)
-      *reinterpret_cast<uint4*>(orow + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
-    if (p.lse != nullptr) p.lse[(long long)vrow * p.Hq + vh] = neg_inf();
+    // no tensor-core work: every position of the tile (or of this split) is
+    // unselected
+    if (a.nsplit > 1) {
+      const long long pv = vpart(vrow, vh);
+      a.part_m[pv] = neg_inf();
+      a.part_l[pv] = 0.f;
+    } else {
+      __half* orow = reinterpret_cast<__half*>(p.out) + ((long long)vrow * p.Hq + vh) * D;
+      for (int c = 0; c < D / 8; ++c)
+        *reinterpret_cast<uint4*>(orow + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
+      if (p.lse != nullptr) p.lse[(long long)vrow * p.Hq + vh] = neg_inf();
+    }
   }
   if (!run_tc && warp >= kSoftWarps / 2) need_fp32 = false;  // listed by the first half
   if (need_fp32) {
@@ -820,9 +970,18 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
     // the CTA gave up waiting: its outputs are marked invalid
     if (tid == 0) flag_or(p.flags, I8KV_FLAG_WAIT_TIMEOUT);
     if (warp < kSoftWarps / 2 && vec_live) {
-      __half* orow = reinterpret_cast<__half*>(p.out) + ((long long)vrow * p.Hq + vh) * D;
-      for (int d = 0; d < D; ++d) orow[d] = __ushort_as_half(0x7E00);
-      if (p.lse != nullptr) p.lse[(long long)vrow * p.Hq + vh] = __int_as_float(0x7FC00000);
+      if (a.nsplit > 1) {
+        // a partial the combine cannot select away: m = +inf makes the
+        // merged weights, O and lse NaN
+        const long long pv = vpart(vrow, vh);
+        for (int d = 0; d < D; ++d) a.part_acc[pv * D + d] = __int_as_float(0x7FC00000);
+        a.part_m[pv] = __int_as_float(0x7F800000);
+        a.part_l[pv] = __int_as_float(0x7FC00000);
+      } else {
+        __half* orow = reinterpret_cast<__half*>(p.out) + ((long long)vrow * p.Hq + vh) * D;
+        for (int d = 0; d < D; ++d) orow[d] = __ushort_as_half(0x7E00);
+        if (p.lse != nullptr) p.lse[(long long)vrow * p.Hq + vh] = __int_as_float(0x7FC00000);
+      }
     }
   } else {
     // ---------------- the FP32 vectors (every warp takes its share) ----------------
@@ -831,7 +990,14 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
     for (int k = warp; k < nfp; k += kThreads / 32) {
       const long long v = v0 + fplist[k];
       const int row = (int)(v / G);
-      fp32_vector<D>(p, row, g * G + (int)(v - (long long)row * G), g, svs);
+      const int h = g * G + (int)(v - (long long)row * G);
+      if (a.nsplit > 1) {
+        const long long pv = vpart(row, h);
+        fp32_vector<D>(p, row, h, g, svs, pos_lo, pos_hi, a.part_acc + pv * D, a.part_m + pv,
+                       a.part_l + pv);
+      } else {
+        fp32_vector<D>(p, row, h, g, svs, 0, N, nullptr, nullptr, nullptr);
+      }
     }
   }
   tc::fence_before_sync();
@@ -896,10 +1062,14 @@ static cudaError_t run_prefill_tc(const pf::Args& a, int smem, int tiles, cudaSt
                            const_cast<uint8_t*>(a.stage));
     if (e != cudaSuccess) return e;
   }
-  cfg.gridDim = dim3((unsigned)tiles);
+  cfg.gridDim = dim3((unsigned)(tiles * a.nsplit));
   cfg.blockDim = dim3(pf::Roles<STAGED>::kThreads);
   cfg.dynamicSmemBytes = (size_t)smem;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess || a.nsplit == 1) return e;
+  // the splits' partials merged as the decode's are (the sink, O, lse)
+  return launch_combine(a.part_acc, a.part_m, a.part_l, a.p.rows * a.p.Hkv, a.nsplit, a.p.Hq,
+                        a.p.Hkv, D, a.p.sink, a.p.out, a.p.lse, s);
 }
 
 size_t prefill_stage_bytes(long long N, int Hkv, int D) {
@@ -907,18 +1077,38 @@ size_t prefill_stage_bytes(long long N, int Hkv, int D) {
   return (size_t)Hkv * (size_t)((N + pf::BN - 1) / pf::BN) * 2 * pf::BN * D * 2;
 }
 
+size_t prefill_partial_bytes(int rows, int Hq, int D, int nsplit) {
+  if (nsplit <= 1) return 0;
+  return (size_t)rows * Hq * nsplit * ((size_t)D + 2) * 4;
+}
+
+int prefill_auto_splits(int rows, int G, int Hkv, int sms) {
+  // A tile's blocks split over several CTAs only where the tiles alone would
+  // leave more than half of the SMs idle: as many splits as fit one wave (up
+  // to 8); otherwise the partials' round trip would cost more than it saves.
+  const long long tiles = (((long long)rows * G + pf::BM - 1) / pf::BM) * Hkv;
+  if (tiles < 1 || sms < 1 || 2 * tiles > sms) return 1;
+  return (int)std::min<long long>(8, sms / tiles);
+}
+
 cudaError_t launch_dsa_prefill_tc(const DecodeParams& p, int D, int smem, int mask_rows,
-                                  void* stage, cudaStream_t s) {
+                                  void* stage, int nsplit, float* part, cudaStream_t s) {
   pf::Args a;
   a.p = p;
   a.stage = static_cast<const uint8_t*>(stage);
+  a.nsplit = nsplit;
+  const long long pvec = (long long)p.rows * p.Hq * nsplit;  // partial vectors
+  a.part_acc = nsplit > 1 ? part : nullptr;
+  a.part_m = nsplit > 1 ? part + pvec * D : nullptr;
+  a.part_l = nsplit > 1 ? part + pvec * (D + 1) : nullptr;
   const long long nvec = (long long)p.rows * p.G;
   a.tiles_per_head = (int)((nvec + pf::BM - 1) / pf::BM);
   a.mask_rows = mask_rows;
   a.mask_words = (int)((p.cache_rows + 31) / 32);
   a.nblocks = (int)((p.cache_rows + pf::BN - 1) / pf::BN);
   const long long tiles = (long long)a.tiles_per_head * p.Hkv;
-  if (tiles > INT32_MAX || (long long)a.nblocks * p.Hkv > INT32_MAX) return cudaErrorInvalidValue;
+  if (tiles * nsplit > INT32_MAX || (long long)a.nblocks * p.Hkv > INT32_MAX)
+    return cudaErrorInvalidValue;
   if (stage != nullptr)
     return D == 256 ? run_prefill_tc<256, true>(a, smem, (int)tiles, s)
                     : run_prefill_tc<128, true>(a, smem, (int)tiles, s);

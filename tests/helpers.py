@@ -48,7 +48,8 @@ def run_dsa(c, d=None, num_splits=0, chunk=0, prefill=False, flags=None, partial
             staged=False):
     """Sparse decode (or prefill) through the binding: (O, lse) as float64, or
     with ``partials`` the workspace partials of a partials-only decode call.
-    ``staged``: the prefill with a workspace (filled with 0xFF bytes first)."""
+    ``staged``: the prefill with a workspace (filled with 0xFF bytes first),
+    its tensor-core path split ``num_splits`` ways (0: automatic)."""
     d = d or sparse_to_device(c)
     S, Hq, D = c.q.shape
     Hkv = c.k_codes.shape[1]
@@ -57,10 +58,12 @@ def run_dsa(c, d=None, num_splits=0, chunk=0, prefill=False, flags=None, partial
     if prefill:
         ws = None
         if staged:
-            wsb = K.prefill_workspace_bytes(S, Hq, Hkv, D, c.k_codes.shape[0], c.idx.shape[1])
+            wsb = K.prefill_workspace_bytes(S, Hq, Hkv, D, c.k_codes.shape[0], c.idx.shape[1],
+                                            num_splits)
             ws = torch.full((max(wsb, 16),), 255, dtype=torch.uint8, device="cuda")
         K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"], c.sigma,
-                      d["sink"], out=out, lse=lse, flags=flags, workspace=ws)
+                      d["sink"], out=out, lse=lse, flags=flags, workspace=ws,
+                      num_splits=num_splits if staged else 0)
     else:
         ns = num_splits
         if ns == 0:

@@ -201,13 +201,21 @@ def test_prefill_workspace_rules(lib):
     # operand images (Hkv x ceil(N / 128) blocks x K and V x 128 x D x 2 bytes),
     # and only for the shapes the tensor-core kernel serves
     need = lib.dsa_prefill_workspace_bytes
-    assert need(16, 24, 2, 256, 300, 100) == 2 * 3 * 2 * 128 * 256 * 2
-    assert need(2048, 24, 2, 256, 8192, 2048) == 2 * 64 * 2 * 128 * 256 * 2
-    assert need(16, 8, 2, 128, 1000, 300) == 2 * 8 * 2 * 128 * 128 * 2
-    assert need(16, 24, 2, 256, 3000, 100) == 0   # 4 * max_sel < N: the gathering kernel
-    assert need(16, 8, 2, 64, 300, 100) == 0      # head_dim 64: the gathering kernel
-    assert need(0, 24, 2, 256, 300, 100) == 0
-    assert need(16, 24, 5, 256, 300, 100) == 0    # Hq not a multiple of Hkv
+    assert need(16, 24, 2, 256, 300, 100, 1) == 2 * 3 * 2 * 128 * 256 * 2
+    assert need(2048, 24, 2, 256, 8192, 2048, 1) == 2 * 64 * 2 * 128 * 256 * 2
+    assert need(16, 8, 2, 128, 1000, 300, 1) == 2 * 8 * 2 * 128 * 128 * 2
+    # with splits, the partials follow at the next 256-byte boundary: S x Hq x
+    # splits x (D accumulators + m + l) x 4 bytes
+    stage = 2 * 3 * 2 * 128 * 256 * 2
+    assert need(16, 24, 2, 256, 300, 100, 3) == (stage + 255) // 256 * 256 + 16 * 24 * 3 * 258 * 4
+    stage = 2 * 8 * 2 * 128 * 128 * 2
+    assert need(5, 8, 2, 128, 1000, 300, 32) == (stage + 255) // 256 * 256 + 5 * 8 * 32 * 130 * 4
+    assert need(16, 24, 2, 256, 300, 100, 33) == 0   # at most 32 splits
+    assert need(16, 24, 2, 256, 300, 100, -1) == 0
+    assert need(16, 24, 2, 256, 3000, 100, 1) == 0   # 4 * max_sel < N: the gathering kernel
+    assert need(16, 8, 2, 64, 300, 100, 1) == 0      # head_dim 64: the gathering kernel
+    assert need(0, 24, 2, 256, 300, 100, 1) == 0
+    assert need(16, 24, 5, 256, 300, 100, 1) == 0    # Hq not a multiple of Hkv
 
 
 def test_prefill_workspace_errors_before_any_launch(lib):
@@ -215,6 +223,13 @@ def test_prefill_workspace_errors_before_any_launch(lib):
     fake = 1 << 20
     args = [fake, fake, fake, fake, fake, 2, fake, 16, 24, 2, 256, 300, 100, 1.0 / 16, None]
     tail = [fake, None, None, None]
-    need = lib.dsa_prefill_workspace_bytes(16, 24, 2, 256, 300, 100)
-    assert lib.dsa_prefill_ws(*args, fake, need - 16, *tail) == 4   # I8KV_EWORKSPACE
-    assert lib.dsa_prefill_ws(*args, fake + 8, need, *tail) == 3    # I8KV_EALIGN
+    need = lib.dsa_prefill_workspace_bytes(16, 24, 2, 256, 300, 100, 1)
+    assert lib.dsa_prefill_ws(*args, 1, fake, need - 16, *tail) == 4   # I8KV_EWORKSPACE
+    assert lib.dsa_prefill_ws(*args, 1, fake + 8, need, *tail) == 3    # I8KV_EALIGN
+    # splits: their partials must fit too, and need a workspace
+    need3 = lib.dsa_prefill_workspace_bytes(16, 24, 2, 256, 300, 100, 3)
+    assert lib.dsa_prefill_ws(*args, 3, fake, need, *tail) == 4
+    assert lib.dsa_prefill_ws(*args, 3, fake, need3 - 16, *tail) == 4
+    assert lib.dsa_prefill_ws(*args, 3, None, 0, *tail) == 4
+    assert lib.dsa_prefill_ws(*args, 33, fake, need3, *tail) == 1     # I8KV_EINVAL
+    assert lib.dsa_prefill_ws(*args, -1, fake, need3, *tail) == 1

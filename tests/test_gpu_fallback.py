@@ -48,7 +48,8 @@ def _ws_layout(m, l, a, R, Hkv, G, ns, D):
 def test_query_folding_rounding_takes_the_fp32_path(K, spread):
     c = W.query_folding_case(spread=spread)
     want = 1.0 / (1.0 + math.exp(-16.0))  # fp16 rounding of Q' would give 0.5
-    for kw in (dict(num_splits=1, chunk=192), dict(num_splits=3, chunk=64), dict(prefill=True)):
+    for kw in (dict(num_splits=1, chunk=192), dict(num_splits=3, chunk=64), dict(prefill=True),
+               dict(prefill=True, staged=True, num_splits=3)):
         f = _flags()
         o, l = run_dsa(c, flags=f, **kw)
         assert abs(o[0, 0, 0] - want) <= 2e-3, (kw, o[0, 0, 0])
@@ -63,7 +64,7 @@ def test_large_queries_dsa(K, S, Hq, max_sel):
     c.q = (c.q.astype(np.float32) * 32).astype(np.float16)  # every head over the budget
     ref_o, ref_l = oracle_dsa(c)
     for kw in (dict(), dict(num_splits=1, chunk=512), dict(num_splits=-(-max_sel // 64), chunk=64),
-               dict(prefill=True)):
+               dict(prefill=True), dict(prefill=True, staged=True, num_splits=4)):
         f = _flags()
         o, l = run_dsa(c, flags=f, **kw)
         assert_close_oracle(o, ref_o, f"{kw}")

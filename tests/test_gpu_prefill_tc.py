@@ -10,8 +10,8 @@ import pytest
 import torch
 
 import workloads as W
-from helpers import (assert_close_oracle, assert_lse_close, assert_lse_oracle, lse_bound,
-                     oracle_dsa, run_dsa)
+from helpers import (assert_close_oracle, assert_lse_close, assert_lse_oracle, assert_split_close,
+                     lse_bound, oracle_dsa, run_dsa)
 
 pytestmark = pytest.mark.gpu
 
@@ -28,15 +28,19 @@ def _flags():
     return torch.zeros(1, dtype=torch.int32, device="cuda")
 
 
-def _run(c, staged=False):
+def _run(c, form=(False, 0)):
+    """form: (staged, num_splits); the converting form is unsplit."""
     f = _flags()
-    o, l = run_dsa(c, prefill=True, flags=f, staged=staged)
+    o, l = run_dsa(c, prefill=True, flags=f, staged=form[0], num_splits=form[1])
     return o, l, int(f.item())
 
 
 # both forms of the kernel: converting the int8 cache in every CTA, and staged
-# (fp16 operand images made once per call in a workspace)
-@pytest.fixture(params=[False, True], ids=["converting", "staged"])
+# (fp16 operand images made once per call in a workspace), the latter with the
+# automatic split count (small cases: up to 8 splits per tile), unsplit, and
+# with 5 splits
+@pytest.fixture(params=[(False, 0), (True, 0), (True, 1), (True, 5)],
+                ids=["converting", "staged", "staged-unsplit", "staged-5"])
 def staged(request):
     return request.param
 
@@ -88,14 +92,18 @@ def test_matches_the_decode_kernel_on_the_same_rows():
 @pytest.mark.parametrize("q0,vs,fp32", [(336.0, 2.0 ** 28, True), (320.0, 2.0 ** 28, False)])
 def test_tail_depth_rule(q0, vs, fp32, staged):
     """A candidate 21 nats below the maximum under a value scale of 2^28 goes to
-    the FP32 path; exactly 20 nats down stays on the tensor cores."""
+    the FP32 path; exactly 20 nats down stays on the tensor cores.  (Split, the
+    rule holds per split, against the split's own running maximum: where the
+    two candidates fall in different splits, each is its split's maximum and
+    the merge weighs them in FP32, so no split needs the FP32 path.)"""
     c = W.tiny_probability_case(q0, 1, vs, D=128)
     c.q = np.concatenate([c.q] * 2, axis=1)  # 8 query heads over 2 KV heads
     c.k_codes = np.concatenate([c.k_codes] * 2, axis=1)
     c.v_codes = np.concatenate([c.v_codes] * 2, axis=1)
     ref_o, ref_l = oracle_dsa(c)
     o, l, f = _run(c, staged)
-    assert bool(f & FP32_PATH) == fp32
+    if not staged[0] or staged[1] == 1:
+        assert bool(f & FP32_PATH) == fp32
     assert np.all(np.abs(o - ref_o) <= 2e-3 + 1e-2 * np.abs(ref_o))
     assert_lse_close(l, ref_l, 1e-5)
 
@@ -158,8 +166,8 @@ def test_staged_form_is_bit_identical(S, Hq, Hkv, D, N, max_sel):
     # products and the softmax are the same code: the outputs agree bit for bit
     c = W.random_sparse(seed=S + 3, S=S, Hq=Hq, Hkv=Hkv, D=D, N=N, max_sel=max_sel,
                         invalid_frac=0.1, sink=True, sigma=1.0 / 16)
-    o1, l1, f1 = _run(c, False)
-    o2, l2, f2 = _run(c, True)
+    o1, l1, f1 = _run(c, (False, 0))
+    o2, l2, f2 = _run(c, (True, 1))
     assert f1 == f2
     assert np.array_equal(o1, o2, equal_nan=True)
     assert np.array_equal(l1, l2, equal_nan=True)
@@ -170,16 +178,28 @@ def test_staged_workspace_is_sized_and_checked():
     import int8_kv_cache_gb300 as K
     from helpers import sparse_to_device
     c = W.random_sparse(seed=8, S=16, Hq=24, Hkv=2, D=256, N=300, max_sel=100, sigma=1.0 / 16)
-    need = K.prefill_workspace_bytes(16, 24, 2, 256, 300, 100)
-    assert need == 2 * 3 * 2 * 128 * 256 * 2  # Hkv x blocks x (K, V) x 128 x D x fp16
+    stage = 2 * 3 * 2 * 128 * 256 * 2  # Hkv x blocks x (K, V) x 128 x D x fp16
+    need = K.prefill_workspace_bytes(16, 24, 2, 256, 300, 100, 1)
+    assert need == stage
+    # automatic: 2 KV heads x 2 tiles of 128 vectors leave most SMs idle, so
+    # each tile's blocks split min(8, SMs / 4) ways, with their partials
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ns = min(8, sms // 4)
+    assert K.prefill_workspace_bytes(16, 24, 2, 256, 300, 100) == \
+        (stage + 255) // 256 * 256 + 16 * 24 * ns * 258 * 4
+    # enough tiles to fill the SMs: no split
+    assert K.prefill_workspace_bytes(2048, 24, 2, 256, 8192, 2048) == 2 * 64 * 2 * 128 * 256 * 2
     d = sparse_to_device(c)
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     with pytest.raises(K.Int8KVError, match="workspace"):
         K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"], c.sigma,
-                      workspace=ws[: need - 16])
+                      workspace=ws[: need - 16], num_splits=1)
+    with pytest.raises(K.Int8KVError, match="workspace"):
+        K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"], c.sigma,
+                      workspace=ws, num_splits=2)  # no room for the partials
     with pytest.raises(K.Int8KVError):
         K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"], c.sigma,
-                      workspace=ws[8:])  # not 16-byte aligned
+                      workspace=ws[8:], num_splits=1)  # not 16-byte aligned
     # the gathering kernel's shapes need none (and ignore one)
     assert K.prefill_workspace_bytes(16, 24, 2, 256, 3000, 100) == 0
     assert K.prefill_workspace_bytes(16, 8, 2, 64, 300, 100) == 0
@@ -198,3 +218,70 @@ def test_largest_cache_the_masks_allow(staged):
     assert not f & WAIT_TIMEOUT
     assert_close_oracle(o, ref_o, "large cache")
     assert_lse_oracle(l, ref_l, bound_of(c))
+
+
+@pytest.mark.parametrize("S,Hq,Hkv,D,N,max_sel", [
+    (37, 24, 2, 256, 700, 400),    # partial last tile, 6 blocks
+    (3, 2, 2, 256, 500, 200),      # G = 1
+    (50, 16, 1, 128, 333, 120),    # N not a multiple of 128
+    (9, 12, 1, 256, 256, 64),      # 2 blocks: most splits get none
+])
+def test_splits_agree_with_the_unsplit_kernel(S, Hq, Hkv, D, N, max_sel):
+    # any split of a tile's blocks merges to the unsplit result (split vs
+    # unsplit within 1e-3), and both match the oracle
+    c = W.random_sparse(seed=S * 3 + N, S=S, Hq=Hq, Hkv=Hkv, D=D, N=N, max_sel=max_sel,
+                        invalid_frac=0.1, sink=True, sigma=1.0 / 16)
+    ref_o, ref_l = oracle_dsa(c)
+    o1, l1, f1 = _run(c, (True, 1))
+    assert not f1 & WAIT_TIMEOUT
+    for ns in (2, 3, 8, 32):
+        o, l, f = _run(c, (True, ns))
+        assert not f & WAIT_TIMEOUT
+        assert_close_oracle(o, ref_o, f"{ns} splits")
+        assert_lse_oracle(l, ref_l, bound_of(c))
+        assert_split_close(o, o1, f"{ns} splits vs one")
+        assert_lse_close(l, l1, 1e-4)
+
+
+def test_split_fp32_vectors_publish_partials():
+    # rows that repeat entries, and every vector of a few rows over the
+    # query-folding budget, go to the FP32 path in each split over that
+    # split's positions; the merge matches the oracle
+    c = W.random_sparse(seed=77, S=12, Hq=24, Hkv=2, D=256, N=900, max_sel=300,
+                        invalid_frac=0.05, sink=True, sigma=1.0 / 16)
+    c.idx[2, 20:30] = c.idx[2, 0:10]                           # repeated entries
+    c.q[5] = (c.q[5].astype(np.float32) * 32).astype(np.float16)  # over the budget
+    ref_o, ref_l = oracle_dsa(c)
+    for ns in (1, 4, 7):
+        o, l, f = _run(c, (True, ns))
+        assert f & FP32_PATH and not f & WAIT_TIMEOUT
+        assert_close_oracle(o, ref_o, f"{ns} splits")
+        assert_lse_close(l, ref_l, 1e-4)
+
+
+def test_split_prefill_can_be_captured_and_replayed():
+    import int8_kv_cache_gb300 as K
+    from helpers import sparse_to_device
+    c = W.random_sparse(seed=22, S=10, Hq=24, Hkv=2, D=256, N=700, max_sel=300, sigma=1.0 / 16)
+    d = sparse_to_device(c)
+    out = torch.empty_like(d["q"])
+    ws = torch.empty(K.prefill_workspace_bytes(10, 24, 2, 256, 700, 300), dtype=torch.uint8,
+                     device="cuda")
+    s = torch.cuda.Stream()
+
+    def call():
+        K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"], c.sigma,
+                      out=out, workspace=ws)
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    eager = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    ref_o, _ = oracle_dsa(c)
+    assert_close_oracle(out.float().cpu().numpy().astype(np.float64), ref_o, "captured splits")
