@@ -870,7 +870,7 @@ def _prefill_table(torch, K, W, np, t, bench_graph, peaks):
             sec = bench_graph(fn, 1, reps=5 if rows > 2048 else 10)
             flops = int((c.idx >= 0).sum()) * Hq * Dh * 4
             # the automatic split count, from the workspace it asked for
-            stage = Hkv * ((N + 127) // 128) * 2 * 128 * Dh * 2
+            stage = Hkv * ((N + 127) // 128) * 2 * 128 * Dh * 2 + S * ((N + 127) // 128) * 16 + S * 4
             splits = 1 if wsb <= stage else \
                 (wsb - (stage + 255) // 256 * 256) // (S * Hq * (Dh + 2) * 4)
             rows_out.append(dict(

@@ -224,9 +224,10 @@ i8kv_status dsa_prefill(const uint16_t* q, const int8_t* k_cache, const int8_t* 
  * take the staged form of the tensor-core kernel for this shape and split
  * count (num_splits as for dsa_prefill_ws; 0 = the automatic count on the
  * current device): Hkv x ceil(N / 128) x 2 x 128 x D x 2 (the cache as fp16
- * operand images), plus with more than one split, from the next 256-byte
- * boundary, S x Hq x splits x (D + 2) x 4 (the splits' fp32 partials: the
- * accumulators, then m, then l).  0 when the tensor-core kernel does not
+ * operand images) + S x ceil(N / 128) x 16 (every row's candidate bitmask)
+ * + S x 4 (every row's repeat flag), plus with more than one split, from the
+ * next 256-byte boundary, S x Hq x splits x (D + 2) x 4 (the splits' fp32
+ * partials: the accumulators, then m, then l).  0 when the tensor-core kernel does not
  * serve the shape (head_dim other than 128 / 256, 4 * max_sel < N, masks too
  * large for shared memory, S, N or max_sel < 1, bad heads) or num_splits is
  * outside [0, 32].  Host only (the automatic count reads the SM count).
@@ -240,7 +241,8 @@ size_t dsa_prefill_workspace_bytes(int32_t S, int32_t Hq, int32_t Hkv, int32_t D
  * the same num_splits).  With one, where the tensor-core kernel serves the
  * shape, the call first converts the cache once into fp16 operand images in
  * the workspace (a kernel of its own, about 3 bytes written per cache byte
- * read) and the prefill kernel copies each block in with one bulk copy
+ * read, whose other CTAs also turn each row's list into a bitmask of cache
+ * positions) and the prefill kernel copies each block in with one bulk copy
  * instead of converting it in every CTA; unsplit, the results are the same
  * bit for bit.
  *   num_splits  0: automatic -- where a KV head's tiles of 128 (row, head)

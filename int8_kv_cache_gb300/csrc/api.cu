@@ -160,7 +160,7 @@ i8kv_status prefill_splits(int32_t S, int32_t G, int32_t Hkv, int32_t num_splits
 // The staged prefill's workspace: the operand images, then (with splits) the
 // partials at the next 256-byte boundary.
 size_t prefill_ws_bytes(int32_t S, int32_t Hq, int32_t Hkv, int32_t D, int64_t N, int ns) {
-  const size_t stage = i8kv::prefill_stage_bytes(N, Hkv, D);
+  const size_t stage = i8kv::prefill_stage_bytes(N, Hkv, D, S);
   if (ns <= 1) return stage;
   return (stage + 255) / 256 * 256 + i8kv::prefill_partial_bytes(S, Hq, D, ns);
 }
@@ -472,7 +472,7 @@ i8kv_status dsa_prefill_ws(const uint16_t* q, const int8_t* k_cache, const int8_
       stage = workspace;
       if (ns > 1)
         part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                        (i8kv::prefill_stage_bytes(N, Hkv, D) + 255) / 256 * 256);
+                                        (i8kv::prefill_stage_bytes(N, Hkv, D, S) + 255) / 256 * 256);
     } else if (num_splits > 1) {
       return I8KV_EWORKSPACE;  // the partials need one
     }

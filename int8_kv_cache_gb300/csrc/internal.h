@@ -86,13 +86,14 @@ cudaError_t launch_paged_fp8(const KernelKey& key, const DecodeParams& p, cudaSt
 bool prefill_tc_plan(int D, int G, int rows, long long N, int max_sel, int* smem_bytes,
                      int* mask_rows);
 // stage: NULL for the converting form; else the staged form's operand images
-// (prefill_stage_bytes of them, 16-byte aligned), written by the call itself.
+// and row bitmasks (prefill_stage_bytes of them, 16-byte aligned), written by
+// the call itself.
 // nsplit > 1 (staged form only): each tile's blocks split over nsplit CTAs,
 // whose partials (prefill_partial_bytes at part: acc, then m, then l) the
 // combine kernel merges into out and lse.
 cudaError_t launch_dsa_prefill_tc(const DecodeParams& p, int D, int smem, int mask_rows,
                                   void* stage, int nsplit, float* part, cudaStream_t s);
-size_t prefill_stage_bytes(long long N, int Hkv, int D);
+size_t prefill_stage_bytes(long long N, int Hkv, int D, int rows);
 size_t prefill_partial_bytes(int rows, int Hq, int D, int nsplit);
 // The automatic split count of the dense prefill on a device with sms SMs.
 int prefill_auto_splits(int rows, int G, int Hkv, int sms);

@@ -136,6 +136,7 @@ struct Layout {
   static constexpr int kTmemCols = (kOCol + D) <= 256 ? 256 : 512;
   static_assert(kNumBars * 8 <= kBarBytes, "barriers");
   static_assert(kK16 % 1024 == 0, "swizzle atoms are 1024-byte aligned");
+  static_assert(kMask % 16 == 0, "the row masks are copied in 16-byte pieces");
   static_assert(kNumSlots * 4 <= 64, "slots");
 };
 
@@ -148,9 +149,12 @@ struct Args {
   float* part_acc;     // [rows * Hkv, nsplit, G, D]   value-scaled accumulators
   float* part_m;       // [rows * Hkv, nsplit, G]      base of the exponentials
   float* part_l;       // [rows * Hkv, nsplit, G]      row sums
+  // staged form: every row's candidate bitmask, made by prefill_stage_kernel
+  uint32_t* gmask;     // [rows, mask_words]
+  int* gdup;           // [rows]  1 where the row lists some position twice
   int tiles_per_head;  // ceil(rows * G / 128)
   int mask_rows;       // rows a tile can span
-  int mask_words;      // ceil(N / 32)
+  int mask_words;      // ceil(N / 32), rounded up to a multiple of 4
   int nblocks;         // ceil(N / BN)
 };
 
@@ -274,10 +278,61 @@ __global__ void __launch_bounds__(kCvtThreads) prefill_stage_kernel(const Args a
   using L = Layout<D>;
   const DecodeParams& p = a.p;
   constexpr int kPairs = BN * D / 32 / kCvtThreads;
-  const int b = blockIdx.x % a.nblocks, g = blockIdx.x / a.nblocks;
   const int ct = threadIdx.x;
-  uint8_t* dst = img + ((long long)g * a.nblocks + b) * (2 * L::kKVBytes);
   grid_dependency_wait();  // the cache may come from the previous kernel of the stream
+  if (blockIdx.x >= p.Hkv * a.nblocks) {
+    // The CTAs after the images: row `row`'s candidate bitmask (in shared
+    // memory, then written out whole) and whether the row lists some
+    // position twice (its valid entries outnumber its mask bits).
+    extern __shared__ uint32_t rmask[];  // mask_words, then two counters
+    const int row = blockIdx.x - p.Hkv * a.nblocks;
+    const int mw = a.mask_words, max_sel = p.max_sel;
+    const long long N = p.cache_rows;
+    uint32_t* cnt = rmask + mw;
+    for (int w = ct; w < mw; w += kCvtThreads) rmask[w] = 0u;
+    if (ct < 2) cnt[ct] = 0u;
+    __syncthreads();
+    const int32_t* list = p.idx + (long long)row * max_sel;
+    constexpr int kBatch = 8;  // list loads in flight per thread
+    int nv = 0;
+    for (int j0 = ct; j0 < max_sel; j0 += kBatch * kCvtThreads) {
+      int tv[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = j0 + u * kCvtThreads;
+        tv[u] = j < max_sel ? __ldg(list + j) : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int t = tv[u];
+        if (t >= 0 && t < N) {
+          atomicOr(rmask + (t >> 5), 1u << (t & 31));
+          ++nv;
+        }
+      }
+    }
+    int nb = 0;
+    __syncthreads();
+    for (int w = ct; w < mw; w += kCvtThreads) {
+      const uint32_t v = rmask[w];
+      a.gmask[(long long)row * mw + w] = v;
+      nb += __popc(v);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      nv += __shfl_xor_sync(0xffffffffu, nv, o);
+      nb += __shfl_xor_sync(0xffffffffu, nb, o);
+    }
+    if ((ct & 31) == 0) {
+      atomicAdd(cnt, (uint32_t)nv);
+      atomicAdd(cnt + 1, (uint32_t)nb);
+    }
+    __syncthreads();
+    if (ct == 0) a.gdup[row] = cnt[1] < cnt[0] ? 1 : 0;
+    return;
+  }
+  const int b = blockIdx.x % a.nblocks, g = blockIdx.x / a.nblocks;
+  uint8_t* dst = img + ((long long)g * a.nblocks + b) * (2 * L::kKVBytes);
 #pragma unroll
   for (int kv = 0; kv < 2; ++kv) {
     const int8_t* src = reinterpret_cast<const int8_t*>(kv == 0 ? p.k : p.v);
@@ -377,82 +432,132 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
   tc::fence_after_sync();
   const uint32_t tbase = static_cast<uint32_t>(slot[kTmem]);
 
+  // the query vector of each softmax-warp thread
+  const int half = (warp >> 2) & 1;         // softmax warps: column half
+  const int r = 32 * (warp & 3) + lane;      // softmax warps: the vector of this thread
+  const long long vidx = v0 + r;
+  const bool vec_live = warp < kSoftWarps && vidx < nvec;
+  const int vrow = vec_live ? (int)(vidx / G) : r_lo;
+  const int vh = vec_live ? g * G + (int)(vidx - (long long)vrow * G) : 0;
+  const __half* qrow = reinterpret_cast<const __half*>(p.q) + ((long long)vrow * p.Hq + vh) * D;
+  // raw query rows in the V buffer, 16-byte chunk c of row r at chunk
+  // c ^ (r mod D/8) (conflict-free reads by the warps' consecutive rows)
+  constexpr int kQChunks = D / 8;
+  auto raw_q = [&](int c) -> uint32_t {
+    return (uint32_t)(L::kV16 + r * D * 2 + 16 * (c ^ (r & (kQChunks - 1))));
+  };
+
+  // raw query rows into the V buffer (cp.async), first: they land while the
+  // masks are made
+  if (warp < kSoftWarps / 2 && vec_live) {
+#pragma unroll 8
+    for (int c = 0; c < kQChunks; ++c) cp_async16(sbase + raw_q(c), qrow + 8 * c, 16);
+  }
+  cp_async_commit();
+
   // ---------------- the rows' candidate bitmasks ----------------
-  {
-    // The tile's rows' lists are consecutive in memory: each thread takes
-    // every kThreads-th group of four entries of them (one 16-byte load where
-    // the lists' alignment allows, else one entry per group), kListBatch
-    // groups in flight at a time (one dependent load per entry would wait out
-    // a memory latency per kThreads entries).  A group's entries that fall in
-    // one mask word are ORed in with one shared-memory atomic.
-    constexpr int kListBatch = 8;
-    const int32_t* lists = p.idx + (long long)r_lo * p.max_sel;
-    const bool vec4 = (p.max_sel & 3) == 0 && (reinterpret_cast<uintptr_t>(lists) & 15) == 0;
-    const int per = vec4 ? 4 : 1;  // entries per group
-    int lo = INT_MAX, hi = -1;
-    auto flush = [&](int rr, int w, uint32_t bits) {
-      if (bits == 0u) return;
-      if (atomicOr(mask + rr * a.mask_words + w, bits) & bits) row_dup[rr] = 1;  // repeated
-      blk_any[w / (BN / 32)] = 1;
-    };
-    int rr = 0, j = tid * per;  // the row and list slot of this thread's next group
-    while (rr < nrows && j >= p.max_sel) {
-      j -= p.max_sel;
-      ++rr;
-    }
-    while (rr < nrows) {
-      int4 tv[kListBatch];
-      int rv[kListBatch];
-#pragma unroll
-      for (int u = 0; u < kListBatch; ++u) {
-        rv[u] = rr;
-        tv[u] = make_int4(-1, -1, -1, -1);
-        if (rr < nrows) {
-          const int32_t* src = lists + (long long)rr * p.max_sel + j;
-          if (vec4)
-            tv[u] = __ldg(reinterpret_cast<const int4*>(src));
-          else
-            tv[u].x = __ldg(src);
-        }
-        j += kThreads * per;
-        while (rr < nrows && j >= p.max_sel) {
-          j -= p.max_sel;
-          ++rr;
-        }
+  if constexpr (STAGED) {
+    // prefill_stage_kernel made every row's bitmask (and its repeat flag):
+    // the tile's rows' masks are consecutive in memory, one cp.async each
+    // 16 bytes; then the blocks some row selects
+    const int mw = a.mask_words;
+    const uint32_t* gm = a.gmask + (long long)r_lo * mw;
+    for (int k = tid; k < nrows * mw / 4; k += kThreads)
+      cp_async16(sbase + L::kMask + 16 * k, gm + 4 * k, 16);
+    cp_async_commit();
+    for (int rr = tid; rr < nrows; rr += kThreads) row_dup[rr] = a.gdup[r_lo + rr] != 0 ? 1 : 0;
+    cp_async_wait_all();
+    __syncthreads();
+    for (int b = tid; b < a.nblocks; b += kThreads) {
+      uint32_t any = 0u;
+      for (int rr = 0; rr < nrows; ++rr) {
+        const uint4 v = *reinterpret_cast<const uint4*>(mask + rr * mw + (BN / 32) * b);
+        any |= v.x | v.y | v.z | v.w;
       }
-#pragma unroll
-      for (int u = 0; u < kListBatch; ++u) {
-        if (rv[u] >= nrows) continue;
-        const int te[4] = {tv[u].x, tv[u].y, tv[u].z, tv[u].w};
-        int cw = -1;
-        uint32_t cb = 0u;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int t = te[e];
-          if (t < 0 || t >= N) continue;
-          const uint32_t bit = 1u << (t & 31);
-          if ((t >> 5) != cw) {
-            flush(rv[u], cw, cb);
-            cw = t >> 5;
-            cb = 0u;
+      blk_any[b] = any != 0u ? 1 : 0;
+      if (any != 0u) {
+        atomicMin(slot_rw + kPMin, b * BN);
+        atomicMax(slot_rw + kPMax, b * BN);
+      }
+    }
+  } else {
+    {
+      // The tile's rows' lists are consecutive in memory: each thread takes
+      // every kThreads-th group of four entries of them (one 16-byte load where
+      // the lists' alignment allows, else one entry per group), kListBatch
+      // groups in flight at a time (one dependent load per entry would wait out
+      // a memory latency per kThreads entries).  A group's entries that fall in
+      // one mask word are ORed in with one shared-memory atomic.
+      constexpr int kListBatch = 8;
+      const int32_t* lists = p.idx + (long long)r_lo * p.max_sel;
+      const bool vec4 = (p.max_sel & 3) == 0 && (reinterpret_cast<uintptr_t>(lists) & 15) == 0;
+      const int per = vec4 ? 4 : 1;  // entries per group
+      int lo = INT_MAX, hi = -1;
+      auto flush = [&](int rr, int w, uint32_t bits) {
+        if (bits == 0u) return;
+        if (atomicOr(mask + rr * a.mask_words + w, bits) & bits) row_dup[rr] = 1;  // repeated
+        blk_any[w / (BN / 32)] = 1;
+      };
+      int rr = 0, j = tid * per;  // the row and list slot of this thread's next group
+      while (rr < nrows && j >= p.max_sel) {
+        j -= p.max_sel;
+        ++rr;
+      }
+      while (rr < nrows) {
+        int4 tv[kListBatch];
+        int rv[kListBatch];
+  #pragma unroll
+        for (int u = 0; u < kListBatch; ++u) {
+          rv[u] = rr;
+          tv[u] = make_int4(-1, -1, -1, -1);
+          if (rr < nrows) {
+            const int32_t* src = lists + (long long)rr * p.max_sel + j;
+            if (vec4)
+              tv[u] = __ldg(reinterpret_cast<const int4*>(src));
+            else
+              tv[u].x = __ldg(src);
           }
-          if (cb & bit) row_dup[rv[u]] = 1;  // repeated within the group
-          cb |= bit;
-          lo = min(lo, t);
-          hi = max(hi, t);
+          j += kThreads * per;
+          while (rr < nrows && j >= p.max_sel) {
+            j -= p.max_sel;
+            ++rr;
+          }
         }
-        flush(rv[u], cw, cb);
+  #pragma unroll
+        for (int u = 0; u < kListBatch; ++u) {
+          if (rv[u] >= nrows) continue;
+          const int te[4] = {tv[u].x, tv[u].y, tv[u].z, tv[u].w};
+          int cw = -1;
+          uint32_t cb = 0u;
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int t = te[e];
+            if (t < 0 || t >= N) continue;
+            const uint32_t bit = 1u << (t & 31);
+            if ((t >> 5) != cw) {
+              flush(rv[u], cw, cb);
+              cw = t >> 5;
+              cb = 0u;
+            }
+            if (cb & bit) row_dup[rv[u]] = 1;  // repeated within the group
+            cb |= bit;
+            lo = min(lo, t);
+            hi = max(hi, t);
+          }
+          flush(rv[u], cw, cb);
+        }
+      }
+  #pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+      }
+      if (lane == 0 && hi >= 0) {
+        atomicMin(slot_rw + kPMin, lo);
+        atomicMax(slot_rw + kPMax, hi);
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-    }
-    if (lane == 0 && hi >= 0) {
-      atomicMin(slot_rw + kPMin, lo);
-      atomicMax(slot_rw + kPMax, hi);
-    }
+    cp_async_wait_all();  // the raw query rows
   }
   // value and key scales of the KV head
   for (int d = tid; d < D; d += kThreads) {
@@ -500,28 +605,21 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
   const int first = (blo <= bhi && blk_any[blo]) ? blo : next_blk(blo);
 
   // ---------------- Q' = fp16(Q * k_scale) (softmax warps) ----------------
-  // Thread r stages its query vector as row r of the A operand: channels
-  // 8c..8c+7 go to slab c / 8, row r, chunk (c % 8) ^ (r % 8).
-  const int half = (warp >> 2) & 1;         // softmax warps: column half
-  const int r = 32 * (warp & 3) + lane;      // softmax warps: the vector of this thread
-  const long long vidx = v0 + r;
-  const bool vec_live = warp < kSoftWarps && vidx < nvec;
+  // Thread r stages its query vector (from the raw row in the V buffer) as
+  // row r of the A operand: channels 8c..8c+7 go to slab c / 8, row r, chunk
+  // (c % 8) ^ (r % 8).
   uint8_t* vflag = smem + L::kVFlag;
-  const int vrow = vec_live ? (int)(vidx / G) : r_lo;
-  const int vh = vec_live ? g * G + (int)(vidx - (long long)vrow * G) : 0;
   bool need_fp32 = false;
   if (warp < kSoftWarps / 2) {
-    const __half* qrow = reinterpret_cast<const __half*>(p.q) + ((long long)vrow * p.Hq + vh) * D;
     uint8_t* qdst = smem + L::kQ + r * 128;
     bool bad = false;
     float err = 0.f;
-    // the query row in batches of kQBatch 16-byte loads in flight
-    constexpr int kQBatch = D / 8 < 16 ? D / 8 : 16;
-    for (int c0 = 0; c0 < D / 8; c0 += kQBatch) {
+    constexpr int kQBatch = kQChunks < 16 ? kQChunks : 16;
+    for (int c0 = 0; c0 < kQChunks; c0 += kQBatch) {
       uint4 raw[kQBatch];
 #pragma unroll
       for (int u = 0; u < kQBatch; ++u)
-        raw[u] = vec_live ? *reinterpret_cast<const uint4*>(qrow + 8 * (c0 + u))
+        raw[u] = vec_live ? *reinterpret_cast<const uint4*>(smem + raw_q(c0 + u))
                           : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int u = 0; u < kQBatch; ++u) {
@@ -557,6 +655,9 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
   // a tile with nothing for the tensor cores (no selected block, or every
   // value scale unusable) skips the pipeline
   const bool run_tc = first <= bhi && !vs_bad;
+  // the lists and raw query rows were read from the buffers that the bulk
+  // copies (async proxy) fill next
+  tc::fence_smem_to_async();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -1021,8 +1122,8 @@ bool prefill_tc_plan(int D, int G, int rows, long long N, int max_sel, int* smem
   if (rows < 1 || N < 1 || max_sel < 1 || N > INT32_MAX / 2) return false;
   if (4LL * max_sel < N) return false;
   const long long mr = std::min<long long>(127 / G + 2, rows);
-  const long long words = (N + 31) / 32;
   const long long nblocks = (N + pf::BN - 1) / pf::BN;
+  const long long words = nblocks * (pf::BN / 32);  // ceil(N / 32) rounded up to whole blocks
   const long long mask = ((mr * words * 4 + nblocks + mr) + 15) / 16 * 16;
   const long long base = D == 256 ? pf::Layout<256>::kMask : pf::Layout<128>::kMask;
   const long long total = base + mask;
@@ -1053,11 +1154,11 @@ static cudaError_t run_prefill_tc(const pf::Args& a, int smem, int tiles, cudaSt
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (STAGED) {
-    // the operand images first (their kernel waits for the previous one of
-    // the stream; the prefill kernel waits for this one)
-    cfg.gridDim = dim3((unsigned)(a.p.Hkv * a.nblocks));
+    // the operand images and the rows' bitmasks first (their kernel waits
+    // for the previous one of the stream; the prefill kernel waits for it)
+    cfg.gridDim = dim3((unsigned)(a.p.Hkv * a.nblocks + a.p.rows));
     cfg.blockDim = dim3(pf::kCvtThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = (size_t)(a.mask_words + 2) * 4;
     e = cudaLaunchKernelEx(&cfg, pf::prefill_stage_kernel<D>, a,
                            const_cast<uint8_t*>(a.stage));
     if (e != cudaSuccess) return e;
@@ -1072,9 +1173,17 @@ static cudaError_t run_prefill_tc(const pf::Args& a, int smem, int tiles, cudaSt
                         a.p.Hkv, D, a.p.sink, a.p.out, a.p.lse, s);
 }
 
-size_t prefill_stage_bytes(long long N, int Hkv, int D) {
-  if (N < 1 || Hkv < 1 || (D != 128 && D != 256)) return 0;
+// The staged form's workspace before the partials: the operand images
+// (Hkv x blocks x K and V x 128 x D fp16), every row's bitmask (4 words per
+// block) and every row's repeat flag.
+static size_t stage_image_bytes(long long N, int Hkv, int D) {
   return (size_t)Hkv * (size_t)((N + pf::BN - 1) / pf::BN) * 2 * pf::BN * D * 2;
+}
+
+size_t prefill_stage_bytes(long long N, int Hkv, int D, int rows) {
+  if (N < 1 || Hkv < 1 || rows < 1 || (D != 128 && D != 256)) return 0;
+  const size_t words = (size_t)((N + pf::BN - 1) / pf::BN) * (pf::BN / 32);
+  return stage_image_bytes(N, Hkv, D) + (size_t)rows * words * 4 + (size_t)rows * 4;
 }
 
 size_t prefill_partial_bytes(int rows, int Hq, int D, int nsplit) {
@@ -1104,10 +1213,17 @@ cudaError_t launch_dsa_prefill_tc(const DecodeParams& p, int D, int smem, int ma
   const long long nvec = (long long)p.rows * p.G;
   a.tiles_per_head = (int)((nvec + pf::BM - 1) / pf::BM);
   a.mask_rows = mask_rows;
-  a.mask_words = (int)((p.cache_rows + 31) / 32);
   a.nblocks = (int)((p.cache_rows + pf::BN - 1) / pf::BN);
+  a.mask_words = a.nblocks * (pf::BN / 32);
+  a.gmask = nullptr;
+  a.gdup = nullptr;
+  if (stage != nullptr) {
+    a.gmask = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(stage) +
+                                          stage_image_bytes(p.cache_rows, p.Hkv, D));
+    a.gdup = reinterpret_cast<int*>(a.gmask + (long long)p.rows * a.mask_words);
+  }
   const long long tiles = (long long)a.tiles_per_head * p.Hkv;
-  if (tiles * nsplit > INT32_MAX || (long long)a.nblocks * p.Hkv > INT32_MAX)
+  if (tiles * nsplit > INT32_MAX || (long long)a.nblocks * p.Hkv + p.rows > INT32_MAX)
     return cudaErrorInvalidValue;
   if (stage != nullptr)
     return D == 256 ? run_prefill_tc<256, true>(a, smem, (int)tiles, s)

@@ -201,15 +201,21 @@ def test_prefill_workspace_rules(lib):
     # operand images (Hkv x ceil(N / 128) blocks x K and V x 128 x D x 2 bytes),
     # and only for the shapes the tensor-core kernel serves
     need = lib.dsa_prefill_workspace_bytes
-    assert need(16, 24, 2, 256, 300, 100, 1) == 2 * 3 * 2 * 128 * 256 * 2
-    assert need(2048, 24, 2, 256, 8192, 2048, 1) == 2 * 64 * 2 * 128 * 256 * 2
-    assert need(16, 8, 2, 128, 1000, 300, 1) == 2 * 8 * 2 * 128 * 128 * 2
+
+    def stage(S, Hkv, D, N):
+        # operand images, then each row's bitmask (16 bytes per 128-position
+        # block) and repeat flag
+        blocks = -(-N // 128)
+        return Hkv * blocks * 2 * 128 * D * 2 + S * blocks * 16 + S * 4
+    assert need(16, 24, 2, 256, 300, 100, 1) == stage(16, 2, 256, 300)
+    assert need(2048, 24, 2, 256, 8192, 2048, 1) == stage(2048, 2, 256, 8192)
+    assert need(16, 8, 2, 128, 1000, 300, 1) == stage(16, 2, 128, 1000)
     # with splits, the partials follow at the next 256-byte boundary: S x Hq x
     # splits x (D accumulators + m + l) x 4 bytes
-    stage = 2 * 3 * 2 * 128 * 256 * 2
-    assert need(16, 24, 2, 256, 300, 100, 3) == (stage + 255) // 256 * 256 + 16 * 24 * 3 * 258 * 4
-    stage = 2 * 8 * 2 * 128 * 128 * 2
-    assert need(5, 8, 2, 128, 1000, 300, 32) == (stage + 255) // 256 * 256 + 5 * 8 * 32 * 130 * 4
+    st = stage(16, 2, 256, 300)
+    assert need(16, 24, 2, 256, 300, 100, 3) == (st + 255) // 256 * 256 + 16 * 24 * 3 * 258 * 4
+    st = stage(5, 2, 128, 1000)
+    assert need(5, 8, 2, 128, 1000, 300, 32) == (st + 255) // 256 * 256 + 5 * 8 * 32 * 130 * 4
     assert need(16, 24, 2, 256, 300, 100, 33) == 0   # at most 32 splits
     assert need(16, 24, 2, 256, 300, 100, -1) == 0
     assert need(16, 24, 2, 256, 3000, 100, 1) == 0   # 4 * max_sel < N: the gathering kernel

@@ -178,7 +178,9 @@ def test_staged_workspace_is_sized_and_checked():
     import int8_kv_cache_gb300 as K
     from helpers import sparse_to_device
     c = W.random_sparse(seed=8, S=16, Hq=24, Hkv=2, D=256, N=300, max_sel=100, sigma=1.0 / 16)
-    stage = 2 * 3 * 2 * 128 * 256 * 2  # Hkv x blocks x (K, V) x 128 x D x fp16
+    # Hkv x blocks x (K, V) x 128 x D x fp16, then the rows' bitmasks (16
+    # bytes per block) and repeat flags
+    stage = 2 * 3 * 2 * 128 * 256 * 2 + 16 * 3 * 16 + 16 * 4
     need = K.prefill_workspace_bytes(16, 24, 2, 256, 300, 100, 1)
     assert need == stage
     # automatic: 2 KV heads x 2 tiles of 128 vectors leave most SMs idle, so
@@ -188,7 +190,8 @@ def test_staged_workspace_is_sized_and_checked():
     assert K.prefill_workspace_bytes(16, 24, 2, 256, 300, 100) == \
         (stage + 255) // 256 * 256 + 16 * 24 * ns * 258 * 4
     # enough tiles to fill the SMs: no split
-    assert K.prefill_workspace_bytes(2048, 24, 2, 256, 8192, 2048) == 2 * 64 * 2 * 128 * 256 * 2
+    assert K.prefill_workspace_bytes(2048, 24, 2, 256, 8192, 2048) == \
+        2 * 64 * 2 * 128 * 256 * 2 + 2048 * 64 * 16 + 2048 * 4
     d = sparse_to_device(c)
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     with pytest.raises(K.Int8KVError, match="workspace"):
