@@ -62,7 +62,7 @@ def parse():
     ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--extra", default="all",
                     choices=["all", "sparse", "paged", "variants", "fp8", "deep", "prefill",
-                             "quantize", "none"],
+                             "prefill_table", "quantize", "none"],
                     help="which other workloads to measure besides the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--clock-sampler", default=None, help=argparse.SUPPRESS)
@@ -648,6 +648,7 @@ def extra_configs(torch, K, W, np, dev, stream, peaks, args):
             res[f"deep_context_{cache}"] = _deep(torch, K, W, np, t, dev, bench_graph, hbm, cache)
     if args.extra in ("all", "prefill"):
         res["sparse_prefill"] = _prefill(torch, K, W, np, t, bench_graph, peaks, dev, stream)
+    if args.extra in ("all", "prefill_table"):
         res["sparse_prefill_table"] = _prefill_table(torch, K, W, np, t, bench_graph, peaks)
     if args.extra in ("all", "quantize", "fp8"):
         res["quantize_on_write"] = _quantize(torch, K, np, t, dev, bench_graph, hbm)
