@@ -605,17 +605,18 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
   const int first = (blo <= bhi && blk_any[blo]) ? blo : next_blk(blo);
 
   // ---------------- Q' = fp16(Q * k_scale) (softmax warps) ----------------
-  // Thread r stages its query vector (from the raw row in the V buffer) as
-  // row r of the A operand: channels 8c..8c+7 go to slab c / 8, row r, chunk
-  // (c % 8) ^ (r % 8).
+  // Threads (half, r) of the softmax warps stage half the channels of query
+  // vector r (from the raw row in the V buffer) into row r of the A operand:
+  // channels 8c..8c+7 go to slab c / 8, row r, chunk (c % 8) ^ (r % 8).
   uint8_t* vflag = smem + L::kVFlag;
   bool need_fp32 = false;
-  if (warp < kSoftWarps / 2) {
+  if (warp < kSoftWarps) {
     uint8_t* qdst = smem + L::kQ + r * 128;
     bool bad = false;
     float err = 0.f;
-    constexpr int kQBatch = kQChunks < 16 ? kQChunks : 16;
-    for (int c0 = 0; c0 < kQChunks; c0 += kQBatch) {
+    constexpr int kHalfChunks = kQChunks / 2;
+    constexpr int kQBatch = kHalfChunks < 16 ? kHalfChunks : 16;
+    for (int c0 = half * kHalfChunks; c0 < (half + 1) * kHalfChunks; c0 += kQBatch) {
       uint4 raw[kQBatch];
 #pragma unroll
       for (int u = 0; u < kQBatch; ++u)
@@ -645,11 +646,22 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
         *reinterpret_cast<uint4*>(qdst + (c >> 3) * L::kSlabQ + (((c & 7) ^ (r & 7)) << 4)) = w;
       }
     }
-    if (vec_live) {
-      if (bad) flag_or(p.flags, I8KV_FLAG_QUERY_RANGE);
-      need_fp32 = bad || p.sigma * 128.f * err > kQueryBudget || vs_bad || row_dup[vrow - r_lo];
+    // the halves' folding-error sums and range flags meet in shared memory
+    // (the pair of warps q, q + 4 on named barrier 1 + q)
+    float* qx = reinterpret_cast<float*>(smem + L::kXchg);  // [2][BM] errors, [2][BM] flags
+    qx[half * BM + r] = err;
+    qx[(2 + half) * BM + r] = bad ? 1.f : 0.f;
+    asm volatile("bar.sync %0, %1;\n" ::"r"(1 + (warp & 3)), "r"(64) : "memory");
+    if (half == 0) {
+      const float err_all = err + qx[BM + r];
+      const bool bad_all = bad || qx[3 * BM + r] != 0.f;
+      if (vec_live) {
+        if (bad_all) flag_or(p.flags, I8KV_FLAG_QUERY_RANGE);
+        need_fp32 = bad_all || p.sigma * 128.f * err_all > kQueryBudget || vs_bad ||
+                    row_dup[vrow - r_lo];
+      }
+      vflag[r] = need_fp32 ? 1 : 0;
     }
-    vflag[r] = need_fp32 ? 1 : 0;
     tc::fence_smem_to_async();  // Q' is read by the tensor core
   }
   // a tile with nothing for the tensor cores (no selected block, or every
