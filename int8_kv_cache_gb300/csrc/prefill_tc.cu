@@ -12,7 +12,7 @@
 // cache (2048 of the first 6-8k tokens per row in the pages' workload), so the
 // kernel does not gather per row.  A CTA takes a tile of 128 query vectors of
 // one KV head (the (row, head) pairs r*G + j, consecutive, so a tile spans
-// about 128 / G rows), builds a bitmask of each of its rows' candidates in
+// about 128 / G rows), holds a bitmask of each of its rows' candidates in
 // shared memory, and streams the cache positions those rows select in blocks
 // of 128 contiguous tokens:
 //   S[128 x 128] = Q'[128 x D] K_block^T     tcgen05 kind::f16, M=128, N=128
@@ -45,10 +45,15 @@
 //   warp 16    lane 0 issues the MMAs; the warp owns the tensor memory.
 //   staged form (320 threads; dsa_prefill_ws): prefill_stage_kernel first
 //              writes every block's fp16 K and V exactly as the converters
-//              would lay them out in shared memory;
+//              would lay them out in shared memory, and every row's bitmask
+//              (its other CTAs, one per row), which the tiles copy in;
 //   warp 8     lane 0 issues the MMAs; the warp owns the tensor memory;
 //   warp 9     lane 0 brings each K or V block in with one bulk copy (the
 //              mbarrier counts the bytes), K one block ahead of V.
+// In the staged form a tile's blocks may also be split over several CTAs
+// (where the tiles alone would leave SMs idle): each takes the blocks of its
+// rank range and the candidates at their positions, and writes the partials
+// that the split-combine kernel merges (PR 33707 §2's partial layout).
 // (An MMA instruction costs the same up to N = 128 columns and about twice as
 // much at N = 256, measured on this part: 128-token blocks keep QK^T at N=128
 // instead of wasting half of every instruction at N = 64.)
