@@ -9,7 +9,9 @@ configuration the benchmark times (the automatic geometry of the library).
   adaptive and fixed chunks: every output, and each split count against the
   single split;
 * sparse prefill, 2048 rows over an 8192-token cache: the GPU runs all rows,
-  the oracle checks 64 of them, one by one.
+  the oracle checks 64 of them, one by one; and the other row counts and
+  contexts the benchmark times (128 / 8192 rows, 8192 / 32768 positions),
+  each on the path and split count the library picks, on sampled rows.
 """
 import dataclasses
 
@@ -91,3 +93,18 @@ def test_sparse_prefill_full_size_sampled_rows(staged):
     ref_o, ref_l = oracle_dsa(sub)
     assert_close_oracle(o[rows], ref_o, "prefill sampled rows")
     assert_lse_oracle(l[rows], ref_l, _sparse_bound(sub))
+
+
+@pytest.mark.parametrize("rows,N", [(128, 8192), (8192, 8192), (128, 32768), (2048, 32768),
+                                    (8192, 32768)])
+def test_sparse_prefill_table_sampled_rows(rows, N):
+    # the library's own choice for each shape: the tensor-core kernel (split 6
+    # ways at 128 rows) where the lists cover a quarter of the cache, else the
+    # gathering kernel
+    c = W.sparse_prefill(seed=0, rows=rows, N=N)
+    o, l = run_dsa(c, prefill=True, staged=True)
+    sample = np.linspace(0, rows - 1, 16).astype(np.int64)
+    sub = dataclasses.replace(c, q=c.q[sample], idx=c.idx[sample])
+    ref_o, ref_l = oracle_dsa(sub)
+    assert_close_oracle(o[sample], ref_o, f"prefill {rows} x {N}")
+    assert_lse_oracle(l[sample], ref_l, _sparse_bound(sub))
