@@ -64,7 +64,10 @@ namespace i8kv {
 
 constexpr int kSub = 16;  // tokens per MMA tile (the M dimension of QK^T)
 
-template <int D, int NT, bool FP16C, bool PAGED>
+// SMALL: 4-warp CTAs, several per SM (the paged kernel, and the gathering
+// prefill: many units, no splits); else one CTA per SM with all the warps
+// that fit (the sparse decode's short splits).
+template <int D, int NT, bool FP16C, bool SMALL>
 struct Tile {
   static constexpr int kElem = FP16C ? 2 : 1;
   static constexpr int kRowBytes = D * kElem;        // one cache row of one KV head
@@ -88,13 +91,15 @@ struct Tile {
   static constexpr int kStages = 4 * 4 * kStageBytes <= kPerGroup ? 4
                                : (4 * 3 * kStageBytes <= kPerGroup ? 3 : 2);
   static constexpr int kWarpRing = kStages * kStageBytes;
-  // ... and the CTA shape: the sparse-candidate kernel puts them all in one
+  // ... and the CTA shape: the sparse-candidate decode puts them all in one
   // CTA per SM (4 to 16 warps: fewer, larger CTAs for its short splits); the
   // paged kernel keeps 4-warp CTAs, several per SM, so that the splits of
-  // sequences of very different lengths spread more evenly over the SMs.
+  // sequences of very different lengths spread more evenly over the SMs, and
+  // so does the gathering prefill (thousands of unsplit units: one CTA's
+  // prologue and merge overlap another's streaming).
   static constexpr int kSmemGroups = (227 * 1024 - 1024 - kQBytes - 256) / (4 * kWarpRing);
   static constexpr int kFitGroups = kSmemGroups < kRegGroups ? kSmemGroups : kRegGroups;
-  static constexpr int kGroups = PAGED ? 1 : kFitGroups;
+  static constexpr int kGroups = SMALL ? 1 : kFitGroups;
   static constexpr int kWarps = 4 * kGroups;
   static constexpr int kThreads = 32 * kWarps;
   static constexpr int kMaskBytes = kWarps * 4 * 4;
@@ -115,7 +120,7 @@ struct Tile {
   static_assert(kCopies >= 1, "copy layout");
   static_assert(kGroups >= 1 && kThreads <= 1024, "CTA shape");
   // resident CTAs per SM the launch bounds promise (the register budget)
-  static constexpr int kMinBlocks = PAGED ? kFitGroups : 1;
+  static constexpr int kMinBlocks = SMALL ? kFitGroups : 1;
   static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
@@ -498,10 +503,10 @@ static __device__ __noinline__ int4 balanced_item(const DecodeParams p, int c) {
 }
 
 template <int D, int NT, bool PAGED, bool FP16C, bool PLO, bool FP8>
-__global__ void __launch_bounds__((Tile<D, NT, FP16C, PAGED>::kThreads),
-                                  (Tile<D, NT, FP16C, PAGED>::kMinBlocks))
+__global__ void __launch_bounds__((Tile<D, NT, FP16C, PAGED || !PLO>::kThreads),
+                                  (Tile<D, NT, FP16C, PAGED || !PLO>::kMinBlocks))
 decode_kernel(const DecodeParams p) {
-  using T = Tile<D, NT, FP16C, PAGED>;
+  using T = Tile<D, NT, FP16C, PAGED || !PLO>;
   constexpr int kWarps = T::kWarps;
   constexpr int kThreads = T::kThreads;
   constexpr int KC = D / 16;  // k-chunks of QK^T and m-tiles of PV

@@ -14,7 +14,7 @@ namespace i8kv {
 
 template <int D, int NT, bool PAGED, bool FP16C, bool PLO, bool FP8>
 cudaError_t run_decode(const DecodeParams& p, cudaStream_t s, KernelInfo* info) {
-  using T = Tile<D, NT, FP16C, PAGED>;
+  using T = Tile<D, NT, FP16C, PAGED || !PLO>;
   auto kern = decode_kernel<D, NT, PAGED, FP16C, PLO, FP8>;
   // the opt-in shared-memory size is a per-function attribute: set it once per device
   static std::atomic<unsigned long long> done{0};
