@@ -298,23 +298,39 @@ __global__ void __launch_bounds__(kCvtThreads) prefill_stage_kernel(const Args a
     if (ct < 2) cnt[ct] = 0u;
     __syncthreads();
     const int32_t* list = p.idx + (long long)row * max_sel;
-    constexpr int kBatch = 8;  // list loads in flight per thread
+    // Thread ct takes kRun consecutive entries of each kRun * kCvtThreads:
+    // neighbours in a sorted list share mask words, and the entries of a run
+    // that fall in one word are ORed in with one shared-memory atomic.
+    constexpr int kRun = 8;
+    const bool vec4 = (max_sel & 3) == 0 && (reinterpret_cast<uintptr_t>(list) & 15) == 0;
     int nv = 0;
-    for (int j0 = ct; j0 < max_sel; j0 += kBatch * kCvtThreads) {
-      int tv[kBatch];
+    for (int j0 = kRun * ct; j0 < max_sel; j0 += kRun * kCvtThreads) {
+      int tv[kRun];
+      if (vec4 && j0 + kRun <= max_sel) {
+        const int4 x = __ldg(reinterpret_cast<const int4*>(list + j0));
+        const int4 y = __ldg(reinterpret_cast<const int4*>(list + j0 + 4));
+        tv[0] = x.x; tv[1] = x.y; tv[2] = x.z; tv[3] = x.w;
+        tv[4] = y.x; tv[5] = y.y; tv[6] = y.z; tv[7] = y.w;
+      } else {
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int j = j0 + u * kCvtThreads;
-        tv[u] = j < max_sel ? __ldg(list + j) : -1;
+        for (int u = 0; u < kRun; ++u) tv[u] = j0 + u < max_sel ? __ldg(list + j0 + u) : -1;
       }
+      int cw = -1;
+      uint32_t cb = 0u;
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
+      for (int u = 0; u < kRun; ++u) {
         const int t = tv[u];
         if (t >= 0 && t < N) {
-          atomicOr(rmask + (t >> 5), 1u << (t & 31));
+          if ((t >> 5) != cw) {
+            if (cb != 0u) atomicOr(rmask + cw, cb);
+            cw = t >> 5;
+            cb = 0u;
+          }
+          cb |= 1u << (t & 31);
           ++nv;
         }
       }
+      if (cb != 0u) atomicOr(rmask + cw, cb);
     }
     int nb = 0;
     __syncthreads();
