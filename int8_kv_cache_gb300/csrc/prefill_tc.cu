@@ -502,81 +502,79 @@ __global__ void __launch_bounds__(Roles<STAGED>::kThreads, 1) prefill_tc_kernel(
       }
     }
   } else {
-    {
-      // The tile's rows' lists are consecutive in memory: each thread takes
-      // every kThreads-th group of four entries of them (one 16-byte load where
-      // the lists' alignment allows, else one entry per group), kListBatch
-      // groups in flight at a time (one dependent load per entry would wait out
-      // a memory latency per kThreads entries).  A group's entries that fall in
-      // one mask word are ORed in with one shared-memory atomic.
-      constexpr int kListBatch = 8;
-      const int32_t* lists = p.idx + (long long)r_lo * p.max_sel;
-      const bool vec4 = (p.max_sel & 3) == 0 && (reinterpret_cast<uintptr_t>(lists) & 15) == 0;
-      const int per = vec4 ? 4 : 1;  // entries per group
-      int lo = INT_MAX, hi = -1;
-      auto flush = [&](int rr, int w, uint32_t bits) {
-        if (bits == 0u) return;
-        if (atomicOr(mask + rr * a.mask_words + w, bits) & bits) row_dup[rr] = 1;  // repeated
-        blk_any[w / (BN / 32)] = 1;
-      };
-      int rr = 0, j = tid * per;  // the row and list slot of this thread's next group
-      while (rr < nrows && j >= p.max_sel) {
-        j -= p.max_sel;
-        ++rr;
-      }
-      while (rr < nrows) {
-        int4 tv[kListBatch];
-        int rv[kListBatch];
-  #pragma unroll
-        for (int u = 0; u < kListBatch; ++u) {
-          rv[u] = rr;
-          tv[u] = make_int4(-1, -1, -1, -1);
-          if (rr < nrows) {
-            const int32_t* src = lists + (long long)rr * p.max_sel + j;
-            if (vec4)
-              tv[u] = __ldg(reinterpret_cast<const int4*>(src));
-            else
-              tv[u].x = __ldg(src);
-          }
-          j += kThreads * per;
-          while (rr < nrows && j >= p.max_sel) {
-            j -= p.max_sel;
-            ++rr;
-          }
+    // The tile's rows' lists are consecutive in memory: each thread takes
+    // every kThreads-th group of four entries of them (one 16-byte load where
+    // the lists' alignment allows, else one entry per group), kListBatch
+    // groups in flight at a time (one dependent load per entry would wait out
+    // a memory latency per kThreads entries).  A group's entries that fall in
+    // one mask word are ORed in with one shared-memory atomic.
+    constexpr int kListBatch = 8;
+    const int32_t* lists = p.idx + (long long)r_lo * p.max_sel;
+    const bool vec4 = (p.max_sel & 3) == 0 && (reinterpret_cast<uintptr_t>(lists) & 15) == 0;
+    const int per = vec4 ? 4 : 1;  // entries per group
+    int lo = INT_MAX, hi = -1;
+    auto flush = [&](int rr, int w, uint32_t bits) {
+      if (bits == 0u) return;
+      if (atomicOr(mask + rr * a.mask_words + w, bits) & bits) row_dup[rr] = 1;  // repeated
+      blk_any[w / (BN / 32)] = 1;
+    };
+    int rr = 0, j = tid * per;  // the row and list slot of this thread's next group
+    while (rr < nrows && j >= p.max_sel) {
+      j -= p.max_sel;
+      ++rr;
+    }
+    while (rr < nrows) {
+      int4 tv[kListBatch];
+      int rv[kListBatch];
+#pragma unroll
+      for (int u = 0; u < kListBatch; ++u) {
+        rv[u] = rr;
+        tv[u] = make_int4(-1, -1, -1, -1);
+        if (rr < nrows) {
+          const int32_t* src = lists + (long long)rr * p.max_sel + j;
+          if (vec4)
+            tv[u] = __ldg(reinterpret_cast<const int4*>(src));
+          else
+            tv[u].x = __ldg(src);
         }
-  #pragma unroll
-        for (int u = 0; u < kListBatch; ++u) {
-          if (rv[u] >= nrows) continue;
-          const int te[4] = {tv[u].x, tv[u].y, tv[u].z, tv[u].w};
-          int cw = -1;
-          uint32_t cb = 0u;
-  #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int t = te[e];
-            if (t < 0 || t >= N) continue;
-            const uint32_t bit = 1u << (t & 31);
-            if ((t >> 5) != cw) {
-              flush(rv[u], cw, cb);
-              cw = t >> 5;
-              cb = 0u;
-            }
-            if (cb & bit) row_dup[rv[u]] = 1;  // repeated within the group
-            cb |= bit;
-            lo = min(lo, t);
-            hi = max(hi, t);
-          }
-          flush(rv[u], cw, cb);
+        j += kThreads * per;
+        while (rr < nrows && j >= p.max_sel) {
+          j -= p.max_sel;
+          ++rr;
         }
       }
-  #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+#pragma unroll
+      for (int u = 0; u < kListBatch; ++u) {
+        if (rv[u] >= nrows) continue;
+        const int te[4] = {tv[u].x, tv[u].y, tv[u].z, tv[u].w};
+        int cw = -1;
+        uint32_t cb = 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = te[e];
+          if (t < 0 || t >= N) continue;
+          const uint32_t bit = 1u << (t & 31);
+          if ((t >> 5) != cw) {
+            flush(rv[u], cw, cb);
+            cw = t >> 5;
+            cb = 0u;
+          }
+          if (cb & bit) row_dup[rv[u]] = 1;  // repeated within the group
+          cb |= bit;
+          lo = min(lo, t);
+          hi = max(hi, t);
+        }
+        flush(rv[u], cw, cb);
       }
-      if (lane == 0 && hi >= 0) {
-        atomicMin(slot_rw + kPMin, lo);
-        atomicMax(slot_rw + kPMax, hi);
-      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lane == 0 && hi >= 0) {
+      atomicMin(slot_rw + kPMin, lo);
+      atomicMax(slot_rw + kPMax, hi);
     }
     cp_async_wait_all();  // the raw query rows
   }
