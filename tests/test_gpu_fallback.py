@@ -168,3 +168,30 @@ def test_large_value_scales_with_deep_candidates(K):
     vsc = np.repeat(c.v_scale[None, :, None, None, :].astype(np.float64), 4, axis=0)
     vsc = np.broadcast_to(vsc.reshape(4, 2, 1, 1, 256), (4, 2, ns, 8, 256)).reshape(8, ns, 8, 256)
     assert np.max(np.abs(on - rn) / (127 * vsc)) < 2e-3
+
+
+@pytest.mark.parametrize("kw", [dict(num_splits=1, chunk=512), dict(num_splits=4, chunk=128),
+                                dict(prefill=True), dict(prefill=True, staged=True, num_splits=1),
+                                dict(prefill=True, staged=True, num_splits=3)],
+                         ids=["decode-1", "decode-4", "prefill", "prefill-staged",
+                              "prefill-staged-3"])
+def test_non_finite_value_scale_takes_the_fp32_path(K, kw):
+    """One channel of KV head 1 has value scale +inf: that head's CTAs take
+    the FP32 path (its output channel is not finite, as the FP64 result is
+    not), and every other output and every lse still match the oracle."""
+    c = W.random_sparse(seed=71, S=6, Hq=24, Hkv=2, D=256, N=900, max_sel=300, sink=True,
+                        sigma=1.0 / 16)
+    assert c.scale_kind == W.SCALE_PER_CHANNEL
+    c.v_scale = c.v_scale.copy()
+    c.v_scale[1, 5] = np.inf
+    with np.errstate(invalid="ignore"):
+        ref_o, ref_l = oracle_dsa(c)
+    f = _flags()
+    o, l = run_dsa(c, flags=f, **kw)
+    assert int(f.item()) & FP32_PATH, kw
+    bad = np.zeros(o.shape, bool)
+    bad[:, 12:, 5] = True
+    assert not np.isfinite(ref_o[bad]).any()
+    assert not np.isfinite(o[bad]).any(), kw
+    assert np.all(np.abs(o[~bad] - ref_o[~bad]) <= 2e-3 + 1e-2 * np.abs(ref_o[~bad])), kw
+    assert_lse_close(l, ref_l, 1e-4)
