@@ -157,8 +157,8 @@ i8kv_status prefill_splits(int32_t S, int32_t G, int32_t Hkv, int32_t num_splits
   return I8KV_OK;
 }
 
-// The staged prefill's workspace: the operand images, then (with splits) the
-// partials at the next 256-byte boundary.
+// The staged prefill's workspace: the operand images and the rows' bitmasks,
+// then (with splits) the partials at the next 256-byte boundary.
 size_t prefill_ws_bytes(int32_t S, int32_t Hq, int32_t Hkv, int32_t D, int64_t N, int ns) {
   const size_t stage = i8kv::prefill_stage_bytes(N, Hkv, D, S);
   if (ns <= 1) return stage;
@@ -458,10 +458,10 @@ i8kv_status dsa_prefill_ws(const uint16_t* q, const int8_t* k_cache, const int8_
   // gathering mma.sync kernel
   int smem = 0, mask_rows = 0;
   if (i8kv::prefill_tc_plan(D, p.G, S, N, max_sel, &smem, &mask_rows)) {
-    // with a workspace: the staged form (fp16 operand images made once per
-    // call, copied in by one thread), its tiles' blocks split over several
-    // CTAs where the tiles alone leave SMs idle; without: the converting form,
-    // unsplit
+    // with a workspace: the staged form (fp16 operand images and the rows'
+    // bitmasks made once per call, the images copied in by one thread), its
+    // tiles' blocks split over several CTAs where the tiles alone leave SMs
+    // idle; without: the converting form, unsplit
     void* stage = nullptr;
     int ns = 1;
     float* part = nullptr;
