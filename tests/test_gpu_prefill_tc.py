@@ -288,3 +288,24 @@ def test_split_prefill_can_be_captured_and_replayed():
     assert torch.equal(out, eager)
     ref_o, _ = oracle_dsa(c)
     assert_close_oracle(out.float().cpu().numpy().astype(np.float64), ref_o, "captured splits")
+
+
+@pytest.mark.parametrize("form", [(False, 0), (True, 1), (True, 4)],
+                         ids=["converting", "staged-unsplit", "staged-4"])
+def test_tiles_whose_rows_attend_nothing(form):
+    # every list entry invalid in the first 20 rows (whole tiles of both KV
+    # heads with no selected block) and in row 31: O = 0, lse = -inf there,
+    # the other rows as the oracle
+    c = W.random_sparse(seed=41, S=40, Hq=24, Hkv=2, D=256, N=600, max_sel=256, sink=True,
+                        sigma=1.0 / 16)
+    c.idx[:20] = -1
+    c.idx[31] = 600 + np.arange(256)
+    ref_o, ref_l = oracle_dsa(c)
+    o, l, f = _run(c, form)
+    assert not f & WAIT_TIMEOUT
+    dead = np.zeros(40, bool)
+    dead[:20] = True
+    dead[31] = True
+    assert np.all(o[dead] == 0) and np.all(np.isneginf(l[dead]))
+    assert_close_oracle(o[~dead], ref_o[~dead], "live rows")
+    assert_lse_close(l[~dead], ref_l[~dead], 1e-4)
