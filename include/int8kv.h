@@ -236,6 +236,16 @@ size_t dsa_prefill_workspace_bytes(int32_t S, int32_t Hq, int32_t Hkv, int32_t D
                                    int32_t max_sel, int32_t num_splits);
 
 /*
+ * dsa_prefill_auto_splits -- the automatic split count of the tensor-core
+ * prefill (num_splits = 0) on a device with `sms` SMs: with tiles = Hkv x
+ * ceil(S x (Hq / Hkv) / 128) tiles of 128 (row, head) vectors, min(8, sms /
+ * tiles) where 2 x tiles <= sms, else 1 (a split's partials cost a round trip
+ * through the combine kernel, paid back only where tiles leave SMs idle).
+ * 0 for S < 1, sms < 1 or bad heads.  Host arithmetic only.
+ */
+int32_t dsa_prefill_auto_splits(int32_t S, int32_t Hq, int32_t Hkv, int32_t sms);
+
+/*
  * dsa_prefill_ws -- dsa_prefill with an optional workspace (the caller's device
  * memory, 16-byte aligned, workspace_bytes >= dsa_prefill_workspace_bytes for
  * the same num_splits).  With one, where the tensor-core kernel serves the

@@ -72,6 +72,7 @@ _SIGNATURES = {
                              _c_vp]),
     "dsa_prefill_workspace_bytes": (_c_sz, [_c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_i32,
                                             _c_i32]),
+    "dsa_prefill_auto_splits": (_c_i32, [_c_i32, _c_i32, _c_i32, _c_i32]),
     "dsa_prefill_ws": (_c_i32, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i32, _c_vp, _c_i32, _c_i32,
                                 _c_i32, _c_i32, _c_i64, _c_i32, _c_f32, _c_vp, _c_i32, _c_vp,
                                 _c_sz, _c_vp, _c_vp, _c_vp, _c_vp]),

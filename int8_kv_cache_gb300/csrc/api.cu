@@ -425,6 +425,11 @@ i8kv_status dsa_prefill(const uint16_t* q, const int8_t* k_cache, const int8_t* 
                         max_sel, softmax_scale, head_sink, 0, nullptr, 0, out, lse, flags, stream);
 }
 
+int32_t dsa_prefill_auto_splits(int32_t S, int32_t Hq, int32_t Hkv, int32_t sms) {
+  if (S < 1 || sms < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return 0;
+  return i8kv::prefill_auto_splits(S, Hq / Hkv, Hkv, sms);
+}
+
 size_t dsa_prefill_workspace_bytes(int32_t S, int32_t Hq, int32_t Hkv, int32_t D, int64_t N,
                                    int32_t max_sel, int32_t num_splits) {
   if (S < 1 || N < 1 || max_sel < 1 || check_heads(Hq, Hkv, D) != I8KV_OK) return 0;

@@ -224,6 +224,26 @@ def test_prefill_workspace_rules(lib):
     assert need(16, 24, 5, 256, 300, 100, 1) == 0    # Hq not a multiple of Hkv
 
 
+def test_prefill_auto_split_rule(lib):
+    # host arithmetic: tiles = Hkv x ceil(S x G / 128); min(8, SMs / tiles)
+    # splits where the tiles fill at most half of the SMs, else 1
+    auto = lib.dsa_prefill_auto_splits
+    assert auto(128, 24, 2, 152) == 6        # 24 tiles
+    assert auto(2048, 24, 2, 152) == 1       # 384 tiles
+    assert auto(512, 24, 2, 152) == 1        # 96 tiles: more than half the SMs
+    assert auto(256, 24, 2, 152) == 3        # 48 tiles
+    assert auto(16, 24, 2, 152) == 8         # 4 tiles: at most 8 splits
+    assert auto(1, 2, 2, 152) == 8           # G = 1: one tile per KV head
+    assert auto(640, 16, 1, 152) == 1        # 80 tiles
+    assert auto(608, 16, 1, 152) == 2        # 76 tiles: exactly half
+    for S in range(1, 3000, 37):
+        for G, Hkv in ((12, 2), (16, 1), (1, 8), (4, 4)):
+            tiles = Hkv * -(-S * G // 128)
+            want = min(8, 152 // tiles) if 2 * tiles <= 152 else 1
+            assert auto(S, G * Hkv, Hkv, 152) == want, (S, G, Hkv)
+    assert auto(0, 24, 2, 152) == 0 and auto(16, 24, 2, 0) == 0 and auto(16, 24, 5, 152) == 0
+
+
 def test_prefill_workspace_errors_before_any_launch(lib):
     # checked before anything touches the device: the addresses are never read
     fake = 1 << 20
