@@ -18,8 +18,9 @@ __all__ = [
 ]
 from .attention import scores, window_chunk_bounds, window_span, window_start  # noqa: E402
 from .attention import e4m3fn_value  # noqa: E402
+from .attention import prefill_block_ranges, prefill_split_partials  # noqa: E402
 from .quantize import e4m3fn_encode, quantize_rows, quantize_rows_fp8, reshape_and_cache  # noqa
 
 __all__ += ["quantize_rows", "reshape_and_cache", "e4m3fn_value", "e4m3fn_encode",
             "quantize_rows_fp8", "scores", "window_chunk_bounds",
-            "window_span", "window_start"]
+            "window_span", "window_start", "prefill_block_ranges", "prefill_split_partials"]

@@ -319,6 +319,67 @@ def sparse_split_partials(q, k_codes, v_codes, k_scale, v_scale, scale_kind, idx
     return m, l, a
 
 
+def prefill_block_ranges(idx, N: int, G: int, num_splits: int, tile: int = 128,
+                         block: int = 128) -> List[List[Tuple[int, int]]]:
+    """Position ranges of the split tensor-core prefill (reading 13 of the
+    design: the pages' prefill has no splits; this is the split-K partial and
+    merge of PR 33707 §2 applied to a tile's blocks).  Query vectors r*G + j
+    of one KV head form tiles of `tile` consecutive vectors; a tile's blocks
+    are the `block`-position blocks holding a valid candidate of any of its
+    rows, ranked in position order; split k takes ranks
+    [k*cnt // num_splits, (k+1)*cnt // num_splits) and the positions from its
+    first block to the next split's first block (split 0 from 0, the last split
+    to N; a rank past the last block stands for the block after the tile's
+    last one).  Returns, per tile, the num_splits (lo, hi) ranges."""
+    S = idx.shape[0]
+    nvec = S * G
+    out = []
+    for t in range(-(-nvec // tile)):
+        r_lo = (t * tile) // G
+        r_hi = (min(t * tile + tile - 1, nvec - 1)) // G
+        pos = np.concatenate([sparse_candidates(idx[r], N) for r in range(r_lo, r_hi + 1)])
+        blocks = sorted(set((pos // block).tolist()))
+        cnt = len(blocks)
+        past = (blocks[-1] + 1) if cnt else 0
+        first = lambda rank: blocks[rank] if rank < cnt else past  # noqa: E731
+        ranges = []
+        for k in range(num_splits):
+            r0, r1 = k * cnt // num_splits, (k + 1) * cnt // num_splits
+            lo = 0 if k == 0 else first(r0) * block
+            hi = N if k == num_splits - 1 else first(r1) * block
+            ranges.append((lo, hi))
+        out.append(ranges)
+    return out
+
+
+def prefill_split_partials(q, k_codes, v_codes, k_scale, v_scale, scale_kind, idx, sigma,
+                           num_splits: int, tile: int = 128, block: int = 128):
+    """Partials of the split tensor-core prefill: vector (r, h) of KV head g
+    lies in tile (r*G + h - g*G) // tile of that head, and its split k covers
+    the candidates of row r at the positions of that tile's range k
+    (prefill_block_ranges).  Returns m, l [S, Hq, splits] and acc
+    [S, Hq, splits, D] (float64)."""
+    S, Hq, D = q.shape
+    N, Hkv, _ = k_codes.shape
+    G = Hq // Hkv
+    ranges = prefill_block_ranges(idx, N, G, num_splits, tile, block)
+    m = np.full((S, Hq, num_splits), -math.inf)
+    l = np.zeros((S, Hq, num_splits))
+    a = np.zeros((S, Hq, num_splits, D))
+    for r in range(S):
+        cand = sparse_candidates(idx[r], N)
+        for j in range(G):
+            t = (r * G + j) // tile
+            for k, (lo, hi) in enumerate(ranges[t]):
+                rows = cand[(cand >= lo) & (cand < hi)]
+                for g in range(Hkv):
+                    K = dequantize(k_codes[rows, g, :], k_scale, scale_kind, g)
+                    V = dequantize(v_codes[rows, g, :], v_scale, scale_kind, g)
+                    h = g * G + j
+                    m[r, h, k], l[r, h, k], a[r, h, k] = partial(q[r, h], K, V, sigma)
+    return m, l, a
+
+
 def window_chunk_bounds(L: int, window: int, chunk: int,
                         num_splits: int) -> List[Tuple[int, int]]:
     """Split k of a windowed row covers [b16 + k*chunk, b16 + (k+1)*chunk)

@@ -309,3 +309,52 @@ def test_tiles_whose_rows_attend_nothing(form):
     assert np.all(o[dead] == 0) and np.all(np.isneginf(l[dead]))
     assert_close_oracle(o[~dead], ref_o[~dead], "live rows")
     assert_lse_close(l[~dead], ref_l[~dead], 1e-4)
+
+
+@pytest.mark.parametrize("S,Hq,Hkv,D,N,max_sel,ns", [
+    (37, 24, 2, 256, 700, 400, 3),   # tiles straddle rows; a partial last tile
+    (3, 2, 2, 256, 500, 200, 4),     # G = 1: one tile spans every row
+    (20, 8, 2, 128, 1000, 300, 5),
+    (9, 12, 1, 256, 256, 64, 8),     # two blocks: most splits get none
+])
+def test_split_partials_match_the_oracle(S, Hq, Hkv, D, N, max_sel, ns):
+    # each split CTA's published partial (the workspace after the images and
+    # the row masks, in the decode's partial layout) against the oracle's
+    # partial over the same position range: same emptiness, lse per split
+    # within the query-rounding bound, normalised accumulators within the
+    # output tolerance
+    import oracle
+    import int8_kv_cache_gb300 as K
+    from helpers import sparse_to_device
+    c = W.random_sparse(seed=S * 5 + ns, S=S, Hq=Hq, Hkv=Hkv, D=D, N=N, max_sel=max_sel,
+                        invalid_frac=0.1, sigma=1.0 / 16)
+    G = Hq // Hkv
+    d = sparse_to_device(c)
+    wsb = K.prefill_workspace_bytes(S, Hq, Hkv, D, N, max_sel, ns)
+    ws = torch.full((wsb,), 255, dtype=torch.uint8, device="cuda")
+    K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"], c.sigma,
+                  out=torch.empty_like(d["q"]), workspace=ws, num_splits=ns)
+    torch.cuda.synchronize()
+    blocks = -(-N // 128)
+    stage = Hkv * blocks * 2 * 128 * D * 2 + S * blocks * 16 + S * 4
+    off = (stage + 255) // 256 * 256
+    pvec = S * Hq * ns
+    f = ws[off:off + pvec * (D + 2) * 4].view(torch.float32).cpu().numpy().astype(np.float64)
+    acc = f[:pvec * D].reshape(S, Hkv, ns, G, D)
+    m = f[pvec * D:pvec * (D + 1)].reshape(S, Hkv, ns, G)
+    l = f[pvec * (D + 1):].reshape(S, Hkv, ns, G)
+    rm, rl, ra = oracle.prefill_split_partials(c.q, c.k_codes, c.v_codes, c.k_scale, c.v_scale,
+                                               c.scale_kind, c.idx, c.sigma, ns)
+    rm = rm.reshape(S, Hkv, G, ns).transpose(0, 1, 3, 2)
+    rl = rl.reshape(S, Hkv, G, ns).transpose(0, 1, 3, 2)
+    ra = ra.reshape(S, Hkv, G, ns, D).transpose(0, 1, 3, 2, 4)
+    live = rl > 0
+    assert np.array_equal(l > 0, live)
+    assert np.all(np.isneginf(m[~live]))
+    bnd = np.broadcast_to(bound_of(c).reshape(S, Hkv, 1, G), (S, Hkv, ns, G))
+    lse = m[live] + np.log(l[live])
+    ref = rm[live] + np.log(rl[live])
+    assert np.all(np.abs(lse - ref) <= bnd[live] + 1e-5 * np.abs(ref))
+    on = acc[live] / l[live][:, None]
+    rn = ra[live] / rl[live][:, None]
+    assert np.all(np.abs(on - rn) <= 2e-3 + 1e-2 * np.abs(rn))

@@ -299,6 +299,48 @@ def test_sparse_split_form_matches_whole(chunk):
     np.testing.assert_allclose(L, L2, rtol=1e-13)
 
 
+@pytest.mark.parametrize("ns,tile,G", [(1, 8, 4), (2, 8, 4), (3, 8, 4), (5, 8, 4), (4, 3, 1),
+                                       (7, 6, 2)])
+def test_prefill_block_split_form_matches_whole(ns, tile, G):
+    # the split prefill's ranges (small tiles and 8-position blocks so that
+    # tiles straddle rows and splits get one block, several or none) cover
+    # [0, N) once per tile, and the merge of the partials is the whole
+    Hkv = 2
+    c = W.random_sparse(seed=40 + ns + tile, S=7, Hq=G * Hkv, Hkv=Hkv, D=8, N=61, max_sel=19,
+                        invalid_frac=0.2, sink=True)
+    c.idx[3, 5] = c.idx[3, 2]  # a repeated entry counts twice in its split
+    c.idx[5, :] = -1            # a row with nothing
+    for ranges in oracle.prefill_block_ranges(c.idx, 61, G, ns, tile=tile, block=8):
+        assert len(ranges) == ns and ranges[0][0] == 0 and ranges[-1][1] == 61
+        assert all(ranges[k][1] == ranges[k + 1][0] for k in range(ns - 1))
+        assert all(lo <= hi for lo, hi in ranges)
+    m, l, a = oracle.prefill_split_partials(c.q, c.k_codes, c.v_codes, c.k_scale, c.v_scale,
+                                            c.scale_kind, c.idx, c.sigma, ns, tile=tile,
+                                            block=8)
+    O, L = oracle.combine_all(m, l, a, c.sink)
+    O2, L2 = oracle.sparse_attention(c.q, c.k_codes, c.v_codes, c.k_scale, c.v_scale,
+                                     c.scale_kind, c.idx, c.sigma, c.sink)
+    np.testing.assert_allclose(O, O2, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(L, L2, rtol=1e-13)
+    assert np.all(np.isneginf(m[5])) and np.all(l[5] == 0)
+
+
+def test_prefill_block_ranges_by_hand():
+    # one tile (G = 2, three rows), 8-position blocks: the rows' candidates sit
+    # in blocks 0, 2, 3 and 6, so 3 splits take ranks [0, 1), [1, 2), [2, 4)
+    idx = np.array([[1, 17, -1], [20, 25, 99], [50, 3, 18]], np.int32)
+    (ranges,) = oracle.prefill_block_ranges(idx, 60, 2, 3, tile=8, block=8)
+    assert ranges == [(0, 16), (16, 24), (24, 60)]
+    # more splits than blocks: ranks [0,0) [0,1) [1,2) [2,2) [2,3) [3,4); the
+    # splits with no rank get empty ranges
+    (ranges,) = oracle.prefill_block_ranges(idx, 60, 2, 6, tile=8, block=8)
+    assert ranges == [(0, 0), (0, 16), (16, 24), (24, 24), (24, 48), (48, 60)]
+    # no candidate at all: every range empty but the last, which is [0, N)
+    (ranges,) = oracle.prefill_block_ranges(np.full((3, 3), -1, np.int32), 60, 2, 3, tile=8,
+                                            block=8)
+    assert ranges == [(0, 0), (0, 0), (0, 60)]
+
+
 @pytest.mark.parametrize("chunk,ns", [(2, 12), (4, 6), (16, 2), (32, 1), (4, 9)])
 def test_paged_split_form_matches_whole(chunk, ns):
     c = W.random_paged(seed=7, B=4, Hq=4, Hkv=2, D=8, bs=2, max_blocks=12, lens=[0, 5, 24, 30],
