@@ -96,7 +96,8 @@ typedef enum {
 /* Human-readable name of a status code (static storage). */
 const char* i8kv_status_string(int status);
 
-/* Library ABI version (major*100 + minor). */
+/* Library ABI version (major*100 + minor).  3.0: dsa_prefill_ws and
+ * dsa_prefill_workspace_bytes take num_splits; dsa_prefill_auto_splits. */
 int32_t i8kv_version(void);
 
 /* The cudaError_t value behind the calling thread's most recent I8KV_ECUDA

@@ -298,7 +298,7 @@ const char* i8kv_status_string(int status) {
   }
 }
 
-int32_t i8kv_version(void) { return 200; }
+int32_t i8kv_version(void) { return 300; }
 
 // The CUDA error code behind the calling thread's last I8KV_ECUDA (0 if none).
 int32_t i8kv_last_cuda_error(void) { return g_last_cuda_error; }
