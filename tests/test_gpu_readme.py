@@ -1,5 +1,6 @@
 """The usage example in README.md runs as written (sparse decode, paged decode
-with a head sink, quantize-on-write) and gives finite outputs."""
+with a head sink, quantize-on-write, the staged prefill) and gives finite
+outputs."""
 import os
 import re
 
@@ -21,3 +22,5 @@ def test_readme_example_runs():
     torch.cuda.synchronize()
     assert ns["out"].shape == (16, 32, 128)
     assert bool(torch.isfinite(ns["out"].float()).all())
+    assert ns["out_p"].shape == (2048, 24, 256)
+    assert bool(torch.isfinite(ns["out_p"].float()).all())
