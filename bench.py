@@ -848,44 +848,48 @@ def _prefill(torch, K, W, np, t, bench_graph, peaks, dev, stream):
 def _prefill_table(torch, K, W, np, t, bench_graph, peaks):
     """Sparse prefill at the pages' row counts and contexts (128 / 2048 / 8192
     rows, the last rows of an 8192- or 32768-token cache, 2048 candidates per
-    row, 24/2 heads, head_dim 256).  Each call runs the path the library picks:
+    row, 24/2 heads, head_dim 256), and the literal reading of the configured
+    workload (row i of 2048 at position i of an 8192-token cache, min(2048,
+    i + 1) candidates).  Each call runs the path the library picks:
     the tensor-core kernel over dense blocks (staged form, with a workspace)
     where the lists cover at least a quarter of the cache, else the gathering
     kernel."""
     rows_out = []
     peak_tf = peaks["bf16_tflops"]
-    for ctx in (8192, 32768):
-        for rows in (128, 2048, 8192):
-            c = W.sparse_prefill(seed=0, rows=rows, N=ctx)
-            d = dict(q=t(c.q), k=t(c.k_codes), v=t(c.v_codes), ks=t(c.k_scale),
-                     vs=t(c.v_scale), idx=t(c.idx))
-            out = torch.empty_like(d["q"])
-            S, Hq, Dh = c.q.shape
-            N, Hkv, _ = c.k_codes.shape
-            wsb = K.prefill_workspace_bytes(S, Hq, Hkv, Dh, N, c.idx.shape[1])
-            ws = torch.empty(wsb, dtype=torch.uint8, device=d["q"].device) if wsb else None
+    shapes = [(rows, ctx, False) for ctx in (8192, 32768) for rows in (128, 2048, 8192)]
+    shapes.append((2048, 8192, True))  # the literal reading: row i at position i
+    for rows, ctx, literal in shapes:
+        c = W.sparse_prefill(seed=0, rows=rows, N=ctx, literal=literal)
+        d = dict(q=t(c.q), k=t(c.k_codes), v=t(c.v_codes), ks=t(c.k_scale),
+                 vs=t(c.v_scale), idx=t(c.idx))
+        out = torch.empty_like(d["q"])
+        S, Hq, Dh = c.q.shape
+        N, Hkv, _ = c.k_codes.shape
+        wsb = K.prefill_workspace_bytes(S, Hq, Hkv, Dh, N, c.idx.shape[1])
+        ws = torch.empty(wsb, dtype=torch.uint8, device=d["q"].device) if wsb else None
 
-            def fn():
-                K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"],
-                              c.sigma, out=out, workspace=ws)
-            sec = bench_graph(fn, 1, reps=5 if rows > 2048 else 10)
-            flops = int((c.idx >= 0).sum()) * Hq * Dh * 4
-            # the automatic split count, from the workspace it asked for
-            stage = Hkv * ((N + 127) // 128) * 2 * 128 * Dh * 2 + S * ((N + 127) // 128) * 16 + S * 4
-            splits = 1 if wsb <= stage else \
-                (wsb - (stage + 255) // 256 * 256) // (S * Hq * (Dh + 2) * 4)
-            rows_out.append(dict(
-                rows=rows, context=ctx,
-                kernel=(f"prefill_tc_kernel<256, staged> (tcgen05), {splits} split(s)" +
-                        (" + combine_kernel<256>" if splits > 1 else "")) if wsb else
-                       "decode_kernel<256, sparse, int8, one probability tile> (mma.sync, "
-                       "gathered rows, no splits)",
-                ms_per_call=round(sec * 1e3, 4), tflops=round(flops / sec / 1e12, 2),
-                frac_of_tensor=round(flops / sec / 1e12 / peak_tf, 4)))
-            del d, out, ws
-    return dict(workload="sparse prefill, rows at positions N - rows + i of an N-token int8 "
-                         "cache, 2048 sorted unique candidates per row from [0, position], "
-                         "24/2 heads, head_dim 256, per-channel scales, softmax scale 1/16",
+        def fn():
+            K.dsa_prefill(d["q"], d["k"], d["v"], d["ks"], d["vs"], c.scale_kind, d["idx"],
+                          c.sigma, out=out, workspace=ws)
+        sec = bench_graph(fn, 1, reps=5 if rows > 2048 else 10)
+        flops = int((c.idx >= 0).sum()) * Hq * Dh * 4
+        # the automatic split count, from the workspace it asked for
+        stage = Hkv * ((N + 127) // 128) * 2 * 128 * Dh * 2 + S * ((N + 127) // 128) * 16 + S * 4
+        splits = 1 if wsb <= stage else \
+            (wsb - (stage + 255) // 256 * 256) // (S * Hq * (Dh + 2) * 4)
+        rows_out.append(dict(
+            rows=rows, context=ctx, positions="i" if literal else f"{ctx - rows} + i",
+            kernel=(f"prefill_tc_kernel<256, staged> (tcgen05), {splits} split(s)" +
+                    (" + combine_kernel<256>" if splits > 1 else "")) if wsb else
+                   "decode_kernel<256, sparse, int8, one probability tile> (mma.sync, "
+                   "gathered rows, no splits)",
+            ms_per_call=round(sec * 1e3, 4), tflops=round(flops / sec / 1e12, 2),
+            frac_of_tensor=round(flops / sec / 1e12 / peak_tf, 4)))
+        del d, out, ws
+    return dict(workload="sparse prefill, rows at positions N - rows + i (and, last, row i at "
+                         "position i) of an N-token int8 cache, min(2048, position + 1) sorted "
+                         "unique candidates per row from [0, position], 24/2 heads, head_dim "
+                         "256, per-channel scales, softmax scale 1/16",
                 tensor_peak=peak_tf, cases=rows_out)
 
 

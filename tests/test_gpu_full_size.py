@@ -95,13 +95,14 @@ def test_sparse_prefill_full_size_sampled_rows(staged):
     assert_lse_oracle(l[rows], ref_l, _sparse_bound(sub))
 
 
-@pytest.mark.parametrize("rows,N", [(128, 8192), (8192, 8192), (128, 32768), (2048, 32768),
-                                    (8192, 32768)])
-def test_sparse_prefill_table_sampled_rows(rows, N):
+@pytest.mark.parametrize("rows,N,literal", [(128, 8192, False), (8192, 8192, False),
+                                            (128, 32768, False), (2048, 32768, False),
+                                            (8192, 32768, False), (2048, 8192, True)])
+def test_sparse_prefill_table_sampled_rows(rows, N, literal):
     # the library's own choice for each shape: the tensor-core kernel (split 6
     # ways at 128 rows) where the lists cover a quarter of the cache, else the
-    # gathering kernel
-    c = W.sparse_prefill(seed=0, rows=rows, N=N)
+    # gathering kernel; and the literal reading (row i at position i)
+    c = W.sparse_prefill(seed=0, rows=rows, N=N, literal=literal)
     o, l = run_dsa(c, prefill=True, staged=True)
     sample = np.linspace(0, rows - 1, 16).astype(np.int64)
     sub = dataclasses.replace(c, q=c.q[sample], idx=c.idx[sample])
